@@ -1,0 +1,337 @@
+"""Pins for the fp64 oracle, each against something other than the oracle itself.
+
+Sources are the pages' definitions ("Attention Kernel 계보": p.2 §1 attention,
+p.3 §2-§9 softmax passes and LSE, p.4 merge, p.13 causal mask, p.15 GQA head
+map), closed forms derived by hand (``tests/golden/closed_form.json``),
+invariants of softmax, and an independent brute force in decimal arithmetic.
+Each pin is chosen so that a plausible slip in the oracle (dropped m in LSE,
+wrong head map, off-by-one causal bound, missing scale, transposed operand,
+lost merge factor) fails at least one of them.
+"""
+import decimal
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from gqa_attention_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_form.json")
+TOL = 1e-12
+
+
+def _ev(expr):
+    return float(eval(str(expr), {"__builtins__": {}}, {"ln": math.log, "nan": math.nan,
+                                                          "inf": math.inf}))
+
+
+def _arr(nested):
+    if isinstance(nested, list):
+        return np.array([_arr(x) for x in nested], dtype=np.float64)
+    return _ev(nested)
+
+
+def _rand(shape, rng, scale=1.0):
+    return rng.standard_normal(shape) * scale
+
+
+# ---------------------------------------------------------------- golden ---
+def _golden_cases():
+    with open(GOLDEN) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: c["name"])
+def test_golden_closed_forms(oracle_mod, case):
+    if case["kind"] == "merge":
+        out, lse = oracle_mod.merge_partials(_arr(case["m"]), _arr(case["l"]), _arr(case["O"]))
+    elif case["kind"] == "decode":
+        out, lse = oracle_mod.decode(_arr(case["q"]), _arr(case["k"]), _arr(case["v"]),
+                                     case["seq_lens"], _ev(case["scale"]))
+    else:
+        out, lse = oracle_mod.prefill_causal_rows(_arr(case["q"]), _arr(case["k"]),
+                                                  _arr(case["v"]), _ev(case["scale"]))
+    np.testing.assert_allclose(out, _arr(case["out"]), rtol=TOL, atol=TOL)
+    np.testing.assert_allclose(lse, _arr(case["lse"]), rtol=TOL, atol=TOL)
+
+
+# ----------------------------------------------------------- closed forms ---
+def test_single_key_returns_that_value(oracle_mod):
+    rng = np.random.default_rng(1)
+    B, H_q, H_kv, d, S = 2, 6, 3, 16, 5
+    q, k, v = _rand((B, H_q, d), rng), _rand((B, S, H_kv, d), rng), _rand((B, S, H_kv, d), rng)
+    tau = 0.3
+    out, lse = oracle_mod.decode(q, k, v, [1, 1], tau)
+    G = H_q // H_kv
+    for b in range(B):
+        for h in range(H_q):
+            np.testing.assert_allclose(out[b, h], v[b, 0, h // G], rtol=0, atol=1e-13)
+            assert lse[b, h] == pytest.approx(tau * q[b, h] @ k[b, 0, h // G], abs=1e-13)
+
+
+def test_identical_keys_give_mean_of_values(oracle_mod):
+    rng = np.random.default_rng(2)
+    B, H_q, H_kv, d, S = 1, 4, 2, 8, 37
+    q = _rand((B, H_q, d), rng)
+    k = np.broadcast_to(_rand((B, 1, H_kv, d), rng), (B, S, H_kv, d)).copy()
+    v = _rand((B, S, H_kv, d), rng)
+    tau = 1 / math.sqrt(d)
+    out, lse = oracle_mod.decode(q, k, v, [S], tau)
+    for h in range(H_q):
+        kv = h // 2
+        np.testing.assert_allclose(out[0, h], v[0, :, kv].mean(axis=0), atol=1e-13)
+        assert lse[0, h] == pytest.approx(tau * q[0, h] @ k[0, 0, kv] + math.log(S), abs=1e-12)
+
+
+def test_zero_query_is_uniform_over_visible_keys(oracle_mod):
+    rng = np.random.default_rng(3)
+    B, S, H_q, H_kv, d = 2, 23, 4, 1, 8
+    q = np.zeros((B, S, H_q, d))
+    k, v = _rand((B, S, H_kv, d), rng), _rand((B, S, H_kv, d), rng)
+    out, lse = oracle_mod.prefill_causal_rows(q, k, v, 0.7)
+    for i in range(S):
+        np.testing.assert_allclose(out[:, i, :, :], np.broadcast_to(
+            v[:, : i + 1, 0, :].mean(axis=1)[:, None, :], (B, H_q, d)), atol=1e-13)
+        np.testing.assert_allclose(lse[:, :, i], math.log(i + 1), atol=1e-13)
+    # decode: LSE = ln L_b and O = mean of the first L_b values
+    qd = np.zeros((B, H_q, d))
+    out, lse = oracle_mod.decode(qd, k, v, [5, 23], 0.7)
+    np.testing.assert_allclose(lse[0], math.log(5), atol=1e-13)
+    np.testing.assert_allclose(lse[1], math.log(23), atol=1e-13)
+    np.testing.assert_allclose(out[1, 2], v[1, :, 0].mean(axis=0), atol=1e-13)
+
+
+def test_causal_row_zero_is_first_value(oracle_mod):
+    rng = np.random.default_rng(4)
+    B, S, H_q, H_kv, d = 1, 9, 8, 2, 16
+    q, k, v = (_rand((B, S, H_q, d), rng), _rand((B, S, H_kv, d), rng),
+               _rand((B, S, H_kv, d), rng))
+    out, lse = oracle_mod.prefill_causal_rows(q, k, v, 0.25, rows=[0])
+    for h in range(H_q):
+        np.testing.assert_allclose(out[0, 0, h], v[0, 0, h // 4], atol=1e-14)
+        assert lse[0, h, 0] == pytest.approx(0.25 * q[0, 0, h] @ k[0, 0, h // 4], abs=1e-13)
+
+
+# ------------------------------------------------------------- invariants ---
+def test_gqa_equals_mha_with_repeated_kv_heads(oracle_mod):
+    rng = np.random.default_rng(5)
+    B, S, H_q, H_kv, d = 2, 19, 12, 3, 8
+    G = H_q // H_kv
+    q, k, v = (_rand((B, S, H_q, d), rng), _rand((B, S, H_kv, d), rng),
+               _rand((B, S, H_kv, d), rng))
+    out_g, lse_g = oracle_mod.prefill_causal_rows(q, k, v, 0.4)
+    out_m, lse_m = oracle_mod.prefill_causal_rows(q, np.repeat(k, G, axis=2),
+                                                  np.repeat(v, G, axis=2), 0.4)
+    np.testing.assert_allclose(out_g, out_m, atol=1e-14)
+    np.testing.assert_allclose(lse_g, lse_m, atol=1e-14)
+    qd = q[:, 0]
+    out_g, lse_g = oracle_mod.decode(qd, k, v, [7, 19], 0.4)
+    out_m, lse_m = oracle_mod.decode(qd, np.repeat(k, G, axis=2), np.repeat(v, G, axis=2),
+                                     [7, 19], 0.4)
+    np.testing.assert_allclose(out_g, out_m, atol=1e-14)
+    np.testing.assert_allclose(lse_g, lse_m, atol=1e-14)
+
+
+@pytest.mark.parametrize("chunk", [1, 3, 8, 64, 1000])
+def test_split_then_merge_equals_unsplit(oracle_mod, chunk):
+    rng = np.random.default_rng(6)
+    B, S, H_q, H_kv, d = 3, 50, 4, 2, 8
+    q, k, v = _rand((B, H_q, d), rng), _rand((B, S, H_kv, d), rng, 2.0), _rand((B, S, H_kv, d), rng)
+    lens = [50, 1, 33]
+    n_split = -(-S // chunk)
+    m, l, O = oracle_mod.decode_partials(q, k, v, lens, 0.35, n_split, chunk)
+    out_s, lse_s = oracle_mod.merge_partials(m, l, O)
+    out, lse = oracle_mod.decode(q, k, v, lens, 0.35)
+    np.testing.assert_allclose(out_s, out, atol=1e-12)
+    np.testing.assert_allclose(lse_s, lse, atol=1e-12)
+    # empty splits are the identity (-inf, 0)
+    for b, L in enumerate(lens):
+        for s_ in range(n_split):
+            if s_ * chunk >= L:
+                assert m[b, :, s_].tolist() == [-math.inf] * H_q
+                assert (l[b, :, s_] == 0).all()
+
+
+def test_merge_is_commutative_and_has_identity(oracle_mod):
+    rng = np.random.default_rng(7)
+    R, n, d = 5, 6, 4
+    m = rng.standard_normal((R, n)) * 3
+    l = rng.uniform(0.5, 4.0, (R, n))
+    O = rng.standard_normal((R, n, d))
+    out, lse = oracle_mod.merge_partials(m, l, O)
+    perm = rng.permutation(n)
+    out_p, lse_p = oracle_mod.merge_partials(m[:, perm], l[:, perm], O[:, perm])
+    np.testing.assert_allclose(out_p, out, atol=1e-13)
+    np.testing.assert_allclose(lse_p, lse, atol=1e-13)
+    m_id = np.concatenate([m, np.full((R, 2), -np.inf)], axis=1)
+    l_id = np.concatenate([l, np.zeros((R, 2))], axis=1)
+    O_id = np.concatenate([O, np.zeros((R, 2, d))], axis=1)
+    out_i, lse_i = oracle_mod.merge_partials(m_id, l_id, O_id)
+    np.testing.assert_allclose(out_i, out, atol=1e-13)
+    np.testing.assert_allclose(lse_i, lse, atol=1e-13)
+    # closed form of the merge: LSE = ln sum_s l_s e^{m_s}; O = sum_s e^{m_s} O_s / sum_s l_s e^{m_s}
+    w = np.exp(m)
+    np.testing.assert_allclose(lse, np.log((l * w).sum(axis=1)), atol=1e-12)
+    np.testing.assert_allclose(out, (w[:, :, None] * O).sum(1) / (l * w).sum(1)[:, None],
+                               atol=1e-12)
+
+
+def test_shift_of_keys_along_query_shifts_lse_only(oracle_mod):
+    rng = np.random.default_rng(8)
+    B, S, H_q, d = 1, 30, 1, 8
+    q, k, v = _rand((B, 1, d), rng), _rand((B, S, 1, d), rng), _rand((B, S, 1, d), rng)
+    lam, tau = 2.5, 0.3
+    out0, lse0 = oracle_mod.decode(q, k, v, [S], tau)
+    k2 = k + lam * q[:, None, :, :]
+    out1, lse1 = oracle_mod.decode(q, k2, v, [S], tau)
+    np.testing.assert_allclose(out1, out0, atol=1e-12)
+    assert lse1[0, 0] - lse0[0, 0] == pytest.approx(tau * lam * float(q[0, 0] @ q[0, 0]),
+                                                    abs=1e-11)
+
+
+def test_decode_ignores_key_order(oracle_mod):
+    rng = np.random.default_rng(9)
+    S, d = 40, 16
+    q, k, v = _rand((1, 2, d), rng), _rand((1, S, 1, d), rng), _rand((1, S, 1, d), rng)
+    perm = rng.permutation(S)
+    out0, lse0 = oracle_mod.decode(q, k, v, [S], 0.25)
+    out1, lse1 = oracle_mod.decode(q, k[:, perm], v[:, perm], [S], 0.25)
+    np.testing.assert_allclose(out1, out0, atol=1e-13)
+    np.testing.assert_allclose(lse1, lse0, atol=1e-13)
+
+
+def test_prefill_row_equals_decode_on_its_prefix(oracle_mod):
+    rng = np.random.default_rng(10)
+    B, S, H_q, H_kv, d = 2, 21, 4, 2, 8
+    q, k, v = (_rand((B, S, H_q, d), rng), _rand((B, S, H_kv, d), rng),
+               _rand((B, S, H_kv, d), rng))
+    rows = [0, 1, 7, 20]
+    out, lse = oracle_mod.prefill_causal_rows(q, k, v, 0.5, rows=rows)
+    for r, i in enumerate(rows):
+        o_d, l_d = oracle_mod.decode(q[:, i], k, v, [i + 1] * B, 0.5)
+        np.testing.assert_allclose(out[:, r], o_d, atol=1e-13)
+        np.testing.assert_allclose(lse[:, :, r], l_d, atol=1e-13)
+
+
+def test_bf16_inputs_are_widened_exactly(oracle_mod):
+    q, k, v, lens = inputs.decode_inputs(2, 4, 2, 16, 33, seed=3, seq_lens=[33, 10])
+    out_b, lse_b = oracle_mod.decode(q, k, v, lens, 0.25)
+    out_f, lse_f = oracle_mod.decode(q.double(), k.double(), v.double(), lens, 0.25)
+    assert np.array_equal(out_b, out_f) and np.array_equal(lse_b, lse_f)
+    assert np.isfinite(out_b).all()  # NaN padding past seq_lens is never read
+
+
+# ------------------------------------------- independent re-derivations ---
+def _brute_decimal(qrow, keys, vals, tau, prec=50):
+    """Naive softmax attention of one row in decimal arithmetic (p.2 §1, p.3 §1).
+
+    Inputs are converted to Decimal exactly; no max subtraction is needed since
+    decimal exponents do not overflow at these magnitudes.
+    """
+    D = decimal.Decimal
+    with decimal.localcontext() as ctx:
+        ctx.prec = prec
+        s = [D(float(tau)) * sum((D(float(a)) * D(float(b)) for a, b in zip(qrow, kj)), D(0))
+             for kj in keys]
+        e = [x.exp() for x in s]
+        tot = sum(e, D(0))
+        out = [float(sum((ei * D(float(vj[t])) for ei, vj in zip(e, vals)), D(0)) / tot)
+               for t in range(len(vals[0]))]
+        return out, float(tot.ln())
+
+
+def test_brute_force_decimal_tiny_shapes(oracle_mod):
+    rng = np.random.default_rng(11)
+    B, S, H_q, H_kv, d = 2, 6, 4, 2, 3
+    G = H_q // H_kv
+    q, k, v = (_rand((B, S, H_q, d), rng), _rand((B, S, H_kv, d), rng, 1.5),
+               _rand((B, S, H_kv, d), rng))
+    tau = 0.6
+    out, lse = oracle_mod.prefill_causal_rows(q, k, v, tau)
+    for b in range(B):
+        for i in range(S):
+            for h in range(H_q):
+                ref_o, ref_l = _brute_decimal(q[b, i, h], k[b, : i + 1, h // G],
+                                              v[b, : i + 1, h // G], tau)
+                np.testing.assert_allclose(out[b, i, h], ref_o, rtol=1e-13, atol=1e-14)
+                assert lse[b, h, i] == pytest.approx(ref_l, rel=1e-13, abs=1e-14)
+    lens = [6, 4]
+    out, lse = oracle_mod.decode(q[:, 2], k, v, lens, tau)
+    for b in range(B):
+        for h in range(H_q):
+            ref_o, ref_l = _brute_decimal(q[b, 2, h], k[b, : lens[b], h // G],
+                                          v[b, : lens[b], h // G], tau)
+            np.testing.assert_allclose(out[b, h], ref_o, rtol=1e-13, atol=1e-14)
+            assert lse[b, h] == pytest.approx(ref_l, rel=1e-13, abs=1e-14)
+
+
+def _online_two_pass(s, vals):
+    """p.3 §4: streaming (m, l) in one pass, then the outputs in a second."""
+    m, l = -math.inf, 0.0
+    for x in s:
+        m_new = max(m, x)
+        l = l * math.exp(m - m_new) + math.exp(x - m_new)
+        m = m_new
+    o = sum(math.exp(x - m) / l * vj for x, vj in zip(s, vals))
+    return o, m + math.log(l)
+
+
+def _online_fused(s, vals):
+    """p.3 §5: (m, l, O) streamed together, O rescaled whenever m grows, divided once."""
+    m, l, o = -math.inf, 0.0, np.zeros_like(vals[0])
+    for x, vj in zip(s, vals):
+        m_new = max(m, x)
+        corr = math.exp(m - m_new)
+        l = l * corr + math.exp(x - m_new)
+        o = o * corr + math.exp(x - m_new) * vj
+        m = m_new
+    return o / l, m + math.log(l)
+
+
+def test_three_pass_matches_online_forms(oracle_mod):
+    rng = np.random.default_rng(12)
+    S, d, tau = 60, 8, 0.5
+    q, k, v = _rand((1, 1, d), rng), _rand((1, S, 1, d), rng, 3.0), _rand((1, S, 1, d), rng)
+    out, lse = oracle_mod.decode(q, k, v, [S], tau)
+    s = [tau * float(q[0, 0] @ k[0, j, 0]) for j in range(S)]
+    vals = [v[0, j, 0] for j in range(S)]
+    for fn in (_online_two_pass, _online_fused):
+        o, l_ = fn(s, vals)
+        np.testing.assert_allclose(out[0, 0], o, atol=1e-12)
+        assert lse[0, 0] == pytest.approx(l_, abs=1e-12)
+
+
+# -------------------------------------------------------- argument checks ---
+def test_invalid_arguments_raise(oracle_mod):
+    q = np.zeros((1, 3, 4))
+    k = np.zeros((1, 5, 2, 4))
+    with pytest.raises(ValueError):
+        oracle_mod.decode(q, k, k, [5], 1.0)  # H_q not a multiple of H_kv
+    q = np.zeros((1, 4, 4))
+    with pytest.raises(ValueError):
+        oracle_mod.decode(q, k, k, [0], 1.0)  # empty sequence
+    with pytest.raises(ValueError):
+        oracle_mod.decode(q, k, k, [6], 1.0)  # longer than the cache
+    with pytest.raises(ValueError):
+        oracle_mod.prefill_causal_rows(np.zeros((1, 5, 4, 4)), k, k, 1.0, rows=[5])
+
+
+# --------------------------------------------------------- input recipes ---
+def test_input_generators_are_seeded_and_padded():
+    a = inputs.decode_inputs(3, 8, 2, 32, 100, seed=5, ragged=(10, 100))
+    b = inputs.decode_inputs(3, 8, 2, 32, 100, seed=5, ragged=(10, 100))
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x,
+                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y)
+    q, k, v, lens = a
+    assert q.dtype == torch.bfloat16 and lens.dtype == torch.int32
+    for bb in range(3):
+        L = int(lens[bb])
+        assert 10 <= L <= 100
+        assert torch.isfinite(k[bb, :L].float()).all() and torch.isnan(k[bb, L:].float()).all()
+    rows = inputs.sample_rows(1000, 16, seed=0)
+    assert rows[0] == 0 and rows[-1] == 999 and len(rows) == 16
+    assert torch.equal(rows, inputs.sample_rows(1000, 16, seed=0))
