@@ -1,0 +1,428 @@
+#!/usr/bin/env python3
+"""Benchmark of the grouped-query attention forward hot path on one GB300.
+
+One step = one pass of the whole path on seeded synthetic inputs:
+  * decode  : Llama3-70B-shaped GQA decode, B=1, H_q=64, H_kv=8, d=128,
+              ctx 32768 -- split-KV kernel + log-sum-exp combine;
+  * prefill : Llama3-70B-shaped causal GQA prefill, B=1, S=8192, H_q=64,
+              H_kv=8, d=128.
+``value`` is the decode leg's KV-cache throughput (GB/s of K and V bytes read,
+inputs resident in HBM, L2 flushed before every timed decode); the prefill
+leg's TFLOP/s (causal FLOPs only) is reported beside it under ``prefill``.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead
+(bounded samples of the same workloads).  Under torchrun (N > 1) every rank runs
+an independent replica (the path has no cross-GPU exchange); the value is the
+sum over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode KV GB/s (% HBM peak); causal prefill TFLOPS (% bf16 peak)"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 512 * 1024 * 1024
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return (float(j["hbm_gbs"]), float(j["bf16_tflops"]),
+                float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), "measured")
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def _source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "gqa_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _recorded_traffic(profile_name, files):
+    """Per-launch DRAM bytes recorded from an ncu capture, if the kernel is unchanged since."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_digest")):
+            k, v = line.split(":", 1)
+            fields[k.strip().lstrip("- ")] = v.strip().strip("`")
+    try:
+        if fields.get("source_digest") != _source_digest(files):
+            return None
+        return float(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gqa_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------- ours ---
+def _time_events(torch, fn, steps, stream, flush=None, marks=1):
+    """Run fn(ev_list) `steps` times with CUDA events; returns per-step lists of ms."""
+    per = []
+    for _ in range(steps):
+        if flush is not None:
+            flush()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(marks + 1)]
+        fn(evs)
+        per.append(evs)
+    torch.cuda.synchronize()
+    return [[evs[i].elapsed_time(evs[i + 1]) for i in range(marks)] for evs in per]
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+
+    import gqa_attention_gb300 as g
+    from gqa_attention_gb300 import inputs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    g.load()
+    stream = torch.cuda.current_stream()
+    hbm_gbs, bf16_tf, bf16_tf_sus, peak_kind = _peaks()
+
+    # ---------------- decode leg (Llama3-70B decode, ctx 32768) ----------------
+    dc = inputs.LLAMA70B_DECODE
+    q, k, v, lens = inputs.decode_inputs_for(dc, seed=0)
+    kv_bytes = 2 * int(lens.sum()) * dc.H_kv * dc.d * 2
+    qd, kd, vd, ld = (x.to(dev) for x in (q, k, v, lens))
+    n_split = g.gqa_attn_decode_default_splits(dc.B, dc.H_kv, dc.S_max, dc.d)
+    ws = g.decode_workspace(dc.B, dc.H_q, dc.d, n_split, dev)
+    out = torch.empty(dc.B, dc.H_q, dc.d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(dc.B, dc.H_q, dtype=torch.float32, device=dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    def decode_step(evs):
+        evs[0].record(stream)
+        st = g.gqa_attn_decode(qd, kd, vd, ld, dc.B, dc.S_max, dc.H_q, dc.H_kv, dc.d, dc.scale,
+                               n_split, ws, out, lse, stream)
+        evs[1].record(stream)
+        st2 = g.gqa_attn_decode_combine(ws, dc.B, dc.H_q, dc.d, n_split, out, lse, stream)
+        evs[2].record(stream)
+        if st or st2:
+            raise RuntimeError(f"decode failed: {g.status_str(st or st2)}")
+
+    # ---------------- prefill leg (Llama3-70B causal prefill, S 8192) ----------
+    pc = inputs.LLAMA70B_PREFILL_8K
+    pq, pk, pv = inputs.prefill_inputs_for(pc, seed=0)
+    pqd, pkd, pvd = (x.to(dev) for x in (pq, pk, pv))
+    pout = torch.empty_like(pqd)
+    plse = torch.empty(pc.B, pc.H_q, pc.S, dtype=torch.float32, device=dev)
+    causal_flops = 4.0 * pc.d * pc.H_q * pc.B * pc.S * (pc.S + 1) / 2
+    prefill_ok = g.gqa_attn_prefill_causal(pqd, pkd, pvd, pc.B, pc.S, pc.H_q, pc.H_kv, pc.d,
+                                           pc.scale, pout, plse, stream) == g.GQA_OK
+    torch.cuda.synchronize()
+
+    def prefill_step(evs):
+        evs[0].record(stream)
+        st = g.gqa_attn_prefill_causal(pqd, pkd, pvd, pc.B, pc.S, pc.H_q, pc.H_kv, pc.d,
+                                       pc.scale, pout, plse, stream)
+        evs[1].record(stream)
+        if st:
+            raise RuntimeError(f"prefill failed: {g.status_str(st)}")
+
+    # ---------------- warm-up ----------------
+    for _ in range(args.warmup):
+        flush()
+        decode_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+        if prefill_ok:
+            prefill_step([torch.cuda.Event(enable_timing=True) for _ in range(2)])
+    torch.cuda.synchronize()
+    if g.gqa_last_device_error(stream) != g.GQA_OK:
+        raise RuntimeError("device error during warm-up")
+
+    # ---------------- timed region ----------------
+    with ClockSampler(dev.index) as clk:
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        dec = _time_events(torch, decode_step, args.steps, stream, flush=flush, marks=2)
+        pre = (_time_events(torch, prefill_step, args.steps, stream, marks=1)
+               if prefill_ok else None)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        wall_s = time.perf_counter() - t_wall
+    clocks = clk.summary()
+    if g.gqa_last_device_error(stream) != g.GQA_OK:
+        raise RuntimeError("device error during the timed region")
+
+    split_ms = statistics.mean(x[0] for x in dec)
+    dec_ms = statistics.mean(x[0] + x[1] for x in dec)
+    pre_ms = statistics.mean(x[0] for x in pre) if pre else None
+
+    # ---------------- end to end through the C ABI from pinned host buffers -----
+    hq, hk, hv, hl = (x.pin_memory() for x in (q, k, v, lens))
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hl))
+    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+
+    def e2e_step(evs):
+        evs[0].record(stream)
+        qd.copy_(hq, non_blocking=True)
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        ld.copy_(hl, non_blocking=True)
+        decode_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        evs[1].record(stream)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    _time_events(torch, e2e_step, 2, stream, flush=flush)
+    e2e = _time_events(torch, e2e_step, e2e_steps, stream, flush=flush)
+    e2e_ms = statistics.mean(x[0] for x in e2e)
+
+    # max over ranks
+    times = torch.tensor([dec_ms, split_ms, pre_ms or 0.0, e2e_ms], device=dev)
+    if dist is not None:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    dec_ms, split_ms, pre_ms_max, e2e_ms = (float(x) for x in times.tolist())
+    pre_ms = pre_ms_max if pre_ms is not None else None
+    if rank != 0:
+        return None
+
+    value = world * kv_bytes / (dec_ms * 1e-3) / 1e9
+    achieved = kv_bytes / (split_ms * 1e-3) / 1e9
+    traffic = _recorded_traffic("decode_split_llama70b_ctx32768.md",
+                                ["decode.cu", "common.cuh", "internal.h"])
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dec_ms + (pre_ms or 0.0), 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded torch.randn, rounded to bf16)",
+        "config": {
+            "workload": f"{dc.name} (value) + {pc.name} (prefill)",
+            "decode": {"B": dc.B, "H_q": dc.H_q, "H_kv": dc.H_kv, "d": dc.d, "ctx": dc.S_max,
+                       "n_split": n_split, "kv_bytes": kv_bytes,
+                       "ms_split_plus_combine": round(dec_ms, 5),
+                       "hbm_frac_of_" + peak_kind: round(value / world / hbm_gbs, 4),
+                       "hbm_frac_of_nominal_8TBs": round(value / world / 8000.0, 4)},
+            "prefill": {"B": pc.B, "S": pc.S, "H_q": pc.H_q, "H_kv": pc.H_kv, "d": pc.d},
+            "l2": "flushed (512 MiB write) before every timed decode; prefill inputs exceed L2",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "clocks": clocks,
+        "roofline": {
+            "kernel": "gqa_decode_split_kernel",
+            "bound": "hbm",
+            "achieved": round(achieved, 2),
+            "peak": hbm_gbs,
+            "unit": "GB/s",
+            "frac": round(achieved / hbm_gbs, 4),
+            "peak_kind": peak_kind,
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": kv_bytes,
+        },
+        "gpu_launches": args.steps * (2 + (1 if prefill_ok else 0)),
+        "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "wall_s_timed_region": round(wall_s, 3),
+    }
+    if pre_ms is not None:
+        tflops = causal_flops / (pre_ms * 1e-3) / 1e12
+        line["prefill"] = {
+            "value": round(world * tflops, 2), "unit": "TFLOP/s", "ms": round(pre_ms, 4),
+            "causal_flops": causal_flops,
+            "roofline": {"kernel": "gqa_prefill_causal_kernel", "bound": "tensor",
+                         "achieved": round(tflops, 2), "peak": bf16_tf_sus, "unit": "TFLOP/s",
+                         "frac": round(tflops / bf16_tf_sus, 4),
+                         "peak_kind": peak_kind + " (sustained)",
+                         "frac_of_burst": round(tflops / bf16_tf, 4),
+                         "traffic": _recorded_traffic("prefill_causal_llama70b_s8192.md",
+                                                      ["prefill.cu", "common.cuh", "internal.h"])},
+        }
+    else:
+        line["prefill"] = None
+    line["cpu_baseline"] = cpu_baseline(args, sample_only=True) if not args.no_cpu_baseline else None
+    return line
+
+
+# ------------------------------------------------------ CPU oracle baseline --
+def cpu_baseline(args, sample_only=True, steps=1):
+    """Time the fp64 oracle on the host cores on a bounded sample of the decode workload."""
+    import oracle
+    from gqa_attention_gb300 import inputs
+
+    oracle.build()
+    dc = inputs.LLAMA70B_DECODE
+    q, k, v, lens = inputs.decode_inputs_for(dc, seed=0)
+    kv_bytes = 2 * int(lens.sum()) * dc.H_kv * dc.d * 2
+    cores = os.cpu_count() or 1
+    times = []
+    for _ in range(max(1, steps)):
+        t0 = time.perf_counter()
+        oracle.decode(q, k, v, lens, dc.scale, nthreads=cores)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    return {"value": round(kv_bytes / t / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"whole {dc.name} decode (all 64 query heads, 32768 keys), fp64, "
+                      f"median of {len(times)} run(s), {t:.3f} s each"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: K timed steps of the whole decode workload on CPU."""
+    if rank != 0:
+        return None
+    import oracle
+    from gqa_attention_gb300 import inputs
+
+    oracle.build()
+    dc = inputs.LLAMA70B_DECODE
+    q, k, v, lens = inputs.decode_inputs_for(dc, seed=0)
+    kv_bytes = 2 * int(lens.sum()) * dc.H_kv * dc.d * 2
+    cores = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle.decode(q, k, v, lens, dc.scale, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode(q, k, v, lens, dc.scale, nthreads=cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = kv_bytes / dt / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded torch.randn, bf16)",
+        "config": {"workload": f"{dc.name} (value)", "l2": "n/a (CPU)",
+                   "parallelism": "CPU threads"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"whole {dc.name} decode per step (fp64 oracle)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        if world > 1 and rank != 0:
+            return 0
+        line = run_reference(args, rank, world)
+        print(json.dumps(line), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    try:
+        line = run_ours(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -5,3 +5,27 @@ The compute runs in ``libgqa_attn.so`` (CUDA kernels behind a C ABI declared in
 is loaded on first use and a missing or unbuildable library raises: there is no
 CPU fallback.
 """
+
+from ._binding import (  # noqa: E402,F401
+    GQA_ERR_CUDA,
+    GQA_ERR_INVALID_ARG,
+    GQA_ERR_TIMEOUT,
+    GQA_ERR_UNSUPPORTED,
+    GQA_OK,
+    GQAError,
+    decode,
+    decode_workspace,
+    gqa_attn_decode,
+    gqa_attn_decode_combine,
+    gqa_attn_decode_default_splits,
+    gqa_attn_decode_split_chunk,
+    gqa_attn_decode_workspace_bytes,
+    gqa_attn_prefill_causal,
+    gqa_last_device_error,
+    gqa_selftest_wait_timeout,
+    gqa_set_wait_limit_ns,
+    load,
+    prefill_causal,
+    split_workspace,
+    status_str,
+)

@@ -1,0 +1,195 @@
+"""ctypes binding of libgqa_attn.so (declared in ``include/gqa_attn.h``).
+
+Argument marshalling only: every step of the attention runs in the library's
+CUDA kernels.  The functions named like the C entry points take torch CUDA
+tensors (or raw integers for pointers) and return the C status code; the
+helpers at the bottom allocate outputs with torch and raise on a bad status.
+There is no CPU fallback: if the library cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libgqa_attn.so")
+
+GQA_OK, GQA_ERR_INVALID_ARG, GQA_ERR_UNSUPPORTED, GQA_ERR_CUDA, GQA_ERR_TIMEOUT = range(5)
+
+#: Every symbol the header declares, with (restype, argtypes).
+_P, _I, _F, _SZ, _U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint64
+SIGNATURES = {
+    "gqa_status_str": (ctypes.c_char_p, [_I]),
+    "gqa_version": (_I, []),
+    "gqa_attn_decode_split_chunk": (_I, [_I, _I]),
+    "gqa_attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "gqa_attn_decode_default_splits": (_I, [_I, _I, _I, _I]),
+    "gqa_attn_decode": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
+    "gqa_attn_decode_combine": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
+    "gqa_attn_prefill_causal": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
+    "gqa_last_device_error": (_I, [_P]),
+    "gqa_set_wait_limit_ns": (_U64, [_U64]),
+    "gqa_selftest_wait_timeout": (_I, [_U64, _P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GQAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_str(status)}")
+
+
+def load(path: str | None = None):
+    """Load (building first if absent) and return the ctypes library handle."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                from . import build as _build  # compile in-tree; raises if nvcc fails
+                _build.build()
+            lib = ctypes.CDLL(p)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ------------------------------------------------------- same-name entries --
+def status_str(status: int) -> str:
+    return load().gqa_status_str(int(status)).decode()
+
+
+def gqa_attn_decode_split_chunk(S_max: int, n_split: int) -> int:
+    return load().gqa_attn_decode_split_chunk(S_max, n_split)
+
+
+def gqa_attn_decode_workspace_bytes(B: int, H_q: int, d: int, n_split: int) -> int:
+    return load().gqa_attn_decode_workspace_bytes(B, H_q, d, n_split)
+
+
+def gqa_attn_decode_default_splits(B: int, H_kv: int, S_max: int, d: int) -> int:
+    return load().gqa_attn_decode_default_splits(B, H_kv, S_max, d)
+
+
+def gqa_attn_decode(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale, n_split,
+                    workspace, out, lse, stream=None) -> int:
+    return load().gqa_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B, S_max,
+                                  H_q, H_kv, d, scale, n_split, _ptr(workspace), _ptr(out),
+                                  _ptr(lse), _stream(stream))
+
+
+def gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream=None) -> int:
+    return load().gqa_attn_decode_combine(_ptr(workspace), B, H_q, d, n_split, _ptr(out),
+                                          _ptr(lse), _stream(stream))
+
+
+def gqa_attn_prefill_causal(q, k, v, B, S, H_q, H_kv, d, scale, out, lse, stream=None) -> int:
+    return load().gqa_attn_prefill_causal(_ptr(q), _ptr(k), _ptr(v), B, S, H_q, H_kv, d, scale,
+                                          _ptr(out), _ptr(lse), _stream(stream))
+
+
+def gqa_last_device_error(stream=None) -> int:
+    return load().gqa_last_device_error(_stream(stream))
+
+
+def gqa_set_wait_limit_ns(limit_ns: int) -> int:
+    return load().gqa_set_wait_limit_ns(int(limit_ns))
+
+
+def gqa_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    return load().gqa_selftest_wait_timeout(int(limit_ns), _stream(stream))
+
+
+# ------------------------------------------------------------ torch helpers --
+def _check(status: int, what: str):
+    if status != GQA_OK:
+        raise GQAError(status, what)
+
+
+def decode_workspace(B, H_q, d, n_split, device="cuda"):
+    """A workspace tensor for gqa_attn_decode (None when n_split == 1)."""
+    import torch
+
+    nbytes = gqa_attn_decode_workspace_bytes(B, H_q, d, n_split)
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def decode(q, k_cache, v_cache, seq_lens, scale=None, n_split=None, workspace=None, out=None,
+           lse=None, stream=None):
+    """Split-KV decode + combine on CUDA tensors; returns (out bf16 [B,H_q,d], lse fp32 [B,H_q])."""
+    import torch
+
+    B, H_q, d = q.shape
+    _, S_max, H_kv, _ = k_cache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if n_split is None:
+        n_split = gqa_attn_decode_default_splits(B, H_kv, S_max, d)
+    if out is None:
+        out = torch.empty((B, H_q, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
+    if n_split > 1 and workspace is None:
+        workspace = decode_workspace(B, H_q, d, n_split, q.device)
+    _check(gqa_attn_decode(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale, n_split,
+                           workspace, out, lse, stream), "gqa_attn_decode")
+    if n_split > 1:
+        _check(gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream),
+               "gqa_attn_decode_combine")
+    return out, lse
+
+
+def prefill_causal(q, k, v, scale=None, out=None, lse=None, stream=None):
+    """Causal prefill on CUDA tensors; returns (out bf16 [B,S,H_q,d], lse fp32 [B,H_q,S])."""
+    import torch
+
+    B, S, H_q, d = q.shape
+    H_kv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, S, H_q, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H_q, S), dtype=torch.float32, device=q.device)
+    _check(gqa_attn_prefill_causal(q, k, v, B, S, H_q, H_kv, d, scale, out, lse, stream),
+           "gqa_attn_prefill_causal")
+    return out, lse
+
+
+def split_workspace(workspace, B, H_q, d, n_split):
+    """Views (ml [B,H_q,n_split,2], O [B,H_q,n_split,d]) of a decode workspace tensor."""
+    import torch
+
+    ml_bytes = B * H_q * n_split * 8
+    off = (ml_bytes + 255) // 256 * 256
+    ml = workspace[:ml_bytes].view(torch.float32).view(B, H_q, n_split, 2)
+    O = workspace[off: off + B * H_q * n_split * d * 4].view(torch.float32).view(B, H_q, n_split, d)
+    return ml, O

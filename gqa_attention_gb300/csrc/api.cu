@@ -1,0 +1,283 @@
+// api.cu -- the C ABI of libgqa_attn.so (declared in include/gqa_attn.h):
+// argument checks, TMA tensor-map encoding, the per-device error word and the
+// kernel launches.  Nothing here computes attention.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "gqa_attn.h"
+#include "internal.h"
+
+namespace {
+
+// One error word per device (a module global is instantiated per context).
+__device__ unsigned g_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+unsigned* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+std::atomic<uint64_t> g_wait_ns{2000000000ull};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+gqa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA; }
+
+// Device pointer of the error word of the current device (looked up once).
+gqa_status error_word(unsigned** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return GQA_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return GQA_OK;
+}
+
+int num_sms_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_num_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 148;
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
+}
+
+gqa_status get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_encode) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !f)
+      return GQA_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  *fn = g_encode;
+  return GQA_OK;
+}
+
+// A bf16 tensor map of `rank` dims (innermost first); strides in bytes for dims 1.. .
+gqa_status encode_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                       const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swz) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  gqa_status st = get_encoder(&enc);
+  if (st != GQA_OK) return st;
+  cuuint64_t gdim[5], gstr[4];
+  cuuint32_t bdim[5], estr[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    estr[i] = 1;
+    if (i + 1 < rank) gstr[i] = strides[i];
+  }
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim,
+                   gstr, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GQA_OK : GQA_ERR_INVALID_ARG;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool head_dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+
+}  // namespace
+
+extern "C" {
+
+const char* gqa_status_str(int status) {
+  switch (status) {
+    case GQA_OK: return "GQA_OK";
+    case GQA_ERR_INVALID_ARG: return "GQA_ERR_INVALID_ARG";
+    case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED";
+    case GQA_ERR_CUDA: return "GQA_ERR_CUDA";
+    case GQA_ERR_TIMEOUT: return "GQA_ERR_TIMEOUT";
+    default: return "GQA_ERR_UNKNOWN";
+  }
+}
+
+int gqa_version(void) { return 100; }
+
+int gqa_attn_decode_split_chunk(int S_max, int n_split) {
+  if (S_max < 1 || n_split < 1) return 0;
+  const long long per = ((long long)S_max + n_split - 1) / n_split;
+  const long long t = gqa::kDecodeTile;
+  return (int)((per + t - 1) / t * t);
+}
+
+size_t gqa_attn_decode_workspace_bytes(int B, int H_q, int d, int n_split) {
+  if (B < 1 || H_q < 1 || d < 1 || n_split <= 1) return 0;
+  return gqa::decode_ws_O_offset(B, H_q, n_split) + (size_t)B * H_q * n_split * d * sizeof(float);
+}
+
+int gqa_attn_decode_default_splits(int B, int H_kv, int S_max, int d) {
+  (void)d;
+  if (B < 1 || H_kv < 1 || S_max < 1) return 1;
+  const long long ctas = 2LL * num_sms_current_device();   // about two CTAs per SM
+  long long n = (ctas + (long long)B * H_kv - 1) / ((long long)B * H_kv);
+  const long long most = (S_max + 255) / 256;               // splits of >= 256 tokens
+  const long long fill = (S_max + 2047) / 2048;             // and of <= ~2048 tokens
+  if (n > most) n = most;
+  if (n < fill) n = fill;
+  if (n < 1) n = 1;
+  if (n > 65535) n = 65535;
+  return (int)n;
+}
+
+gqa_status gqa_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* seq_lens, int B, int S_max, int H_q, int H_kv, int d,
+                           float scale, int n_split, void* workspace, void* out, float* lse,
+                           gqa_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !seq_lens || !out || !lse) return GQA_ERR_INVALID_ARG;
+  if (B < 1 || S_max < 1 || H_q < 1 || H_kv < 1 || n_split < 1) return GQA_ERR_INVALID_ARG;
+  if (B > 65535 || H_kv > 65535 || H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  if ((long long)B * S_max > 0xffffffffLL || n_split > 0x7fffffff) return GQA_ERR_INVALID_ARG;
+  if (!head_dim_ok(d) || H_q / H_kv > 16) return GQA_ERR_UNSUPPORTED;
+  if (n_split > 1 && !workspace) return GQA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(seq_lens, 4) || (workspace && !aligned(workspace, 256)))
+    return GQA_ERR_INVALID_ARG;
+
+  unsigned* err = nullptr;
+  gqa_status st = error_word(&err);
+  if (st != GQA_OK) return st;
+
+  // K/V cache viewed as [B*S_max rows][H_kv][d]; one box = 64 token rows of one
+  // head, at most 64 elements (128 bytes) wide, swizzled for ldmatrix.
+  const int box_d = d >= 64 ? 64 : d;
+  const uint64_t dims[3] = {(uint64_t)d, (uint64_t)H_kv, (uint64_t)B * S_max};
+  const uint64_t strides[2] = {(uint64_t)d * 2, (uint64_t)H_kv * d * 2};
+  const uint32_t box[3] = {(uint32_t)box_d, 1u, (uint32_t)gqa::kDecodeTile};
+  const CUtensorMapSwizzle swz = box_d == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUtensorMap tm_k, tm_v;
+  if ((st = encode_bf16(&tm_k, k_cache, 3, dims, strides, box, swz)) != GQA_OK) return st;
+  if ((st = encode_bf16(&tm_v, v_cache, 3, dims, strides, box, swz)) != GQA_OK) return st;
+
+  gqa::DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.seq_lens = seq_lens;
+  p.B = B;
+  p.S_max = S_max;
+  p.H_q = H_q;
+  p.H_kv = H_kv;
+  p.G = H_q / H_kv;
+  p.d = d;
+  p.n_split = n_split;
+  p.chunk = gqa_attn_decode_split_chunk(S_max, n_split);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.ws_ml = static_cast<float2*>(workspace);
+  p.ws_O = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                gqa::decode_ws_O_offset(B, H_q, n_split))
+                     : nullptr;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.err = err;
+  p.wait_ns = g_wait_ns.load();
+  return cuda_status(gqa::launch_decode_split(p, tm_k, tm_v, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_attn_decode_combine(const void* workspace, int B, int H_q, int d, int n_split,
+                                   void* out, float* lse, gqa_stream_t stream) {
+  if (!workspace || !out || !lse) return GQA_ERR_INVALID_ARG;
+  if (B < 1 || H_q < 1 || n_split < 1 || B > 65535 || H_q > 65535) return GQA_ERR_INVALID_ARG;
+  if (!head_dim_ok(d)) return GQA_ERR_UNSUPPORTED;
+  if (n_split > 32768) return GQA_ERR_UNSUPPORTED;  // split weights live in shared memory
+  if (!aligned(workspace, 256) || !aligned(out, 16) || !aligned(lse, 4)) return GQA_ERR_INVALID_ARG;
+  gqa::CombineParams p;
+  p.ws_ml = static_cast<const float2*>(workspace);
+  p.ws_O = reinterpret_cast<const float*>(static_cast<const char*>(workspace) +
+                                          gqa::decode_ws_O_offset(B, H_q, n_split));
+  p.B = B;
+  p.H_q = H_q;
+  p.d = d;
+  p.n_split = n_split;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  return cuda_status(gqa::launch_decode_combine(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_attn_prefill_causal(const void* q, const void* k, const void* v, int B, int S,
+                                   int H_q, int H_kv, int d, float scale, void* out, float* lse,
+                                   gqa_stream_t stream) {
+  if (!q || !k || !v || !out || !lse) return GQA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
+  if (B > 65535 || H_q > 65535 || !std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  if (d != 128) return GQA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4))
+    return GQA_ERR_INVALID_ARG;
+  unsigned* err = nullptr;
+  gqa_status st = error_word(&err);
+  if (st != GQA_OK) return st;
+
+  // Q viewed as [B][S][H_q][d] with boxes of 128 rows of one head, 64 elements
+  // wide (two boxes per 128-wide row), 128-byte swizzle; K and V likewise.
+  const uint64_t dq[4] = {(uint64_t)d, (uint64_t)H_q, (uint64_t)S, (uint64_t)B};
+  const uint64_t sq[3] = {(uint64_t)d * 2, (uint64_t)H_q * d * 2, (uint64_t)S * H_q * d * 2};
+  const uint64_t dk[4] = {(uint64_t)d, (uint64_t)H_kv, (uint64_t)S, (uint64_t)B};
+  const uint64_t sk[3] = {(uint64_t)d * 2, (uint64_t)H_kv * d * 2, (uint64_t)S * H_kv * d * 2};
+  const uint32_t box[4] = {64u, 1u, 128u, 1u};
+  CUtensorMap tm_q, tm_k, tm_v;
+  if ((st = encode_bf16(&tm_q, q, 4, dq, sq, box, CU_TENSOR_MAP_SWIZZLE_128B)) != GQA_OK) return st;
+  if ((st = encode_bf16(&tm_k, k, 4, dk, sk, box, CU_TENSOR_MAP_SWIZZLE_128B)) != GQA_OK) return st;
+  if ((st = encode_bf16(&tm_v, v, 4, dk, sk, box, CU_TENSOR_MAP_SWIZZLE_128B)) != GQA_OK) return st;
+
+  gqa::PrefillParams p;
+  p.B = B;
+  p.S = S;
+  p.H_q = H_q;
+  p.H_kv = H_kv;
+  p.G = H_q / H_kv;
+  p.d = d;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.err = err;
+  p.wait_ns = g_wait_ns.load();
+  return cuda_status(gqa::launch_prefill_causal(p, tm_q, tm_k, tm_v, num_sms_current_device(),
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_last_device_error(gqa_stream_t stream) {
+  unsigned* err = nullptr;
+  gqa_status st = error_word(&err);
+  if (st != GQA_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  if (word) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+      return GQA_ERR_CUDA;
+  }
+  if (word & gqa::kErrTimeout) return GQA_ERR_TIMEOUT;
+  if (word & gqa::kErrBadSeqLen) return GQA_ERR_INVALID_ARG;
+  return GQA_OK;
+}
+
+uint64_t gqa_set_wait_limit_ns(uint64_t limit_ns) {
+  if (limit_ns < 1000) limit_ns = 1000;
+  return g_wait_ns.exchange(limit_ns);
+}
+
+gqa_status gqa_selftest_wait_timeout(uint64_t limit_ns, gqa_stream_t stream) {
+  unsigned* err = nullptr;
+  gqa_status st = error_word(&err);
+  if (st != GQA_OK) return st;
+  if (limit_ns < 1000) limit_ns = 1000;
+  return cuda_status(gqa::launch_wait_selftest(err, limit_ns, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

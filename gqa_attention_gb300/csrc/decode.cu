@@ -1,0 +1,504 @@
+// decode.cu -- split-KV grouped-query decode (stage 1) and the log-sum-exp
+// merge of the split partials (stage 2).
+//
+// Stage 1 follows the split-K decode of "Attention Kernel 계보" p.18 §4 with
+// the GQA fold of p.15 §4/§7 and ADR-0060 §5.2: one CTA per (split, KV head,
+// sequence) streams its split's K/V tiles once and serves all G query heads of
+// the group, which sit in the M rows of the warp-level bf16 mma (G <= 16, rows
+// past G are zero).  Softmax is the one-pass streaming (m, l, O) update of
+// p.3 §5, in base-2 units with log2(e) folded into the scale (p.3 §8).  The four
+// consumer warps take disjoint 16-token slices of every 64-token tile and are
+// merged once at the end through shared memory (FA2 K-split, p.9 §5).  A fifth
+// warp only issues TMA copies into a ring of NSTAGE shared-memory stages with
+// full/empty mbarriers (p.10 §3); every wait has a time limit.
+#include "common.cuh"
+#include "internal.h"
+
+namespace gqa {
+namespace {
+
+constexpr int kTile = kDecodeTile;  // tokens per stage
+constexpr int kConsumerWarps = 4;   // 16 tokens each
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+
+template <int D>
+struct DecodeLayout {
+  static constexpr int kBox = D >= 64 ? 64 : D;            // elements per TMA box row
+  static constexpr int kSpan = kBox * 2;                    // swizzle span (bytes)
+  static constexpr int kChunksPerRow = kBox / 8;            // 16-byte chunks per box row
+  static constexpr int kBlocks = D / kBox;                  // boxes per tile row
+  static constexpr int kBlockBytes = kTile * kSpan;         // one box of a tile
+  static constexpr int kTileBytes = kBlocks * kBlockBytes;  // K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;        // K + V
+  // Shared-memory byte offset of (token row, 16-byte chunk along d) in a tile.
+  __device__ static __forceinline__ uint32_t offset(int row, int chunk) {
+    const int blk = chunk / kChunksPerRow;
+    const int cc = chunk % kChunksPerRow;
+    return blk * kBlockBytes + swizzle<kSpan>(row * kSpan + cc * 16);
+  }
+};
+
+template <int D, int NSTAGE>
+constexpr int decode_smem_bytes() {
+  return NSTAGE * DecodeLayout<D>::kStageBytes + 1024;  // + alignment slack
+}
+
+__device__ __forceinline__ float quad_max(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+}
+__device__ __forceinline__ float quad_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  return v + __shfl_xor_sync(0xffffffffu, v, 2);
+}
+
+// Online-softmax update of one query row held by a quad of lanes: x are this
+// lane's 4 scores of the row in base-2 units (masked ones are -inf).  Returns
+// the rescale factor for the row's O accumulators and writes exp2(x - m) to p.
+__device__ __forceinline__ float online_update(float (&x)[4], float& m, float& l, float (&p)[4]) {
+  const float mx = quad_max(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
+  const float m_new = fmaxf(m, mx);
+  const float ref = (m_new == -INFINITY) ? 0.f : m_new;  // no (-inf) - (-inf)
+  const float alpha = exp2f(m - ref);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = exp2f(x[i] - ref);
+  l = l * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
+  m = m_new;
+  return alpha;
+}
+
+template <int D, bool ROWS16, int NSTAGE>
+__global__ void __launch_bounds__(kThreads, 1)
+    gqa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+  using Lay = DecodeLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[NSTAGE];
+  __shared__ __align__(8) uint64_t empty_bar[NSTAGE];
+  __shared__ int abort_flag;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t smem_base = smem_u32(smem);
+
+  const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.G;
+  const int h0 = kv * G;
+  const int L = p.seq_lens[b];
+
+  // ---- device-side argument check and empty splits (no pipeline needed) ----
+  if (L < 1 || L > p.S_max) {
+    if (threadIdx.x == 0 && split == 0 && kv == 0) atomicOr(p.err, kErrBadSeqLen);
+    for (int e = threadIdx.x; e < G * D; e += kThreads) {
+      const int r = e / D, c = e % D;
+      const size_t row = (size_t)b * p.H_q + h0 + r;
+      if (p.n_split == 1) {
+        p.out[row * D + c] = __float2bfloat16(NAN);
+        if (c == 0) p.lse[row] = NAN;
+      } else if (c == 0) {
+        p.ws_ml[row * p.n_split + split] = make_float2(NAN, NAN);
+      }
+    }
+    return;
+  }
+  const int t0 = split * p.chunk;
+  if (t0 >= L) {  // empty split: the merge identity (-inf, 0); O is not written
+    for (int r = threadIdx.x; r < G; r += kThreads)
+      p.ws_ml[((size_t)b * p.H_q + h0 + r) * p.n_split + split] = make_float2(-INFINITY, 0.f);
+    return;
+  }
+  const int t_end = min(t0 + p.chunk, L);
+  const int n_tiles = (t_end - t0 + kTile - 1) / kTile;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), kConsumerWarps);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------ producer ----
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      int issued = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int st = i % NSTAGE;
+        if (i >= NSTAGE &&
+            !mbar_wait(smem_u32(&empty_bar[st]), ((i / NSTAGE) - 1) & 1, p.wait_ns, p.err)) {
+          *reinterpret_cast<volatile int*>(&abort_flag) = 1;
+          break;
+        }
+        if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
+        const uint32_t fb = smem_u32(&full_bar[st]);
+        mbar_arrive_expect_tx(fb, Lay::kStageBytes);
+        const uint32_t dst_k = smem_base + st * Lay::kStageBytes;
+        const uint32_t dst_v = dst_k + Lay::kTileBytes;
+        const int row = b * p.S_max + t0 + i * kTile;
+#pragma unroll
+        for (int blk = 0; blk < Lay::kBlocks; ++blk) {
+          tma_load_3d(dst_k + blk * Lay::kBlockBytes, &tm_k, fb, blk * Lay::kBox, kv, row);
+          tma_load_3d(dst_v + blk * Lay::kBlockBytes, &tm_v, fb, blk * Lay::kBox, kv, row);
+        }
+        issued = i + 1;
+      }
+      // No copy may still target this CTA's shared memory when it exits.
+      for (int i = max(0, issued - NSTAGE); i < issued; ++i)
+        mbar_wait(smem_u32(&full_bar[i % NSTAGE]), (i / NSTAGE) & 1, p.wait_ns, p.err);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers ---
+  const int g = lane >> 2, t = lane & 3;
+  // Q group as the A operand: rows = query heads h0..h0+G-1 (zero past G).
+  uint32_t qa[D / 16][4];
+  {
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q);
+    const size_t rb0 = ((size_t)b * p.H_q + h0 + g) * (D / 2);
+    const size_t rb1 = rb0 + 8 * (D / 2);
+    const bool v0 = g < G, v1 = g + 8 < G;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int c = kk * 8 + t;  // 32-bit word index of columns (kk*16 + 2t, +1)
+      qa[kk][0] = v0 ? q32[rb0 + c] : 0u;
+      qa[kk][1] = v1 ? q32[rb1 + c] : 0u;
+      qa[kk][2] = v0 ? q32[rb0 + c + 4] : 0u;
+      qa[kk][3] = v1 ? q32[rb1 + c + 4] : 0u;
+    }
+  }
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+
+  // ldmatrix lane roles.  K (non-transposed): matrix mi = lane/8 covers tokens
+  // (mi/2)*8.. and d-chunk (mi%2); V (transposed): tokens (mi%2)*8.., chunk mi/2.
+  const int k_row = warp * 16 + ((lane >> 4) << 3) + (lane & 7);
+  const int k_chk = (lane >> 3) & 1;
+  const int v_row = warp * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
+  const int v_chk = lane >> 4;
+
+  bool aborted = false;
+  for (int i = 0; i < n_tiles; ++i) {
+    const int st = i % NSTAGE;
+    bool ok = *reinterpret_cast<volatile int*>(&abort_flag) == 0;
+    if (ok) ok = mbar_wait(smem_u32(&full_bar[st]), (i / NSTAGE) & 1, p.wait_ns, p.err);
+    // Keep the warp converged for the warp-collective ldmatrix/mma below.
+    if (!__all_sync(0xffffffffu, ok)) {
+      *reinterpret_cast<volatile int*>(&abort_flag) = 1;
+      aborted = true;
+      break;
+    }
+    const uint32_t kbase = smem_base + st * Lay::kStageBytes;
+    const uint32_t vbase = kbase + Lay::kTileBytes;
+    const int tok0 = t0 + i * kTile + warp * 16;  // first token of this warp's slice
+
+    // S = Q K^T over this warp's 16 tokens (two n8 tiles).
+    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      uint32_t b00, b01, b10, b11;
+      ldsm_x4(kbase + Lay::offset(k_row, kk * 2 + k_chk), b00, b01, b10, b11);
+      mma_bf16_16816(sacc[0], qa[kk], b00, b01);
+      mma_bf16_16816(sacc[1], qa[kk], b10, b11);
+    }
+
+    // Scores in base-2 units; tokens past the split end are masked by select.
+    const bool partial = tok0 + 16 > t_end;
+    float x0[4], x1[4];  // row g (x0) and row g+8 (x1)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int tk = tok0 + nt * 8 + 2 * t + c;
+        const bool ok = !partial || tk < t_end;
+        x0[nt * 2 + c] = ok ? sacc[nt][c] * p.scale_log2 : -INFINITY;
+        x1[nt * 2 + c] = ok ? sacc[nt][2 + c] * p.scale_log2 : -INFINITY;
+      }
+    }
+    float p0[4], p1[4] = {0.f, 0.f, 0.f, 0.f};
+    const float a0 = online_update(x0, m0, l0, p0);
+    float a1 = 1.f;
+    if (ROWS16) a1 = online_update(x1, m1, l1, p1);
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      o[n][0] *= a0;
+      o[n][1] *= a0;
+      if (ROWS16) {
+        o[n][2] *= a1;
+        o[n][3] *= a1;
+      }
+    }
+    // P as the A operand of P V (k = this warp's 16 tokens).
+    uint32_t pa[4];
+    pa[0] = pack_bf16x2(p0[0], p0[1]);
+    pa[1] = pack_bf16x2(p1[0], p1[1]);
+    pa[2] = pack_bf16x2(p0[2], p0[3]);
+    pa[3] = pack_bf16x2(p1[2], p1[3]);
+
+    // Values of masked tokens may be anything (even NaN): zero them in the
+    // B fragments so that 0 * V cannot produce NaN.
+    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+    if (partial) {
+      const int tk = tok0 + 2 * t;
+      vm0 = (tk < t_end ? 0x0000ffffu : 0u) | (tk + 1 < t_end ? 0xffff0000u : 0u);
+      vm1 = (tk + 8 < t_end ? 0x0000ffffu : 0u) | (tk + 9 < t_end ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int jj = 0; jj < D / 16; ++jj) {
+      uint32_t v0, v1, v2, v3;
+      ldsm_x4_trans(vbase + Lay::offset(v_row, jj * 2 + v_chk), v0, v1, v2, v3);
+      mma_bf16_16816(o[2 * jj], pa, v0 & vm0, v1 & vm1);
+      mma_bf16_16816(o[2 * jj + 1], pa, v2 & vm0, v3 & vm1);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
+  }
+  (void)aborted;
+
+  l0 = quad_sum(l0);
+  if (ROWS16) l1 = quad_sum(l1);
+
+  // ------------------------------------------- merge the four warp partials --
+  named_bar_sync(1, kConsumerWarps * 32);
+  const bool failed = *reinterpret_cast<volatile int*>(&abort_flag) != 0;
+  float* mO = reinterpret_cast<float*>(smem);  // [warps][16][D]
+  float2* mML = reinterpret_cast<float2*>(smem + kConsumerWarps * 16 * D * 4);  // [warps][16]
+  if (!failed) {
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      const int col = n * 8 + 2 * t;
+      *reinterpret_cast<float2*>(&mO[(warp * 16 + g) * D + col]) = make_float2(o[n][0], o[n][1]);
+      if (ROWS16)
+        *reinterpret_cast<float2*>(&mO[(warp * 16 + g + 8) * D + col]) =
+            make_float2(o[n][2], o[n][3]);
+    }
+    if (t == 0) {
+      mML[warp * 16 + g] = make_float2(m0, l0);
+      if (ROWS16) mML[warp * 16 + g + 8] = make_float2(m1, l1);
+    }
+  }
+  named_bar_sync(1, kConsumerWarps * 32);
+
+  constexpr int V4 = D / 4;
+  for (int e = threadIdx.x; e < G * V4; e += kConsumerWarps * 32) {
+    const int r = e / V4, c4 = e % V4;
+    const size_t row = (size_t)b * p.H_q + h0 + r;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float M = -INFINITY, Lsum = 0.f;
+    if (!failed) {
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mML[w * 16 + r].x);
+      const float ref = (M == -INFINITY) ? 0.f : M;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float2 ml = mML[w * 16 + r];
+        const float a = exp2f(ml.x - ref);
+        Lsum += a * ml.y;
+        const float4 ow = *reinterpret_cast<const float4*>(&mO[(w * 16 + r) * D + c4 * 4]);
+        acc.x += a * ow.x;
+        acc.y += a * ow.y;
+        acc.z += a * ow.z;
+        acc.w += a * ow.w;
+      }
+    } else {
+      M = NAN;
+      Lsum = NAN;
+      acc = make_float4(NAN, NAN, NAN, NAN);
+    }
+    if (p.n_split == 1) {
+      const float inv = 1.f / Lsum;
+      uint2 packed;
+      packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+      packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(&p.out[row * D + c4 * 4]) = packed;
+      if (c4 == 0) p.lse[row] = (M + log2f(Lsum)) * kLn2;
+    } else {
+      const size_t idx = row * p.n_split + split;
+      *reinterpret_cast<float4*>(&p.ws_O[idx * D + c4 * 4]) = acc;
+      if (c4 == 0) p.ws_ml[idx] = make_float2(M * kLn2, Lsum);
+    }
+  }
+}
+
+// -------------------------------------------------------------- combine ----
+// One CTA per (query head, sequence).  Weights of the splits are computed
+// once into shared memory; thread groups of D/4 lanes then sum the weighted
+// O partials of disjoint subsets of splits, and the groups are added last.
+constexpr int kCombineThreads = 128;
+
+__device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float o = __shfl_xor_sync(0xffffffffu, v, off);
+    v = is_max ? fmaxf(v, o) : v + o;
+  }
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  v = red[0];
+#pragma unroll
+  for (int w = 1; w < kCombineThreads / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+  return v;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kCombineThreads)
+    gqa_decode_combine_kernel(const CombineParams p) {
+  extern __shared__ float csm[];  // weights [n_split], then group sums [groups][D]
+  __shared__ float red[kCombineThreads / 32];
+  const int h = blockIdx.x, b = blockIdx.y;
+  const size_t row = (size_t)b * p.H_q + h;
+  const float2* ml = p.ws_ml + row * p.n_split;
+  const float* O = p.ws_O + row * p.n_split * D;
+  float* w_s = csm;
+  constexpr int TPR = D / 4;                        // threads per O row
+  constexpr int GROUPS = kCombineThreads / TPR;
+  float* gsum = csm + ((p.n_split + 3) & ~3);
+
+  // M = max_s m_s; a NaN anywhere poisons the row.
+  float M = -INFINITY;
+  float bad = 0.f;
+  for (int s = threadIdx.x; s < p.n_split; s += kCombineThreads) {
+    const float2 v = ml[s];
+    if (isnan(v.x) || isnan(v.y)) bad = 1.f;
+    M = fmaxf(M, v.x);
+  }
+  M = block_reduce(M, red, true);
+  bad = block_reduce(bad, red, true);
+  const float ref = (M == -INFINITY) ? 0.f : M;
+  float L = 0.f;
+  for (int s = threadIdx.x; s < p.n_split; s += kCombineThreads) {
+    const float2 v = ml[s];
+    const float w = (v.x == -INFINITY) ? 0.f : exp2f((v.x - ref) * kLog2e);
+    w_s[s] = w;
+    L += w * v.y;
+  }
+  L = block_reduce(L, red, false);  // also orders the w_s writes before the reads below
+
+  const int grp = threadIdx.x / TPR, c4 = threadIdx.x % TPR;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = grp; s < p.n_split; s += GROUPS) {
+    const float w = w_s[s];
+    if (w == 0.f) continue;  // empty split: its O is never read
+    const float4 v = *reinterpret_cast<const float4*>(&O[(size_t)s * D + c4 * 4]);
+    acc.x += w * v.x;
+    acc.y += w * v.y;
+    acc.z += w * v.z;
+    acc.w += w * v.w;
+  }
+  *reinterpret_cast<float4*>(&gsum[grp * D + c4 * 4]) = acc;
+  __syncthreads();
+  if (threadIdx.x < TPR) {
+    float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int gi = 0; gi < GROUPS; ++gi) {
+      const float4 v = *reinterpret_cast<const float4*>(&gsum[gi * D + c4 * 4]);
+      tot.x += v.x;
+      tot.y += v.y;
+      tot.z += v.z;
+      tot.w += v.w;
+    }
+    const bool poisoned = bad != 0.f || !(L > 0.f);
+    const float inv = poisoned ? NAN : 1.f / L;
+    uint2 packed;
+    packed.x = pack_bf16x2(tot.x * inv, tot.y * inv);
+    packed.y = pack_bf16x2(tot.z * inv, tot.w * inv);
+    *reinterpret_cast<uint2*>(&p.out[row * D + c4 * 4]) = packed;
+    if (c4 == 0) p.lse[row] = poisoned ? NAN : M + logf(L);
+  }
+}
+
+__global__ void gqa_wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // Nothing ever arrives on `bar`: the wait must give up and flag a timeout.
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, limit_ns, err);
+}
+
+// Raises the dynamic shared-memory limit of `kern` once per device.
+inline cudaError_t set_smem_attr_once(const void* kern, int smem, unsigned char* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;  // benign race: idempotent
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
+  return e;
+}
+
+template <int D, bool ROWS16, int NSTAGE>
+cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                         cudaStream_t stream) {
+  constexpr int smem = decode_smem_bytes<D, NSTAGE>();
+  auto kern = gqa_decode_split_kernel<D, ROWS16, NSTAGE>;
+  static unsigned char done[64];
+  cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem, done);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_split, p.H_kv, p.B);
+  kern<<<grid, kThreads, smem, stream>>>(tm_k, tm_v, p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_split_rows(const DecodeParams& p, const CUtensorMap& tm_k,
+                              const CUtensorMap& tm_v, cudaStream_t stream) {
+  constexpr int NSTAGE = D >= 128 ? 4 : 6;
+  if (p.G > 8) return launch_split<D, true, NSTAGE>(p, tm_k, tm_v, stream);
+  return launch_split<D, false, NSTAGE>(p, tm_k, tm_v, stream);
+}
+
+template <int D>
+cudaError_t launch_comb(const CombineParams& p, cudaStream_t stream) {
+  constexpr int TPR = D / 4;
+  constexpr int GROUPS = kCombineThreads / TPR;
+  const size_t smem = (size_t)(((p.n_split + 3) & ~3) + GROUPS * D) * sizeof(float);
+  auto kern = gqa_decode_combine_kernel<D>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(p.H_q, p.B);
+  kern<<<grid, kCombineThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tm_k,
+                                const CUtensorMap& tm_v, cudaStream_t stream) {
+  switch (p.d) {
+    case 32: return launch_split_rows<32>(p, tm_k, tm_v, stream);
+    case 64: return launch_split_rows<64>(p, tm_k, tm_v, stream);
+    case 128: return launch_split_rows<128>(p, tm_k, tm_v, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_decode_combine(const CombineParams& p, cudaStream_t stream) {
+  switch (p.d) {
+    case 32: return launch_comb<32>(p, stream);
+    case 64: return launch_comb<64>(p, stream);
+    case 128: return launch_comb<128>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t stream) {
+  gqa_wait_selftest_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace gqa

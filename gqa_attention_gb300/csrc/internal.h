@@ -1,0 +1,63 @@
+// internal.h -- parameter blocks and launchers shared between the C-ABI shim
+// (api.cu) and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gqa {
+
+// Bits of the per-device error word.
+enum : unsigned { kErrTimeout = 1u, kErrBadSeqLen = 2u };
+
+constexpr int kDecodeTile = 64;  // tokens per decode pipeline stage; split chunks are multiples
+
+struct DecodeParams {
+  const __nv_bfloat16* q;  // [B, H_q, d]
+  const int32_t* seq_lens; // [B]
+  int B, S_max, H_q, H_kv, G, d;
+  int n_split, chunk;
+  float scale_log2;        // tau * log2(e)
+  float2* ws_ml;           // [B, H_q, n_split]  (m in natural-log units, l)
+  float* ws_O;             // [B, H_q, n_split, d]
+  __nv_bfloat16* out;      // [B, H_q, d]      (n_split == 1)
+  float* lse;              // [B, H_q]         (n_split == 1)
+  unsigned* err;           // device error word
+  uint64_t wait_ns;        // time limit of every pipeline wait
+};
+
+struct CombineParams {
+  const float2* ws_ml;
+  const float* ws_O;
+  int B, H_q, d, n_split;
+  __nv_bfloat16* out;
+  float* lse;
+};
+
+struct PrefillParams {
+  int B, S, H_q, H_kv, G, d;
+  float scale_log2;
+  __nv_bfloat16* out;  // [B, S, H_q, d]
+  float* lse;          // [B, H_q, S]
+  unsigned* err;
+  uint64_t wait_ns;
+};
+
+// Kernel launchers; each returns the launch status (cudaGetLastError).
+cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tm_k,
+                                const CUtensorMap& tm_v, cudaStream_t stream);
+cudaError_t launch_decode_combine(const CombineParams& p, cudaStream_t stream);
+cudaError_t launch_prefill_causal(const PrefillParams& p, const CUtensorMap& tm_q,
+                                  const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                  int num_sms, cudaStream_t stream);
+cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t stream);
+
+// Layout of the decode workspace: byte offset of the O partials.
+inline size_t decode_ws_O_offset(int B, int H_q, int n_split) {
+  size_t ml = (size_t)B * H_q * n_split * sizeof(float2);
+  return (ml + 255) / 256 * 256;
+}
+
+}  // namespace gqa

@@ -1,0 +1,161 @@
+/*
+ * gqa_attn.h -- C ABI of libgqa_attn.so: grouped-query fused attention forward
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("Attention Kernel 계보", p.2 §1 and p.15 §2): for query head h
+ * of a group of G = H_q / H_kv query heads sharing KV head kv = floor(h / G),
+ *     O_h = softmax(tau * q_h K_kv^T) V_kv,   LSE_h = ln sum_j exp(tau * q_h . k_j)
+ * over the visible keys j, computed with the streaming (m, l, O) softmax of p.3
+ * §5 so that the score matrix never reaches memory.  LSE is in natural-log units
+ * of the scaled scores (p.3 §9).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers marked "device" are CUDA device pointers; the caller owns every
+ *   buffer and keeps it alive until the stream work completes.  Tensors are
+ *   dense, row-major, innermost index last, in the layouts given per call.
+ *   bf16 = IEEE bfloat16 (2 bytes), fp32 = IEEE binary32.
+ * - Every call is asynchronous on `stream` (NULL = legacy default stream) and
+ *   never synchronises, except gqa_last_device_error().  The library allocates
+ *   no memory per call; it keeps one 4-byte device error word per device,
+ *   created on first use.
+ * - Arguments that the host can check are checked before anything is launched;
+ *   a failed check returns GQA_ERR_INVALID_ARG or GQA_ERR_UNSUPPORTED and leaves
+ *   every output untouched.  A launch failure returns GQA_ERR_CUDA.
+ * - Faults found on the device (a seq_lens entry out of range, a pipeline wait
+ *   that exceeded its time limit) set bits in the device error word; the
+ *   affected outputs are written as NaN and the call still returns GQA_OK.
+ *   gqa_last_device_error() reports and clears them.
+ * - Device pointers must be 16-byte aligned (tensor-memory-access copies).
+ * - Thread safety: calls on different streams may run concurrently; the only
+ *   shared state is the error word.
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* gqa_stream_t;
+
+typedef enum gqa_status {
+  GQA_OK = 0,
+  GQA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, bad seq_len on device */
+  GQA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. head dim) */
+  GQA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  GQA_ERR_TIMEOUT = 4      /* a device pipeline wait exceeded its time limit */
+} gqa_status;
+
+/* Static, human-readable name of a status code.  Never NULL. */
+const char* gqa_status_str(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int gqa_version(void);
+
+/* ------------------------------------------------------------------------
+ * Split-KV decode ("Attention Kernel 계보", p.18 §4; ADR-0060 §5.1-§5.3)
+ * ------------------------------------------------------------------------
+ * One query token per sequence (T_q = 1) attends keys [0, seq_lens[b]) of a
+ * padded cache.  The keys of each sequence are cut into n_split contiguous
+ * splits of `chunk` tokens, chunk = gqa_attn_decode_split_chunk(S_max, n_split):
+ * split s covers [s*chunk, min((s+1)*chunk, seq_lens[b])) and may be empty.
+ *
+ * Workspace (fp32, device, gqa_attn_decode_workspace_bytes() bytes, caller-
+ * owned) holds one partial per (b, h, s):
+ *   at byte 0:                 float2 ml[B][H_q][n_split] = (m_s, l_s)
+ *   at byte round_up(B*H_q*n_split*8, 256):  float O[B][H_q][n_split][d]
+ * with, over the keys j of split s and scaled scores x_j = tau * q_h . k_j,
+ *   m_s = max_j x_j,  l_s = sum_j exp(x_j - m_s),  O_s = sum_j exp(x_j - m_s) v_j
+ * (unnormalised; "Attention Kernel 계보", p.4 §2, §8).  An empty split is the
+ * merge identity: m_s = -inf, l_s = 0, and its O_s is not written or read.
+ */
+
+/* Tokens per split for a cache of S_max positions cut n_split ways: ceil(S_max/
+ * n_split) rounded up to a multiple of 64.  Returns 0 if an argument is < 1. */
+int gqa_attn_decode_split_chunk(int S_max, int n_split);
+
+/* Workspace bytes for gqa_attn_decode with n_split > 1; 0 if n_split == 1 or an
+ * argument is < 1. */
+size_t gqa_attn_decode_workspace_bytes(int B, int H_q, int d, int n_split);
+
+/* Deterministic split count for a (B, H_kv, S_max, d) decode on the current
+ * device: enough CTAs to fill every SM about twice, no split shorter than
+ * 256 tokens.  Returns >= 1 (1 for invalid input). */
+int gqa_attn_decode_default_splits(int B, int H_kv, int S_max, int d);
+
+/* Stage 1 of split-KV decode.
+ *   q         device bf16 [B, H_q, d]           query (post-RoPE), read only
+ *   k_cache   device bf16 [B, S_max, H_kv, d]   keys, read only
+ *   v_cache   device bf16 [B, S_max, H_kv, d]   values, read only
+ *   seq_lens  device int32 [B], 1 <= seq_lens[b] <= S_max (checked on device:
+ *             a batch with a bad length gets NaN outputs and sets the
+ *             GQA_ERR_INVALID_ARG bit of the error word)
+ *   H_q % H_kv == 0, G = H_q / H_kv <= 16, d in {32, 64, 128}, scale finite > 0
+ *   n_split   >= 1.  n_split == 1: writes out and lse directly, workspace unused
+ *             (may be NULL).  n_split > 1: writes the workspace only; call
+ *             gqa_attn_decode_combine() next on the same stream.
+ *   out       device bf16 [B, H_q, d]     O = sum_j softmax_j v_j
+ *   lse       device fp32 [B, H_q]        LSE = m + ln l
+ * Keys past seq_lens[b] are never used: their cache rows may hold anything. */
+gqa_status gqa_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* seq_lens, int B, int S_max, int H_q, int H_kv, int d,
+                           float scale, int n_split, void* workspace, void* out, float* lse,
+                           gqa_stream_t stream);
+
+/* Stage 2 of split-KV decode: merges the n_split partials of each (b, h) with
+ * the associative merge ("Attention Kernel 계보", p.4 §3-§9; p.18 §4 stage 2):
+ *   M = max_s m_s,  L = sum_s e^(m_s - M) l_s,  O = sum_s e^(m_s - M) O_s / L,
+ *   out = O (bf16), lse = M + ln L (fp32).
+ * Splits with m_s = -inf contribute nothing.  If every split of a row is
+ * empty the row is written as NaN.  Layouts as for gqa_attn_decode; the
+ * workspace may also be filled by the caller in the documented format. */
+gqa_status gqa_attn_decode_combine(const void* workspace, int B, int H_q, int d, int n_split,
+                                   void* out, float* lse, gqa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Causal prefill ("Attention Kernel 계보", p.9 §4 and p.13 §1-§6)
+ * ------------------------------------------------------------------------
+ * S_q = S_kv = S; query row i sees keys j <= i.  Key tiles entirely above the
+ * diagonal are never loaded; only diagonal tiles are masked.
+ *   q     device bf16 [B, S, H_q, d]     read only
+ *   k, v  device bf16 [B, S, H_kv, d]    read only
+ *   H_q % H_kv == 0, d == 128, S >= 1, B >= 1, scale finite > 0
+ *   out   device bf16 [B, S, H_q, d]
+ *   lse   device fp32 [B, H_q, S]
+ */
+gqa_status gqa_attn_prefill_causal(const void* q, const void* k, const void* v, int B, int S,
+                                   int H_q, int H_kv, int d, float scale, void* out, float* lse,
+                                   gqa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics
+ * ------------------------------------------------------------------------ */
+
+/* Synchronises `stream`, reads and clears the current device's error word and
+ * maps it to a status: GQA_ERR_TIMEOUT if a wait timed out, else
+ * GQA_ERR_INVALID_ARG if a device-side argument check failed, else GQA_OK.
+ * GQA_ERR_CUDA if the synchronisation itself failed. */
+gqa_status gqa_last_device_error(gqa_stream_t stream);
+
+/* Sets the time limit, in nanoseconds, of every device pipeline wait launched
+ * afterwards from this process (default 2e9; values < 1000 are raised to 1000).
+ * Returns the previous limit. */
+uint64_t gqa_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Launches one CTA that waits on a pipeline barrier nothing will ever signal,
+ * using the same bounded wait as the kernels, with a limit of `limit_ns`.  The
+ * wait must give up, set the timeout bit and return; a following
+ * gqa_last_device_error() then reports GQA_ERR_TIMEOUT.  Used to test the
+ * failure path without hanging a GPU. */
+gqa_status gqa_selftest_wait_timeout(uint64_t limit_ns, gqa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */
