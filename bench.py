@@ -7,8 +7,9 @@ One step = one pass of the whole path on seeded synthetic inputs:
   * prefill : Llama3-70B-shaped causal GQA prefill, B=1, S=8192, H_q=64,
               H_kv=8, d=128.
 ``value`` is the decode leg's KV-cache throughput (GB/s of K and V bytes read,
-inputs resident in HBM, L2 flushed before every timed decode); the prefill
-leg's TFLOP/s (causal FLOPs only) is reported beside it under ``prefill``.
+inputs resident in HBM; three rotating K/V copies so that no step finds its
+inputs in L2); the prefill leg's TFLOP/s (causal FLOPs only) is reported beside
+it under ``prefill``.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -35,7 +36,6 @@ sys.path.insert(0, ROOT)
 METRIC = "decode KV GB/s (% HBM peak); causal prefill TFLOPS (% bf16 peak)"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-L2_FLUSH_BYTES = 512 * 1024 * 1024
 
 
 def _peaks():
@@ -134,17 +134,19 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------- ours ---
-def _time_events(torch, fn, steps, stream, flush=None, marks=1):
-    """Run fn(ev_list) `steps` times with CUDA events; returns per-step lists of ms."""
-    per = []
-    for _ in range(steps):
-        if flush is not None:
-            flush()
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(marks + 1)]
-        fn(evs)
-        per.append(evs)
-    torch.cuda.synchronize()
-    return [[evs[i].elapsed_time(evs[i + 1]) for i in range(marks)] for evs in per]
+def _time_region(torch, fn, steps, stream):
+    """Events around `steps` back-to-back calls fn(i); returns mean ms per call."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        fn(i)
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+N_KV_COPIES = 3  # 3 x 256 MiB of K/V: consecutive steps never find their inputs in L2
 
 
 def run_ours(args, rank, world, dist):
@@ -163,25 +165,28 @@ def run_ours(args, rank, world, dist):
     dc = inputs.LLAMA70B_DECODE
     q, k, v, lens = inputs.decode_inputs_for(dc, seed=0)
     kv_bytes = 2 * int(lens.sum()) * dc.H_kv * dc.d * 2
-    qd, kd, vd, ld = (x.to(dev) for x in (q, k, v, lens))
+    qd, ld = q.to(dev), lens.to(dev)
+    kds = [k.to(dev) for _ in range(N_KV_COPIES)]
+    vds = [v.to(dev) for _ in range(N_KV_COPIES)]
     n_split = g.gqa_attn_decode_default_splits(dc.B, dc.H_kv, dc.S_max, dc.d)
     ws = g.decode_workspace(dc.B, dc.H_q, dc.d, n_split, dev)
     out = torch.empty(dc.B, dc.H_q, dc.d, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(dc.B, dc.H_q, dtype=torch.float32, device=dev)
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def flush():
-        flush_buf.fill_(1)
+    def split_only(i):
+        st = g.gqa_attn_decode(qd, kds[i % N_KV_COPIES], vds[i % N_KV_COPIES], ld, dc.B,
+                               dc.S_max, dc.H_q, dc.H_kv, dc.d, dc.scale, n_split, ws, out, lse,
+                               stream)
+        if st:
+            raise RuntimeError(f"decode failed: {g.status_str(st)}")
 
-    def decode_step(evs):
-        evs[0].record(stream)
-        st = g.gqa_attn_decode(qd, kd, vd, ld, dc.B, dc.S_max, dc.H_q, dc.H_kv, dc.d, dc.scale,
-                               n_split, ws, out, lse, stream)
-        evs[1].record(stream)
-        st2 = g.gqa_attn_decode_combine(ws, dc.B, dc.H_q, dc.d, n_split, out, lse, stream)
-        evs[2].record(stream)
-        if st or st2:
-            raise RuntimeError(f"decode failed: {g.status_str(st or st2)}")
+    def decode_step(i):
+        # split kernel + combine kernel back to back (the combine may overlap the
+        # split kernel's tail through programmatic dependent launch)
+        split_only(i)
+        st = g.gqa_attn_decode_combine(ws, dc.B, dc.H_q, dc.d, n_split, out, lse, stream)
+        if st:
+            raise RuntimeError(f"combine failed: {g.status_str(st)}")
 
     # ---------------- prefill leg (Llama3-70B causal prefill, S 8192) ----------
     pc = inputs.LLAMA70B_PREFILL_8K
@@ -194,20 +199,18 @@ def run_ours(args, rank, world, dist):
                                            pc.scale, pout, plse, stream) == g.GQA_OK
     torch.cuda.synchronize()
 
-    def prefill_step(evs):
-        evs[0].record(stream)
+    def prefill_step(i):
         st = g.gqa_attn_prefill_causal(pqd, pkd, pvd, pc.B, pc.S, pc.H_q, pc.H_kv, pc.d,
                                        pc.scale, pout, plse, stream)
-        evs[1].record(stream)
         if st:
             raise RuntimeError(f"prefill failed: {g.status_str(st)}")
 
     # ---------------- warm-up ----------------
-    for _ in range(args.warmup):
-        flush()
-        decode_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    for i in range(args.warmup):
+        decode_step(i)
+        split_only(i)
         if prefill_ok:
-            prefill_step([torch.cuda.Event(enable_timing=True) for _ in range(2)])
+            prefill_step(i)
     torch.cuda.synchronize()
     if g.gqa_last_device_error(stream) != g.GQA_OK:
         raise RuntimeError("device error during warm-up")
@@ -218,9 +221,9 @@ def run_ours(args, rank, world, dist):
             dist.barrier()
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
-        dec = _time_events(torch, decode_step, args.steps, stream, flush=flush, marks=2)
-        pre = (_time_events(torch, prefill_step, args.steps, stream, marks=1)
-               if prefill_ok else None)
+        dec_ms = _time_region(torch, decode_step, args.steps, stream)
+        split_ms = _time_region(torch, split_only, args.steps, stream)
+        pre_ms = _time_region(torch, prefill_step, args.steps, stream) if prefill_ok else None
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
@@ -229,10 +232,6 @@ def run_ours(args, rank, world, dist):
     if g.gqa_last_device_error(stream) != g.GQA_OK:
         raise RuntimeError("device error during the timed region")
 
-    split_ms = statistics.mean(x[0] for x in dec)
-    dec_ms = statistics.mean(x[0] + x[1] for x in dec)
-    pre_ms = statistics.mean(x[0] for x in pre) if pre else None
-
     # ---------------- end to end through the C ABI from pinned host buffers -----
     hq, hk, hv, hl = (x.pin_memory() for x in (q, k, v, lens))
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -240,21 +239,18 @@ def run_ours(args, rank, world, dist):
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hl))
     d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
 
-    def e2e_step(evs):
-        evs[0].record(stream)
+    def e2e_step(i):
         qd.copy_(hq, non_blocking=True)
-        kd.copy_(hk, non_blocking=True)
-        vd.copy_(hv, non_blocking=True)
+        kds[0].copy_(hk, non_blocking=True)
+        vds[0].copy_(hv, non_blocking=True)
         ld.copy_(hl, non_blocking=True)
-        decode_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+        decode_step(0)
         hout.copy_(out, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
-        evs[1].record(stream)
 
-    e2e_steps = max(3, min(args.steps, 20))
-    _time_events(torch, e2e_step, 2, stream, flush=flush)
-    e2e = _time_events(torch, e2e_step, e2e_steps, stream, flush=flush)
-    e2e_ms = statistics.mean(x[0] for x in e2e)
+    e2e_steps = max(3, min(args.steps, 50))
+    _time_region(torch, e2e_step, 2, stream)
+    e2e_ms = _time_region(torch, e2e_step, e2e_steps, stream)
 
     # max over ranks
     times = torch.tensor([dec_ms, split_ms, pre_ms or 0.0, e2e_ms], device=dev)
@@ -287,10 +283,14 @@ def run_ours(args, rank, world, dist):
             "decode": {"B": dc.B, "H_q": dc.H_q, "H_kv": dc.H_kv, "d": dc.d, "ctx": dc.S_max,
                        "n_split": n_split, "kv_bytes": kv_bytes,
                        "ms_split_plus_combine": round(dec_ms, 5),
+                       "ms_split_kernel": round(split_ms, 5),
                        "hbm_frac_of_" + peak_kind: round(value / world / hbm_gbs, 4),
                        "hbm_frac_of_nominal_8TBs": round(value / world / 8000.0, 4)},
             "prefill": {"B": pc.B, "S": pc.S, "H_q": pc.H_q, "H_kv": pc.H_kv, "d": pc.d},
-            "l2": "flushed (512 MiB write) before every timed decode; prefill inputs exceed L2",
+            "l2": (f"decode: {N_KV_COPIES} rotating K/V copies ({N_KV_COPIES * kv_bytes >> 20} MiB), "
+                   "each step reads a copy the previous step did not touch; prefill inputs "
+                   "(160 MiB) exceed L2"),
+            "timing": "CUDA events around K back-to-back steps on the launching stream",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "clocks": clocks,
@@ -305,7 +305,7 @@ def run_ours(args, rank, world, dist):
             "traffic": traffic,
             "algorithmic_bytes_per_launch": kv_bytes,
         },
-        "gpu_launches": args.steps * (2 + (1 if prefill_ok else 0)),
+        "gpu_launches": args.steps * (3 + (1 if prefill_ok else 0)),
         "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4)},
@@ -317,21 +317,22 @@ def run_ours(args, rank, world, dist):
             "value": round(world * tflops, 2), "unit": "TFLOP/s", "ms": round(pre_ms, 4),
             "causal_flops": causal_flops,
             "roofline": {"kernel": "gqa_prefill_causal_kernel", "bound": "tensor",
-                         "achieved": round(tflops, 2), "peak": bf16_tf_sus, "unit": "TFLOP/s",
-                         "frac": round(tflops / bf16_tf_sus, 4),
-                         "peak_kind": peak_kind + " (sustained)",
-                         "frac_of_burst": round(tflops / bf16_tf, 4),
+                         "achieved": round(tflops, 2), "peak": bf16_tf, "unit": "TFLOP/s",
+                         "frac": round(tflops / bf16_tf, 4),
+                         "peak_kind": peak_kind + " (burst)",
+                         "frac_of_sustained": round(tflops / bf16_tf_sus, 4),
                          "traffic": _recorded_traffic("prefill_causal_llama70b_s8192.md",
-                                                      ["prefill.cu", "common.cuh", "internal.h"])},
+                                                      ["prefill.cu", "tcgen05.cuh", "common.cuh",
+                                                       "internal.h"])},
         }
     else:
         line["prefill"] = None
-    line["cpu_baseline"] = cpu_baseline(args, sample_only=True) if not args.no_cpu_baseline else None
+    line["cpu_baseline"] = cpu_baseline(args, steps=5) if not args.no_cpu_baseline else None
     return line
 
 
 # ------------------------------------------------------ CPU oracle baseline --
-def cpu_baseline(args, sample_only=True, steps=1):
+def cpu_baseline(args, steps=1):
     """Time the fp64 oracle on the host cores on a bounded sample of the decode workload."""
     import oracle
     from gqa_attention_gb300 import inputs
@@ -390,7 +391,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -57,14 +57,20 @@ def _compile(src: str, obj: str, extra) -> str:
     return r.stderr
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every csrc/*.cu for sm_103a and link libgqa_attn.so; return its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: str = LIB,
+          build_dir: str = BUILD) -> str:
+    """Compile every csrc/*.cu for sm_103a and link libgqa_attn.so; return its path.
+
+    ``extra_flags``, ``lib_path`` and ``build_dir`` let a tuning run build a
+    variant (e.g. ``-DGQA_DECODE_STAGES_D128=4``) beside the default library.
+    """
+    BUILD_, LIB_ = build_dir, lib_path
+    os.makedirs(BUILD_, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     dep_t = _deps_mtime()
     jobs = []
     for src in srcs:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD_, os.path.basename(src)[:-3] + ".o")
         if force or not os.path.exists(obj) or os.path.getmtime(obj) < max(
                 os.path.getmtime(src), dep_t):
             jobs.append((src, obj))
@@ -75,17 +81,17 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
                 msg = f.result()
                 if verbose and msg:
                     print(f"[{os.path.basename(futs[f])}]\n{msg}", file=sys.stderr)
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
-    if jobs or force or not os.path.exists(LIB):
+    objs = [os.path.join(BUILD_, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    if jobs or force or not os.path.exists(LIB_):
         lib64 = os.path.join(cuda_home(), "lib64")
-        tmp = LIB + f".tmp{os.getpid()}"
+        tmp = LIB_ + f".tmp{os.getpid()}"
         cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
                "-Xlinker", f"-rpath,{lib64}", "-Xlinker", "--no-undefined"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}\n{r.stdout}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, LIB_)
+    return LIB_
 
 
 if __name__ == "__main__":

@@ -191,7 +191,6 @@ gqa_status gqa_attn_decode_combine(const void* workspace, int B, int H_q, int d,
   if (!workspace || !out || !lse) return GQA_ERR_INVALID_ARG;
   if (B < 1 || H_q < 1 || n_split < 1 || B > 65535 || H_q > 65535) return GQA_ERR_INVALID_ARG;
   if (!head_dim_ok(d)) return GQA_ERR_UNSUPPORTED;
-  if (n_split > 32768) return GQA_ERR_UNSUPPORTED;  // split weights live in shared memory
   if (!aligned(workspace, 256) || !aligned(out, 16) || !aligned(lse, 4)) return GQA_ERR_INVALID_ARG;
   gqa::CombineParams p;
   p.ws_ml = static_cast<const float2*>(workspace);
@@ -211,7 +210,9 @@ gqa_status gqa_attn_prefill_causal(const void* q, const void* k, const void* v, 
                                    gqa_stream_t stream) {
   if (!q || !k || !v || !out || !lse) return GQA_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
-  if (B > 65535 || H_q > 65535 || !std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  if (B > 65535 || H_q > 65535 || !std::isfinite(scale) || !(scale > 0.f))
+    return GQA_ERR_INVALID_ARG;
+  if ((long long)B * S * H_q > 0x7fffffffLL) return GQA_ERR_INVALID_ARG;
   if (d != 128) return GQA_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
       !aligned(lse, 4))

@@ -17,6 +17,10 @@
 namespace gqa {
 namespace {
 
+#ifndef GQA_DECODE_STAGES_D128
+#define GQA_DECODE_STAGES_D128 3  // 3 x 32 KB stages: two CTAs fit on one SM
+#endif
+
 constexpr int kTile = kDecodeTile;  // tokens per stage
 constexpr int kConsumerWarps = 4;   // 16 tokens each
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
@@ -68,7 +72,7 @@ __device__ __forceinline__ float online_update(float (&x)[4], float& m, float& l
 }
 
 template <int D, bool ROWS16, int NSTAGE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     gqa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
   using Lay = DecodeLayout<D>;
@@ -111,6 +115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t_end = min(t0 + p.chunk, L);
   const int n_tiles = (t_end - t0 + kTile - 1) / kTile;
 
+  // Let a dependent combine launch get scheduled now; it waits for this grid.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
@@ -329,91 +335,103 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // -------------------------------------------------------------- combine ----
-// One CTA per (query head, sequence).  Weights of the splits are computed
-// once into shared memory; thread groups of D/4 lanes then sum the weighted
-// O partials of disjoint subsets of splits, and the groups are added last.
+// One CTA of four warps per (query head, sequence).  Warp w folds splits
+// w, w+4, w+8, ... : each lane loads the (m, l) pair of every split it folds
+// (a broadcast) and its D/32 columns of each O partial, all in one round of
+// loads, then merges them; the four warp results are merged last.  The merge
+// is the associative one of "Attention Kernel 계보" p.4, so the grouping does
+// not change the result beyond rounding.  The kernel may start before the
+// decode kernel ends (programmatic dependent launch); it reads nothing before
+// griddepcontrol.wait.
 constexpr int kCombineThreads = 128;
-
-__device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float o = __shfl_xor_sync(0xffffffffu, v, off);
-    v = is_max ? fmaxf(v, o) : v + o;
-  }
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  v = red[0];
-#pragma unroll
-  for (int w = 1; w < kCombineThreads / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
-  return v;
-}
+constexpr int kCombineWarps = kCombineThreads / 32;
+constexpr int kCombineChunk = 16;  // splits per warp per round of loads
 
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads)
     gqa_decode_combine_kernel(const CombineParams p) {
-  extern __shared__ float csm[];  // weights [n_split], then group sums [groups][D]
-  __shared__ float red[kCombineThreads / 32];
+  constexpr int VEC = D / 32;  // columns per lane
+  __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
+  __shared__ int s_bad[kCombineWarps];
+  __shared__ __align__(16) float s_o[kCombineWarps][D];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x, b = blockIdx.y;
   const size_t row = (size_t)b * p.H_q + h;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const float2* ml = p.ws_ml + row * p.n_split;
-  const float* O = p.ws_O + row * p.n_split * D;
-  float* w_s = csm;
-  constexpr int TPR = D / 4;                        // threads per O row
-  constexpr int GROUPS = kCombineThreads / TPR;
-  float* gsum = csm + ((p.n_split + 3) & ~3);
+  const float* O = p.ws_O + row * p.n_split * D + lane * VEC;
 
-  // M = max_s m_s; a NaN anywhere poisons the row.
-  float M = -INFINITY;
-  float bad = 0.f;
-  for (int s = threadIdx.x; s < p.n_split; s += kCombineThreads) {
-    const float2 v = ml[s];
-    if (isnan(v.x) || isnan(v.y)) bad = 1.f;
-    M = fmaxf(M, v.x);
-  }
-  M = block_reduce(M, red, true);
-  bad = block_reduce(bad, red, true);
-  const float ref = (M == -INFINITY) ? 0.f : M;
-  float L = 0.f;
-  for (int s = threadIdx.x; s < p.n_split; s += kCombineThreads) {
-    const float2 v = ml[s];
-    const float w = (v.x == -INFINITY) ? 0.f : exp2f((v.x - ref) * kLog2e);
-    w_s[s] = w;
-    L += w * v.y;
-  }
-  L = block_reduce(L, red, false);  // also orders the w_s writes before the reads below
-
-  const int grp = threadIdx.x / TPR, c4 = threadIdx.x % TPR;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = grp; s < p.n_split; s += GROUPS) {
-    const float w = w_s[s];
-    if (w == 0.f) continue;  // empty split: its O is never read
-    const float4 v = *reinterpret_cast<const float4*>(&O[(size_t)s * D + c4 * 4]);
-    acc.x += w * v.x;
-    acc.y += w * v.y;
-    acc.z += w * v.z;
-    acc.w += w * v.w;
-  }
-  *reinterpret_cast<float4*>(&gsum[grp * D + c4 * 4]) = acc;
-  __syncthreads();
-  if (threadIdx.x < TPR) {
-    float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int gi = 0; gi < GROUPS; ++gi) {
-      const float4 v = *reinterpret_cast<const float4*>(&gsum[gi * D + c4 * 4]);
-      tot.x += v.x;
-      tot.y += v.y;
-      tot.z += v.z;
-      tot.w += v.w;
+  float M = -INFINITY, L = 0.f, acc[VEC];
+#pragma unroll
+  for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+  bool bad = false;
+  for (int base = warp; base < p.n_split; base += kCombineWarps * kCombineChunk) {
+    float2 mlv[kCombineChunk];
+    float ov[kCombineChunk][VEC];
+#pragma unroll
+    for (int c = 0; c < kCombineChunk; ++c) {
+      const int s = base + kCombineWarps * c;
+      const bool in = s < p.n_split;
+      mlv[c] = in ? ml[s] : make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) ov[c][v] = in ? O[(size_t)s * D + v] : 0.f;
     }
-    const bool poisoned = bad != 0.f || !(L > 0.f);
-    const float inv = poisoned ? NAN : 1.f / L;
-    uint2 packed;
-    packed.x = pack_bf16x2(tot.x * inv, tot.y * inv);
-    packed.y = pack_bf16x2(tot.z * inv, tot.w * inv);
-    *reinterpret_cast<uint2*>(&p.out[row * D + c4 * 4]) = packed;
-    if (c4 == 0) p.lse[row] = poisoned ? NAN : M + logf(L);
+    float cm = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kCombineChunk; ++c) {
+      bad |= isnan(mlv[c].x) || isnan(mlv[c].y);
+      cm = fmaxf(cm, mlv[c].x);
+    }
+    const float Mn = fmaxf(M, cm);
+    const float ref = (Mn == -INFINITY) ? 0.f : Mn;
+    const float a_old = (M == -INFINITY) ? 0.f : exp2f((M - ref) * kLog2e);
+    L *= a_old;
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) acc[v] *= a_old;
+#pragma unroll
+    for (int c = 0; c < kCombineChunk; ++c) {
+      // an empty split (m = -inf) has weight 0 and its O (never written) is not used
+      const bool live = mlv[c].x != -INFINITY;
+      const float w = live ? exp2f((mlv[c].x - ref) * kLog2e) : 0.f;
+      L += w * mlv[c].y;
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) acc[v] += live ? w * ov[c][v] : 0.f;
+    }
+    M = Mn;
   }
+  if (lane == 0) {
+    s_m[warp] = M;
+    s_l[warp] = L;
+    s_bad[warp] = bad;
+  }
+#pragma unroll
+  for (int v = 0; v < VEC; ++v) s_o[warp][lane * VEC + v] = acc[v];
+  __syncthreads();
+  if (warp != 0) return;
+  float Mt = -INFINITY;
+  bool poisoned = false;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) {
+    Mt = fmaxf(Mt, s_m[w]);
+    poisoned |= s_bad[w] != 0;
+  }
+  const float ref = (Mt == -INFINITY) ? 0.f : Mt;
+  float Lt = 0.f, tot[VEC];
+#pragma unroll
+  for (int v = 0; v < VEC; ++v) tot[v] = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) {
+    const float a = (s_m[w] == -INFINITY) ? 0.f : exp2f((s_m[w] - ref) * kLog2e);
+    Lt += a * s_l[w];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) tot[v] += a * s_o[w][lane * VEC + v];
+  }
+  poisoned |= !(Lt > 0.f);  // every split empty, or NaN
+  const float inv = poisoned ? NAN : 1.f / Lt;
+  __nv_bfloat16* dst = p.out + row * D + lane * VEC;
+#pragma unroll
+  for (int v = 0; v < VEC; ++v) dst[v] = __float2bfloat16(tot[v] * inv);
+  if (lane == 0) p.lse[row] = poisoned ? NAN : Mt + logf(Lt);
 }
 
 __global__ void gqa_wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {
@@ -454,24 +472,25 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tm_k, const C
 template <int D>
 cudaError_t launch_split_rows(const DecodeParams& p, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, cudaStream_t stream) {
-  constexpr int NSTAGE = D >= 128 ? 4 : 6;
+  constexpr int NSTAGE = D >= 128 ? GQA_DECODE_STAGES_D128 : 6;
   if (p.G > 8) return launch_split<D, true, NSTAGE>(p, tm_k, tm_v, stream);
   return launch_split<D, false, NSTAGE>(p, tm_k, tm_v, stream);
 }
 
 template <int D>
 cudaError_t launch_comb(const CombineParams& p, cudaStream_t stream) {
-  constexpr int TPR = D / 4;
-  constexpr int GROUPS = kCombineThreads / TPR;
-  const size_t smem = (size_t)(((p.n_split + 3) & ~3) + GROUPS * D) * sizeof(float);
-  auto kern = gqa_decode_combine_kernel<D>;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  dim3 grid(p.H_q, p.B);
-  kern<<<grid, kCombineThreads, smem, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.H_q, p.B);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gqa_decode_combine_kernel<D>, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -1,10 +1,442 @@
-// prefill.cu -- causal grouped-query prefill (placeholder until the tcgen05 kernel lands).
-#include "common.cuh"
-#include "internal.h"
+// prefill.cu -- causal grouped-query prefill on the fifth-generation tensor cores.
+//
+// What it computes (S_q = S_kv): for query row i of head h, O = softmax over
+// keys j <= i of tau * q_i . k_j, times V, with h reading KV head floor(h / G)
+// ("Attention Kernel 계보" p.2 §1, p.13 §1, p.15 §2).  The loop order is FA2's
+// (p.8-p.9): a query tile stays resident while the key/value tiles stream past,
+// the running (m, l, O) state is updated online and O is divided by l once.
+//
+// Work item = (sequence b, KV head, pair of query heads of that KV head's group,
+// 128-row query tile).  The two query heads share every K/V tile the CTA loads
+// (the GQA reuse of p.15 §4/§7), and their two softmaxes alternate with the
+// tensor core: while one warpgroup turns S into P for its head, the tensor core
+// runs the other head's P V and next Q K^T (the two-warpgroup ping-pong of p.11,
+// here with tcgen05 and tensor memory instead of wgmma and registers).
+// Causal block classes (p.13 §2-§4): key tiles past the query tile are never
+// loaded; tiles fully below the diagonal run unmasked; only the diagonal tile
+// is masked, by select.  Items are handed to persistent CTAs heaviest first in
+// a snake order (p.13 §6).
+//
+// Roles (384 threads):
+//   warp 0      TMA producer: Q pair once per item, then K_j, V_j through a
+//               three-slot shared-memory ring.
+//   warp 1      allocates tensor memory; one lane issues every tcgen05.mma:
+//               S_X = Q_X K_j^T and O_X += P_X V_j for X in {A, B}.
+//   warps 2-3   idle.
+//   warps 4-7   softmax + epilogue of head A (thread = one query row).
+//   warps 8-11  softmax + epilogue of head B.
+// Tensor memory (512 columns x 128 lanes, fp32): S_A | S_B | O_A | O_B.
+// Shared memory: Q_A, Q_B, P_A, P_B and three K/V slots, 32 KB each, every
+// tile stored as two 128-row x 128-byte halves with the 128-byte swizzle.
+//
+// O is rescaled only when a row's running maximum grows by more than 2^8
+// (base 2); p = 2^(x - m_ref) then stays <= 2^8, and because l and O always
+// share the same reference m_ref, the final O / l is unchanged (p.3 §5 holds
+// for any reference value, not only the running maximum).
+#include "tcgen05.cuh"
 
 namespace gqa {
-cudaError_t launch_prefill_causal(const PrefillParams&, const CUtensorMap&, const CUtensorMap&,
-                                  const CUtensorMap&, int, cudaStream_t) {
-  return cudaErrorNotSupported;
+namespace {
+
+constexpr int kPThreads = 384;
+constexpr int kSlots = 3;
+constexpr uint32_t kTileB = 128u * 128u * 2u;  // one 128 x 128 bf16 tile
+constexpr uint32_t kHalfB = kTileB / 2;        // 128 rows x 128 bytes
+constexpr uint32_t kOffQ = 0;                  // Q_A, Q_B
+constexpr uint32_t kOffP = 2 * kTileB;         // P_A, P_B
+constexpr uint32_t kOffRing = 4 * kTileB;      // K/V slots
+constexpr uint32_t kPrefillSmem = kOffRing + kSlots * kTileB + 1024;
+constexpr float kRescaleLog2 = 8.f;
+
+struct Item {
+  int b, kv, hp, qt;
+};
+
+// k-th item of this CTA: rounds of `grid` items, alternating direction, items
+// ordered by descending query tile (the heaviest first).
+__device__ __forceinline__ bool item_of(int k, int n_items, int per_qt, int n_qt, int n_pairs,
+                                        int H_kv, Item& it) {
+  const int grid = gridDim.x, cta = blockIdx.x;
+  const int idx = k * grid + ((k & 1) ? (grid - 1 - cta) : cta);
+  if (idx >= n_items) return false;
+  it.qt = n_qt - 1 - idx / per_qt;
+  int r = idx % per_qt;
+  it.hp = r % n_pairs;
+  r /= n_pairs;
+  it.kv = r % H_kv;
+  it.b = r / H_kv;
+  return true;
 }
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    gqa_prefill_causal_kernel(const __grid_constant__ CUtensorMap tm_q,
+                              const __grid_constant__ CUtensorMap tm_k,
+                              const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t q_full, q_empty, drain;
+  __shared__ __align__(8) uint64_t slot_full[kSlots], slot_empty[kSlots];
+  __shared__ __align__(8) uint64_t s_full[2], p_ready[2], o_full[2], o_empty[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int n_qt = (p.S + 127) / 128;
+  const int n_pairs = (p.G + 1) / 2;
+  const int per_qt = p.B * p.H_kv * n_pairs;
+  const int n_items = n_qt * per_qt;
+  const int n_rounds = (n_items + gridDim.x - 1) / gridDim.x;
+  volatile int* abort_v = &abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&q_full), 1);
+    mbar_init(smem_u32(&q_empty), 1);
+    mbar_init(smem_u32(&drain), 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(smem_u32(&slot_full[s]), 1);
+      mbar_init(smem_u32(&slot_empty[s]), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_u32(&s_full[x]), 1);
+      mbar_init(smem_u32(&p_ready[x]), 4);
+      mbar_init(smem_u32(&o_full[x]), 1);
+      mbar_init(smem_u32(&o_empty[x]), 4);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), 512);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  // A bounded wait that also gives up once another role has aborted.
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (*abort_v) return false;
+    if (mbar_wait(smem_u32(bar), parity, p.wait_ns, p.err)) return true;
+    *abort_v = 1;
+    return false;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------- TMA producer --
+    if (lane == 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      uint32_t ring = 0, q_iter = 0;
+      bool ok = true;
+      for (int k = 0; ok && k < n_rounds; ++k) {
+        Item it;
+        if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, it)) continue;
+        const bool pair = 2 * it.hp + 1 < p.G;
+        const int hA = it.kv * p.G + 2 * it.hp;
+        if (q_iter > 0 && !wait(&q_empty, (q_iter - 1) & 1)) break;
+        const uint32_t qb = smem_u32(&q_full);
+        mbar_arrive_expect_tx(qb, pair ? 2 * kTileB : kTileB);
+        for (int dh = 0; dh < 2; ++dh) {
+          tma_load_4d(sb + kOffQ + dh * kHalfB, &tm_q, qb, dh * 64, hA, it.qt * 128, it.b);
+          if (pair)
+            tma_load_4d(sb + kOffQ + kTileB + dh * kHalfB, &tm_q, qb, dh * 64, hA + 1,
+                        it.qt * 128, it.b);
+        }
+        ++q_iter;
+        const int n = it.qt + 1;
+        for (int j = 0; ok && j < n; ++j) {
+          for (int t = 0; t < 2; ++t) {  // K_j then V_j
+            const uint32_t slot = ring % kSlots;
+            if (ring >= kSlots && !wait(&slot_empty[slot], ((ring / kSlots) - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = smem_u32(&slot_full[slot]);
+            mbar_arrive_expect_tx(fb, kTileB);
+            const CUtensorMap* m = t == 0 ? &tm_k : &tm_v;
+            for (int dh = 0; dh < 2; ++dh)
+              tma_load_4d(sb + kOffRing + slot * kTileB + dh * kHalfB, m, fb, dh * 64, it.kv,
+                          j * 128, it.b);
+            ++ring;
+          }
+        }
+      }
+      // No copy may still target shared memory when the CTA exits.
+      for (uint32_t r = ring > kSlots ? ring - kSlots : 0; r < ring; ++r)
+        mbar_wait(smem_u32(&slot_full[r % kSlots]), (r / kSlots) & 1, p.wait_ns, p.err);
+      if (q_iter > 0) mbar_wait(smem_u32(&q_full), (q_iter - 1) & 1, p.wait_ns, p.err);
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t idS = instr_desc_bf16_f32(128, 128, false);
+      constexpr uint32_t idPV = instr_desc_bf16_f32(128, 128, true);
+      auto issue_s = [&](int x, uint32_t slot) {  // S_x = Q_x K^T
+        const uint32_t qa = sb + kOffQ + x * kTileB, kb = sb + kOffRing + slot * kTileB;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfB + (kk & 3) * 32;
+          tc_mma_ss(tmem + 128 * x, smem_desc_sw128(qa + off, 16, 1024),
+                    smem_desc_sw128(kb + off, 16, 1024), idS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int x, uint32_t slot, bool acc) {  // O_x (+)= P_x V
+        const uint32_t pa = sb + kOffP + x * kTileB, vb = sb + kOffRing + slot * kTileB;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t aoff = (kk >> 2) * kHalfB + (kk & 3) * 32;
+          tc_mma_ss(tmem + 256 + 128 * x, smem_desc_sw128(pa + aoff, 16, 1024),
+                    smem_desc_sw128(vb + kk * 2048, kHalfB, 1024), idPV, (acc || kk > 0) ? 1 : 0);
+        }
+      };
+      uint32_t ring = 0, q_iter = 0, pr_ph[2] = {0, 0}, oe_ph[2] = {0, 0};
+      bool o_busy[2] = {false, false};
+      bool ok = true;
+      for (int k = 0; ok && k < n_rounds; ++k) {
+        Item it;
+        if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, it)) continue;
+        const bool pair = 2 * it.hp + 1 < p.G;
+        const int nx = pair ? 2 : 1;
+        const int n = it.qt + 1;
+        if (!wait(&q_full, q_iter & 1)) break;
+        ++q_iter;
+        uint32_t kslot = ring % kSlots;
+        if (!wait(&slot_full[kslot], (ring / kSlots) & 1)) break;
+        ++ring;
+        tc_fence_after();
+        for (int x = 0; x < nx; ++x) {
+          issue_s(x, kslot);
+          tc_commit(smem_u32(&s_full[x]));
+        }
+        tc_commit(smem_u32(&slot_empty[kslot]));
+        if (n == 1) tc_commit(smem_u32(&q_empty));
+        for (int j = 0; ok && j < n; ++j) {
+          const uint32_t vslot = ring % kSlots;
+          if (!wait(&slot_full[vslot], (ring / kSlots) & 1)) {
+            ok = false;
+            break;
+          }
+          ++ring;
+          const bool more = j + 1 < n;
+          for (int x = 0; x < nx; ++x) {
+            if (!wait(&p_ready[x], pr_ph[x])) {
+              ok = false;
+              break;
+            }
+            pr_ph[x] ^= 1;
+            if (j == 0 && o_busy[x]) {  // the previous item's epilogue must have read O_x
+              if (!wait(&o_empty[x], oe_ph[x])) {
+                ok = false;
+                break;
+              }
+              oe_ph[x] ^= 1;
+              o_busy[x] = false;
+            }
+            tc_fence_after();
+            issue_pv(x, vslot, j > 0);
+            if (more) {
+              if (x == 0) {
+                kslot = ring % kSlots;
+                if (!wait(&slot_full[kslot], (ring / kSlots) & 1)) {
+                  ok = false;
+                  break;
+                }
+                ++ring;
+                tc_fence_after();
+              }
+              issue_s(x, kslot);
+              tc_commit(smem_u32(&s_full[x]));
+            } else {
+              tc_commit(smem_u32(&o_full[x]));
+              o_busy[x] = true;
+            }
+          }
+          if (!ok) break;
+          tc_commit(smem_u32(&slot_empty[vslot]));
+          if (more) {
+            tc_commit(smem_u32(&slot_empty[kslot]));
+            if (j + 2 == n) tc_commit(smem_u32(&q_empty));
+          }
+        }
+      }
+      // Every MMA issued here has completed (and every commit has landed)
+      // before tensor memory is released.
+      tc_commit(smem_u32(&drain));
+      mbar_wait(smem_u32(&drain), 0, p.wait_ns, p.err);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------ softmax + epilogue ----
+    const int x = (warp - 4) >> 2;  // 0: head A, 1: head B
+    const int quarter = warp & 3;   // tensor-memory lanes 32*quarter ..
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_base + 128 * x;
+    const uint32_t tO = tmem + lane_base + 256 + 128 * x;
+    const uint32_t pbuf = sb + kOffP + x * kTileB;
+    const float c2 = p.scale_log2;
+    uint32_t s_ph = 0, of_ph = 0;
+    bool alive = true;
+    auto vote_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      const bool ok = wait(bar, parity);
+      return __all_sync(0xffffffffu, ok);
+    };
+    for (int k = 0; alive && k < n_rounds; ++k) {
+      Item it;
+      if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, it)) continue;
+      const bool pair = 2 * it.hp + 1 < p.G;
+      if (x == 1 && !pair) continue;
+      const int h = it.kv * p.G + 2 * it.hp + x;
+      const int n = it.qt + 1;
+      const int q_row = it.qt * 128 + r;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; j < n; ++j) {
+        if (!vote_wait(&s_full[x], s_ph)) {
+          alive = false;
+          break;
+        }
+        s_ph ^= 1;
+        tc_fence_after();
+        uint32_t sr[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+
+        // Diagonal tile: key column c is visible from row r iff c <= r.
+        const bool diag = j == it.qt;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          float v = __uint_as_float(sr[c]);
+          if (diag && c > r) v = -INFINITY;
+          sr[c] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
+        const float m_tile = mx * c2;  // tile maximum of the base-2 scores (c2 > 0)
+        float alpha = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          m_ref = m_tile;
+        } else if (m_tile > m_ref + kRescaleLog2) {
+          alpha = ex2_approx(m_ref - m_tile);
+          m_ref = m_tile;
+          rescale = true;
+        }
+        const float neg = -m_ref;
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const float pv = ex2_approx(fmaf(__uint_as_float(sr[c]), c2, neg));
+          sum += pv;
+          sr[c] = __float_as_uint(pv);
+        }
+        l = l * alpha + sum;
+
+        // O rows of this warp whose reference moved: O *= alpha (O is stable:
+        // the commit that signalled S also covered the previous P V).
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
+            tmem_wait_ld();
+            reg_fence32(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + 32 * c, o);
+          }
+          tmem_wait_st();
+        }
+
+        // P (bf16) into shared memory as a K-major operand with the 128-byte swizzle.
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int qd = 0; qd < 8; ++qd) {
+            const int c0 = hh * 64 + qd * 8;
+            st_shared_v4(pbuf + hh * kHalfB + r * 128 + ((qd ^ (r & 7)) << 4),
+                         pack_bf16x2(__uint_as_float(sr[c0]), __uint_as_float(sr[c0 + 1])),
+                         pack_bf16x2(__uint_as_float(sr[c0 + 2]), __uint_as_float(sr[c0 + 3])),
+                         pack_bf16x2(__uint_as_float(sr[c0 + 4]), __uint_as_float(sr[c0 + 5])),
+                         pack_bf16x2(__uint_as_float(sr[c0 + 6]), __uint_as_float(sr[c0 + 7])));
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&p_ready[x]));
+      }
+      if (!alive) break;
+
+      // Epilogue: O / l in bf16 and LSE = (m_ref + log2 l) * ln 2.
+      if (!vote_wait(&o_full[x], of_ph)) break;
+      of_ph ^= 1;
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const bool store = q_row < p.S;
+      __nv_bfloat16* dst = p.out + ((static_cast<size_t>(it.b) * p.S + q_row) * p.H_q + h) * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * c, o);
+        tmem_wait_ld();
+        reg_fence32(o);
+        if (store) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+            d4[v] = w;
+          }
+        }
+      }
+      if (store)
+        p.lse[(static_cast<size_t>(it.b) * p.H_q + h) * p.S + q_row] = (m_ref + log2f(l)) * kLn2;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&o_empty[x]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_causal(const PrefillParams& p, const CUtensorMap& tm_q,
+                                  const CUtensorMap& tm_k, const CUtensorMap& tm_v, int num_sms,
+                                  cudaStream_t stream) {
+  static unsigned char attr_done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    e = cudaFuncSetAttribute(gqa_prefill_causal_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kPrefillSmem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = 1;
+  }
+  const long long n_items =
+      (long long)((p.S + 127) / 128) * p.B * p.H_kv * ((p.G + 1) / 2);
+  const int grid = (int)(n_items < num_sms ? n_items : num_sms);
+  gqa_prefill_causal_kernel<<<grid, kPThreads, kPrefillSmem, stream>>>(tm_q, tm_k, tm_v, p);
+  return cudaGetLastError();
+}
+
 }  // namespace gqa

@@ -1,0 +1,103 @@
+"""GPU parity of the causal prefill kernel against the fp64 oracle.
+
+Small shapes are compared on every row (several 128-row tiles plus a ragged
+tail); the two full-size workloads are compared on seeded sampled rows, in the
+launch configuration the benchmark times.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_attention_gb300 as g
+from gqa_attention_gb300 import inputs
+
+from parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gqa_attention_gb300 import build
+
+    build.build()
+    g.load()
+    yield
+    assert g.gqa_last_device_error() == g.GQA_OK
+
+
+def _gpu(q, k, v, scale=None):
+    out, lse = g.prefill_causal(q.to(DEV), k.to(DEV), v.to(DEV), scale=scale)
+    torch.cuda.synchronize()
+    return out.cpu(), lse.cpu()
+
+
+@pytest.mark.parametrize("S", [1, 17, 128, 129, 300, 512])
+@pytest.mark.parametrize("H_q,H_kv", [(8, 2), (2, 2), (6, 2), (3, 1)])
+def test_small_shapes_all_rows(oracle_mod, S, H_q, H_kv):
+    B = 2 if S <= 300 else 1
+    q, k, v = inputs.prefill_inputs(B, S, H_q, H_kv, 128, seed=S + H_q)
+    ref_o, ref_l = oracle_mod.prefill_causal_rows(q, k, v, 1 / math.sqrt(128))
+    out, lse = _gpu(q, k, v)
+    assert_parity(out, lse, ref_o, ref_l, f"S={S} H_q={H_q} H_kv={H_kv}")
+
+
+def test_non_default_scale_and_value_range(oracle_mod):
+    q, k, v = inputs.prefill_inputs(1, 260, 4, 2, 128, seed=9, value_scale=2.0)
+    ref_o, ref_l = oracle_mod.prefill_causal_rows(q, k, v, 0.05)
+    out, lse = _gpu(q, k, v, scale=0.05)
+    assert_parity(out, lse, ref_o, ref_l, "scale=0.05")
+
+
+def test_large_scores_trigger_rescaling(oracle_mod):
+    # Every query shares a direction u and the keys move along u with their
+    # position, so each row's running maximum keeps rising (by ~40 in base-2
+    # units over the sequence): the lazy O rescale path runs many times.
+    B, S, H_q, H_kv, d = 1, 640, 2, 1, 128
+    q, k, v = inputs.prefill_inputs(B, S, H_q, H_kv, d, seed=4)
+    gen = torch.Generator().manual_seed(5)
+    u = torch.randn(d, generator=gen)
+    u /= u.norm()
+    ramp = torch.linspace(0, 40, S).view(1, S, 1, 1)
+    q = (q.float() + 8 * u).to(torch.bfloat16)
+    k = (k.float() + ramp * u).to(torch.bfloat16)
+    ref_o, ref_l = oracle_mod.prefill_causal_rows(q, k, v, 1 / math.sqrt(d))
+    assert ref_l[0, 0, -64:].mean() - ref_l[0, 0, :64].mean() > 10  # the maximum keeps rising
+    out, lse = _gpu(q, k, v)
+    assert_parity(out, lse, ref_o, ref_l, "rescale")
+
+
+def test_deterministic_and_in_bounds():
+    B, S, H_q, H_kv, d = 1, 384, 8, 2, 128
+    q, k, v = inputs.prefill_inputs(B, S, H_q, H_kv, d, seed=1)
+    pad = 1 << 16
+    n_o, n_l = B * S * H_q * d, B * H_q * S
+    ob = torch.full((n_o + 2 * pad,), 3.0, dtype=torch.bfloat16, device=DEV)
+    lb = torch.full((n_l + 2 * pad,), 3.0, dtype=torch.float32, device=DEV)
+    outs = []
+    for _ in range(2):
+        out = ob[pad: pad + n_o].view(B, S, H_q, d)
+        lse = lb[pad: pad + n_l].view(B, H_q, S)
+        g.prefill_causal(q.to(DEV), k.to(DEV), v.to(DEV), out=out, lse=lse)
+        torch.cuda.synchronize()
+        outs.append((out.clone(), lse.clone()))
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1], outs[1][1])
+    for buf, n in ((ob, n_o), (lb, n_l)):
+        assert (buf[:pad].float() == 3.0).all() and (buf[pad + n:].float() == 3.0).all()
+
+
+@pytest.mark.parametrize("cfg", inputs.PREFILL_CONFIGS, ids=lambda c: c.name)
+def test_full_size_workloads_on_sampled_rows(oracle_mod, cfg):
+    q, k, v = inputs.prefill_inputs_for(cfg, seed=0)
+    rows = inputs.sample_rows(cfg.S, cfg.oracle_rows or 256, seed=0)
+    ref_o, ref_l = oracle_mod.prefill_causal_rows(q, k, v, cfg.scale, rows=rows)
+    out, lse = _gpu(q, k, v)
+    ridx = rows.numpy()
+    assert_parity(out[:, ridx], lse[:, :, ridx], ref_o, ref_l, cfg.name)
+    assert torch.isfinite(lse).all()
