@@ -205,10 +205,15 @@ def run_ours(args, rank, world, dist):
         if st:
             raise RuntimeError(f"prefill failed: {g.status_str(st)}")
 
+    run_decode = args.only in (None, "decode")
+    if args.only == "decode":
+        prefill_ok = False
+
     # ---------------- warm-up ----------------
     for i in range(args.warmup):
-        decode_step(i)
-        split_only(i)
+        if run_decode:
+            decode_step(i)
+            split_only(i)
         if prefill_ok:
             prefill_step(i)
     torch.cuda.synchronize()
@@ -221,8 +226,8 @@ def run_ours(args, rank, world, dist):
             dist.barrier()
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
-        dec_ms = _time_region(torch, decode_step, args.steps, stream)
-        split_ms = _time_region(torch, split_only, args.steps, stream)
+        dec_ms = _time_region(torch, decode_step, args.steps, stream) if run_decode else float("nan")
+        split_ms = _time_region(torch, split_only, args.steps, stream) if run_decode else float("nan")
         pre_ms = _time_region(torch, prefill_step, args.steps, stream) if prefill_ok else None
         torch.cuda.synchronize()
         if dist is not None:
@@ -249,8 +254,11 @@ def run_ours(args, rank, world, dist):
         hlse.copy_(lse, non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 50))
-    _time_region(torch, e2e_step, 2, stream)
-    e2e_ms = _time_region(torch, e2e_step, e2e_steps, stream)
+    if run_decode:
+        _time_region(torch, e2e_step, 2, stream)
+        e2e_ms = _time_region(torch, e2e_step, e2e_steps, stream)
+    else:
+        e2e_ms = float("nan")
 
     # max over ranks
     times = torch.tensor([dec_ms, split_ms, pre_ms or 0.0, e2e_ms], device=dev)
@@ -395,6 +403,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["decode", "prefill"], default=None,
+                    help="run one leg only (for profiler captures); the JSON line is partial")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -309,17 +309,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
 
-        // Diagonal tile: key column c is visible from row r iff c <= r.
-        const bool diag = j == it.qt;
-        float mx = -INFINITY;
+        // Row maximum.  Diagonal tile: key column c is visible from row r iff
+        // c <= r (select, only on this tile); other tiles are unmasked.
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (j == it.qt) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          float v = __uint_as_float(sr[c]);
-          if (diag && c > r) v = -INFINITY;
-          sr[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          for (int c = 0; c < 128; ++c)
+            if (c > r) sr[c] = __float_as_uint(-INFINITY);
         }
-        const float m_tile = mx * c2;  // tile maximum of the base-2 scores (c2 > 0)
+#pragma unroll
+        for (int c = 0; c < 128; c += 8) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            m4[t] = fmax3(m4[t], __uint_as_float(sr[c + 2 * t]), __uint_as_float(sr[c + 2 * t + 1]));
+        }
+        const float m_tile = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * c2;  // c2 > 0
         float alpha = 1.f;
         bool rescale = false;
         if (j == 0) {
@@ -330,17 +334,32 @@ __global__ void __launch_bounds__(kPThreads, 1)
           rescale = true;
         }
         const float neg = -m_ref;
-        float sum = 0.f;
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const float pv = ex2_approx(fmaf(__uint_as_float(sr[c]), c2, neg));
-          sum += pv;
-          sr[c] = __float_as_uint(pv);
-        }
-        l = l * alpha + sum;
 
-        // O rows of this warp whose reference moved: O *= alpha (O is stable:
-        // the commit that signalled S also covered the previous P V).
+        // P = 2^(x c2 - m_ref), summed in fp32 and written as bf16 into shared
+        // memory (K-major operand, 128-byte swizzle), 8 columns at a time.
+        float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 8) {
+          float e[8];
+#pragma unroll
+          for (int t = 0; t < 8; t += 2)
+            ffma2(e[t], e[t + 1], __uint_as_float(sr[c0 + t]), __uint_as_float(sr[c0 + t + 1]), c2,
+                  c2, neg, neg);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) e[t] = ex2_approx(e[t]);
+          fadd2(sa0, sa1, sa0, sa1, e[0], e[1]);
+          fadd2(sb0, sb1, sb0, sb1, e[2], e[3]);
+          fadd2(sa0, sa1, sa0, sa1, e[4], e[5]);
+          fadd2(sb0, sb1, sb0, sb1, e[6], e[7]);
+          const int hh = c0 >> 6, qd = (c0 & 63) >> 3;
+          st_shared_v4(pbuf + hh * kHalfB + r * 128 + ((qd ^ (r & 7)) << 4), pack_bf16x2(e[0], e[1]),
+                       pack_bf16x2(e[2], e[3]), pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+        }
+        l = l * alpha + ((sa0 + sa1) + (sb0 + sb1));
+
+        // O rows of this warp whose reference moved: O *= alpha.  O is stable:
+        // the commit that signalled S also covered the previous P V; the next
+        // P V is issued only after p_ready below.
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -355,19 +374,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
           tmem_wait_st();
         }
 
-        // P (bf16) into shared memory as a K-major operand with the 128-byte swizzle.
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-          for (int qd = 0; qd < 8; ++qd) {
-            const int c0 = hh * 64 + qd * 8;
-            st_shared_v4(pbuf + hh * kHalfB + r * 128 + ((qd ^ (r & 7)) << 4),
-                         pack_bf16x2(__uint_as_float(sr[c0]), __uint_as_float(sr[c0 + 1])),
-                         pack_bf16x2(__uint_as_float(sr[c0 + 2]), __uint_as_float(sr[c0 + 3])),
-                         pack_bf16x2(__uint_as_float(sr[c0 + 4]), __uint_as_float(sr[c0 + 5])),
-                         pack_bf16x2(__uint_as_float(sr[c0 + 6]), __uint_as_float(sr[c0 + 7])));
-          }
-        }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
