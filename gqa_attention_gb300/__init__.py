@@ -18,6 +18,7 @@ from ._binding import (  # noqa: E402,F401
     gqa_attn_decode,
     gqa_attn_decode_combine,
     gqa_attn_decode_default_splits,
+    gqa_attn_decode_noalloc,
     gqa_attn_decode_split_chunk,
     gqa_attn_decode_workspace_bytes,
     gqa_attn_prefill_causal,

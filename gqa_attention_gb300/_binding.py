@@ -28,6 +28,7 @@ SIGNATURES = {
     "gqa_attn_decode_default_splits": (_I, [_I, _I, _I, _I]),
     "gqa_attn_decode": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
     "gqa_attn_decode_combine": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
+    "gqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
     "gqa_attn_prefill_causal": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "gqa_last_device_error": (_I, [_P]),
     "gqa_set_wait_limit_ns": (_U64, [_U64]),
@@ -106,6 +107,13 @@ def gqa_attn_decode(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale
 
 def gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream=None) -> int:
     return load().gqa_attn_decode_combine(_ptr(workspace), B, H_q, d, n_split, _ptr(out),
+                                          _ptr(lse), _stream(stream))
+
+
+def gqa_attn_decode_noalloc(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale, n_split,
+                            out, lse, stream=None) -> int:
+    return load().gqa_attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+                                          B, S_max, H_q, H_kv, d, scale, n_split, _ptr(out),
                                           _ptr(lse), _stream(stream))
 
 

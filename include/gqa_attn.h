@@ -117,6 +117,34 @@ gqa_status gqa_attn_decode(const void* q, const void* k_cache, const void* v_cac
 gqa_status gqa_attn_decode_combine(const void* workspace, int B, int H_q, int d, int n_split,
                                    void* out, float* lse, gqa_stream_t stream);
 
+/* Split-KV decode that allocates nothing, for callers that cannot call
+ * cudaMalloc when they decode: code inside a CUDA graph capture or an
+ * allocator's critical section, or a serving process whose device memory pool
+ * is fixed up front.  The pages have no counterpart of this entry point; it is
+ * a property of this library's interface.
+ *
+ * Same arguments, layouts, checks and results as gqa_attn_decode() with the
+ * same n_split followed by gqa_attn_decode_combine(), except that the split
+ * partials live in a 16 MiB scratch array inside this library's device image
+ * (present on every GPU that loads the library, until the process exits)
+ * instead of a caller workspace.  The caller still passes q, the caches,
+ * seq_lens, out and lse.
+ *   - If gqa_attn_decode_workspace_bytes(B, H_q, d, n_split) exceeds 16 MiB
+ *     (16777216 bytes) the call returns GQA_ERR_INVALID_ARG before any launch.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.  The first
+ *     call with n_split > 1 on a device looks up the scratch array's device
+ *     address (cudaGetSymbolAddress) with that device current; make that first
+ *     call before any stream capture.
+ *   - Every call shares the one array per device and it keeps the previous
+ *     call's contents.  Nothing in it needs to start at zero: each call writes
+ *     every partial that its combine reads.  Calls whose kernels overlap on the
+ *     GPU (other streams, other host threads) race on the array: order them.
+ *   - n_split == 1 uses no scratch and behaves exactly like gqa_attn_decode. */
+gqa_status gqa_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* seq_lens, int B, int S_max, int H_q, int H_kv,
+                                   int d, float scale, int n_split, void* out, float* lse,
+                                   gqa_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Causal prefill ("Attention Kernel 계보", p.9 §4 and p.13 §1-§6)
  * ------------------------------------------------------------------------
