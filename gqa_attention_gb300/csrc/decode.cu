@@ -477,6 +477,10 @@ cudaError_t launch_split_rows(const DecodeParams& p, const CUtensorMap& tm_k,
   return launch_split<D, false, NSTAGE>(p, tm_k, tm_v, stream);
 }
 
+#ifndef GQA_COMBINE_PDL
+#define GQA_COMBINE_PDL 1  // launch the combine as a programmatic dependent of the split kernel
+#endif
+
 template <int D>
 cudaError_t launch_comb(const CombineParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -488,7 +492,7 @@ cudaError_t launch_comb(const CombineParams& p, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = GQA_COMBINE_PDL ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, gqa_decode_combine_kernel<D>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

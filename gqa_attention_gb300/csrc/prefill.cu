@@ -19,15 +19,18 @@
 //
 // Roles (384 threads):
 //   warp 0      TMA producer: Q pair once per item, then K_j, V_j through a
-//               three-slot shared-memory ring.
-//   warp 1      allocates tensor memory; one lane issues every tcgen05.mma:
+//               five-slot shared-memory ring.
+//   warp 1      allocates tensor memory and issues every tcgen05.mma (the
+//               whole warp runs the loop, one elected lane issues):
 //               S_X = Q_X K_j^T and O_X += P_X V_j for X in {A, B}.
 //   warps 2-3   idle.
 //   warps 4-7   softmax + epilogue of head A (thread = one query row).
 //   warps 8-11  softmax + epilogue of head B.
-// Tensor memory (512 columns x 128 lanes, fp32): S_A | S_B | O_A | O_B.
-// Shared memory: Q_A, Q_B, P_A, P_B and three K/V slots, 32 KB each, every
-// tile stored as two 128-row x 128-byte halves with the 128-byte swizzle.
+// Tensor memory (512 columns x 128 lanes, fp32): S_A | S_B | O_A | O_B; P_X
+// (bf16, two per column) overwrites the first 64 columns of S_X once S_X has
+// been read, and is the tensor-memory A operand of O_X += P_X V.
+// Shared memory: Q_A, Q_B and five K/V slots, 32 KB each, every tile stored as
+// two 128-row x 128-byte halves with the 128-byte swizzle.
 //
 // O is rescaled only when a row's running maximum grows by more than 2^8
 // (base 2); p = 2^(x - m_ref) then stays <= 2^8, and because l and O always
@@ -39,12 +42,11 @@ namespace gqa {
 namespace {
 
 constexpr int kPThreads = 384;
-constexpr int kSlots = 3;
+constexpr int kSlots = 5;
 constexpr uint32_t kTileB = 128u * 128u * 2u;  // one 128 x 128 bf16 tile
 constexpr uint32_t kHalfB = kTileB / 2;        // 128 rows x 128 bytes
 constexpr uint32_t kOffQ = 0;                  // Q_A, Q_B
-constexpr uint32_t kOffP = 2 * kTileB;         // P_A, P_B
-constexpr uint32_t kOffRing = 4 * kTileB;      // K/V slots
+constexpr uint32_t kOffRing = 2 * kTileB;      // K/V slots
 constexpr uint32_t kPrefillSmem = kOffRing + kSlots * kTileB + 1024;
 constexpr float kRescaleLog2 = 8.f;
 
@@ -125,6 +127,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
     return false;
   };
 
+  // The same, taken by every lane of a warp, with one agreed result.
+  auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+    const bool ok = wait(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------- TMA producer --
     if (lane == 0) {
@@ -172,8 +180,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (q_iter > 0) mbar_wait(smem_u32(&q_full), (q_iter - 1) & 1, p.wait_ns, p.err);
     }
   } else if (warp == 1) {
-    // --------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
+    // ------------------------------------------------- MMA issuer (warp 1) --
+    {
       constexpr uint32_t idS = instr_desc_bf16_f32(128, 128, false);
       constexpr uint32_t idPV = instr_desc_bf16_f32(128, 128, true);
       auto issue_s = [&](int x, uint32_t slot) {  // S_x = Q_x K^T
@@ -185,14 +193,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     smem_desc_sw128(kb + off, 16, 1024), idS, kk > 0);
         }
       };
-      auto issue_pv = [&](int x, uint32_t slot, bool acc) {  // O_x (+)= P_x V
-        const uint32_t pa = sb + kOffP + x * kTileB, vb = sb + kOffRing + slot * kTileB;
+      auto issue_pv = [&](int x, uint32_t slot, bool acc) {  // O_x (+)= P_x V, P_x in TMEM
+        const uint32_t vb = sb + kOffRing + slot * kTileB;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kHalfB + (kk & 3) * 32;
-          tc_mma_ss(tmem + 256 + 128 * x, smem_desc_sw128(pa + aoff, 16, 1024),
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_ts(tmem + 256 + 128 * x, tmem + 128 * x + 8 * kk,
                     smem_desc_sw128(vb + kk * 2048, kHalfB, 1024), idPV, (acc || kk > 0) ? 1 : 0);
-        }
       };
       uint32_t ring = 0, q_iter = 0, pr_ph[2] = {0, 0}, oe_ph[2] = {0, 0};
       bool o_busy[2] = {false, false};
@@ -203,10 +209,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const bool pair = 2 * it.hp + 1 < p.G;
         const int nx = pair ? 2 : 1;
         const int n = it.qt + 1;
-        if (!wait(&q_full, q_iter & 1)) break;
+        if (!wait_all(&q_full, q_iter & 1)) break;
         ++q_iter;
         uint32_t kslot = ring % kSlots;
-        if (!wait(&slot_full[kslot], (ring / kSlots) & 1)) break;
+        if (!wait_all(&slot_full[kslot], (ring / kSlots) & 1)) break;
         ++ring;
         tc_fence_after();
         for (int x = 0; x < nx; ++x) {
@@ -217,20 +223,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (n == 1) tc_commit(smem_u32(&q_empty));
         for (int j = 0; ok && j < n; ++j) {
           const uint32_t vslot = ring % kSlots;
-          if (!wait(&slot_full[vslot], (ring / kSlots) & 1)) {
+          if (!wait_all(&slot_full[vslot], (ring / kSlots) & 1)) {
             ok = false;
             break;
           }
           ++ring;
           const bool more = j + 1 < n;
           for (int x = 0; x < nx; ++x) {
-            if (!wait(&p_ready[x], pr_ph[x])) {
+            if (!wait_all(&p_ready[x], pr_ph[x])) {
               ok = false;
               break;
             }
             pr_ph[x] ^= 1;
             if (j == 0 && o_busy[x]) {  // the previous item's epilogue must have read O_x
-              if (!wait(&o_empty[x], oe_ph[x])) {
+              if (!wait_all(&o_empty[x], oe_ph[x])) {
                 ok = false;
                 break;
               }
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (more) {
               if (x == 0) {
                 kslot = ring % kSlots;
-                if (!wait(&slot_full[kslot], (ring / kSlots) & 1)) {
+                if (!wait_all(&slot_full[kslot], (ring / kSlots) & 1)) {
                   ok = false;
                   break;
                 }
@@ -268,6 +274,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       // before tensor memory is released.
       tc_commit(smem_u32(&drain));
       mbar_wait(smem_u32(&drain), 0, p.wait_ns, p.err);
+      __syncwarp();
     }
   } else if (warp >= 4) {
     // ------------------------------------------------ softmax + epilogue ----
@@ -277,14 +284,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_base + 128 * x;
     const uint32_t tO = tmem + lane_base + 256 + 128 * x;
-    const uint32_t pbuf = sb + kOffP + x * kTileB;
     const float c2 = p.scale_log2;
     uint32_t s_ph = 0, of_ph = 0;
     bool alive = true;
-    auto vote_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      const bool ok = wait(bar, parity);
-      return __all_sync(0xffffffffu, ok);
-    };
     for (int k = 0; alive && k < n_rounds; ++k) {
       Item it;
       if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, it)) continue;
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const int q_row = it.qt * 128 + r;
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
-        if (!vote_wait(&s_full[x], s_ph)) {
+        if (!wait_all(&s_full[x], s_ph)) {
           alive = false;
           break;
         }
@@ -335,25 +337,31 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         const float neg = -m_ref;
 
-        // P = 2^(x c2 - m_ref), summed in fp32 and written as bf16 into shared
-        // memory (K-major operand, 128-byte swizzle), 8 columns at a time.
+        // P = 2^(x c2 - m_ref), summed in fp32, and written as packed bf16 over
+        // the first 64 columns of S_x: the A operand of the next P V.  The MMA
+        // that overwrites S_x next is issued after that P V (tcgen05.mma
+        // instructions of one thread execute in issue order).
         float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 8) {
-          float e[8];
+        for (int c0 = 0; c0 < 128; c0 += 16) {
+          uint32_t pk[8];
 #pragma unroll
-          for (int t = 0; t < 8; t += 2)
-            ffma2(e[t], e[t + 1], __uint_as_float(sr[c0 + t]), __uint_as_float(sr[c0 + t + 1]), c2,
-                  c2, neg, neg);
+          for (int g8 = 0; g8 < 16; g8 += 8) {
+            float e[8];
 #pragma unroll
-          for (int t = 0; t < 8; ++t) e[t] = ex2_approx(e[t]);
-          fadd2(sa0, sa1, sa0, sa1, e[0], e[1]);
-          fadd2(sb0, sb1, sb0, sb1, e[2], e[3]);
-          fadd2(sa0, sa1, sa0, sa1, e[4], e[5]);
-          fadd2(sb0, sb1, sb0, sb1, e[6], e[7]);
-          const int hh = c0 >> 6, qd = (c0 & 63) >> 3;
-          st_shared_v4(pbuf + hh * kHalfB + r * 128 + ((qd ^ (r & 7)) << 4), pack_bf16x2(e[0], e[1]),
-                       pack_bf16x2(e[2], e[3]), pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+            for (int t = 0; t < 8; t += 2)
+              ffma2(e[t], e[t + 1], __uint_as_float(sr[c0 + g8 + t]),
+                    __uint_as_float(sr[c0 + g8 + t + 1]), c2, c2, neg, neg);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) e[t] = ex2_approx(e[t]);
+            fadd2(sa0, sa1, sa0, sa1, e[0], e[1]);
+            fadd2(sb0, sb1, sb0, sb1, e[2], e[3]);
+            fadd2(sa0, sa1, sa0, sa1, e[4], e[5]);
+            fadd2(sb0, sb1, sb0, sb1, e[6], e[7]);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) pk[g8 / 2 + t] = pack_bf16x2(e[2 * t], e[2 * t + 1]);
+          }
+          tmem_st8(tS + c0 / 2, pk);
         }
         l = l * alpha + ((sa0 + sa1) + (sb0 + sb1));
 
@@ -374,7 +382,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           tmem_wait_st();
         }
 
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&p_ready[x]));
@@ -382,7 +390,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (!alive) break;
 
       // Epilogue: O / l in bf16 and LSE = (m_ref + log2 l) * ln 2.
-      if (!vote_wait(&o_full[x], of_ph)) break;
+      if (!wait_all(&o_full[x], of_ph)) break;
       of_ph ^= 1;
       tc_fence_after();
       const float inv = 1.f / l;
