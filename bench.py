@@ -134,6 +134,21 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------- ours ---
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of `values` over all ranks (identity when dist is None)."""
+    import torch
+
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_rate(world, units_per_rank, seconds_slowest):
+    """Aggregate throughput: every rank's units over the slowest rank's time."""
+    return world * units_per_rank / seconds_slowest
+
+
 def _time_region(torch, fn, steps, stream):
     """Events around `steps` back-to-back calls fn(i); returns mean ms per call."""
     e0 = torch.cuda.Event(enable_timing=True)
@@ -261,15 +276,13 @@ def run_ours(args, rank, world, dist):
         e2e_ms = float("nan")
 
     # max over ranks
-    times = torch.tensor([dec_ms, split_ms, pre_ms or 0.0, e2e_ms], device=dev)
-    if dist is not None:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    dec_ms, split_ms, pre_ms_max, e2e_ms = (float(x) for x in times.tolist())
+    dec_ms, split_ms, pre_ms_max, e2e_ms = max_over_ranks(
+        [dec_ms, split_ms, pre_ms or 0.0, e2e_ms], dist, dev)
     pre_ms = pre_ms_max if pre_ms is not None else None
     if rank != 0:
         return None
 
-    value = world * kv_bytes / (dec_ms * 1e-3) / 1e9
+    value = whole_job_rate(world, kv_bytes, dec_ms * 1e-3) / 1e9
     achieved = kv_bytes / (split_ms * 1e-3) / 1e9
     traffic = _recorded_traffic("decode_split_llama70b_ctx32768.md",
                                 ["decode.cu", "common.cuh", "internal.h"])
@@ -314,7 +327,8 @@ def run_ours(args, rank, world, dist):
             "algorithmic_bytes_per_launch": kv_bytes,
         },
         "gpu_launches": args.steps * (3 + (1 if prefill_ok else 0)),
-        "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(whole_job_rate(world, kv_bytes, e2e_ms * 1e-3) / 1e9, 2),
+                "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4)},
         "wall_s_timed_region": round(wall_s, 3),
@@ -322,7 +336,8 @@ def run_ours(args, rank, world, dist):
     if pre_ms is not None:
         tflops = causal_flops / (pre_ms * 1e-3) / 1e12
         line["prefill"] = {
-            "value": round(world * tflops, 2), "unit": "TFLOP/s", "ms": round(pre_ms, 4),
+            "value": round(whole_job_rate(world, causal_flops, pre_ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "ms": round(pre_ms, 4),
             "causal_flops": causal_flops,
             "roofline": {"kernel": "gqa_prefill_causal_kernel", "bound": "tensor",
                          "achieved": round(tflops, 2), "peak": bf16_tf, "unit": "TFLOP/s",

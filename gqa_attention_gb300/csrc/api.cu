@@ -122,10 +122,13 @@ size_t gqa_attn_decode_workspace_bytes(int B, int H_q, int d, int n_split) {
 int gqa_attn_decode_default_splits(int B, int H_kv, int S_max, int d) {
   (void)d;
   if (B < 1 || H_kv < 1 || S_max < 1) return 1;
-  const long long ctas = 2LL * num_sms_current_device();   // about two CTAs per SM
-  long long n = (ctas + (long long)B * H_kv - 1) / ((long long)B * H_kv);
-  const long long most = (S_max + 255) / 256;               // splits of >= 256 tokens
-  const long long fill = (S_max + 2047) / 2048;             // and of <= ~2048 tokens
+  // About one CTA per SM (measured best for a single long sequence), with
+  // splits of at least 128 tokens and at most 8192 tokens (ragged batches then
+  // have enough CTAs to balance).
+  const long long groups = (long long)B * H_kv;
+  long long n = (num_sms_current_device() + groups - 1) / groups;
+  const long long most = (S_max + 127) / 128;
+  const long long fill = (S_max + 8191) / 8192;
   if (n > most) n = most;
   if (n < fill) n = fill;
   if (n < 1) n = 1;

@@ -59,10 +59,12 @@ def test_workspace_bytes_formula(lib):
 
 
 def test_default_splits_are_bounded(lib):
-    # no GPU here: the SM count falls back to a default; the bounds still hold
-    for B, H_kv, S in [(1, 2, 1024), (1, 8, 32768), (8, 8, 131072), (64, 8, 64)]:
+    # no GPU here: the SM count falls back to a default; the chunk bounds hold
+    for B, H_kv, S in [(1, 2, 1024), (1, 8, 32768), (8, 8, 131072), (64, 8, 64), (1, 1, 1)]:
         n = g.gqa_attn_decode_default_splits(B, H_kv, S, 128)
-        assert 1 <= n <= max(1, -(-S // 256)) or n == -(-S // 2048)
+        assert 1 <= n <= max(1, -(-S // 128))
+        assert n >= -(-S // 8192)
+    assert g.gqa_attn_decode_default_splits(0, 8, 100, 128) == 1
 
 
 FAKE = 0x10000  # never dereferenced: every case below fails a host check first
