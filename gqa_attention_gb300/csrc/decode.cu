@@ -17,6 +17,13 @@
 namespace gqa {
 namespace {
 
+#ifndef GQA_SPLIT_PDL
+#define GQA_SPLIT_PDL 1  // launch the split kernel as a programmatic dependent
+#endif
+#ifndef GQA_COMBINE_PDL
+#define GQA_COMBINE_PDL 1  // launch the combine as a programmatic dependent of the split kernel
+#endif
+
 #ifndef GQA_DECODE_STAGES_D128
 #define GQA_DECODE_STAGES_D128 3  // 3 x 32 KB stages: two CTAs fit on one SM
 #endif
@@ -89,6 +96,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
   const int h0 = kv * G;
+  // Launched as a programmatic dependent of the previous kernel in the stream:
+  // nothing is read or written before that kernel has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int L = p.seq_lens[b];
 
   // ---- device-side argument check and empty splits (no pipeline needed) ----
@@ -357,6 +367,8 @@ __global__ void __launch_bounds__(kCombineThreads)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x, b = blockIdx.y;
   const size_t row = (size_t)b * p.H_q + h;
+  // A following split kernel may be scheduled now; it waits for this grid.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const float2* ml = p.ws_ml + row * p.n_split;
   const float* O = p.ws_O + row * p.n_split * D + lane * VEC;
@@ -464,8 +476,18 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tm_k, const C
   static unsigned char done[64];
   cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem, done);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_split, p.H_kv, p.B);
-  kern<<<grid, kThreads, smem, stream>>>(tm_k, tm_v, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_split, p.H_kv, p.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = GQA_SPLIT_PDL ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, tm_k, tm_v, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -476,10 +498,6 @@ cudaError_t launch_split_rows(const DecodeParams& p, const CUtensorMap& tm_k,
   if (p.G > 8) return launch_split<D, true, NSTAGE>(p, tm_k, tm_v, stream);
   return launch_split<D, false, NSTAGE>(p, tm_k, tm_v, stream);
 }
-
-#ifndef GQA_COMBINE_PDL
-#define GQA_COMBINE_PDL 1  // launch the combine as a programmatic dependent of the split kernel
-#endif
 
 template <int D>
 cudaError_t launch_comb(const CombineParams& p, cudaStream_t stream) {
