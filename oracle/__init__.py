@@ -17,6 +17,11 @@ computes, with its sources:
   row i sees keys ``[0, i]`` (p.13 §1).
 * :func:`decode_partials`: per-split (m, l, O) with O unnormalised (p.4 §2, §8;
   p.18 §4 stage 1); empty splits are the identity (-inf, 0, 0) (p.4 §9).
+* :func:`prefill_chunk_rows`: a chunk of T_q queries that are the last T_q
+  tokens of each sequence (ADR-0060 §0.5.3 q_block_meta, §5.4): chunk row i of
+  sequence b sits at position a = seq_lens[b] - T_q + i and sees keys
+  a - window <= j <= a (the sliding window of p.13 §7; no lower bound when
+  window < 0).
 * :func:`merge_partials`: the merge m = max, l = a_a l_a + a_b l_b,
   O = a_a O_a + a_b O_b folded over the splits, then O / l and m + ln l
   (p.4 §3, §8; p.18 §4 stage 2).
@@ -64,8 +69,10 @@ def _load():
             lib.orc_decode_partials.argtypes = [P, P, P, I, P, I, I, I, I, I, D, I, I, P, P, P, I]
             lib.orc_merge_partials.argtypes = [P, P, P, L, I, I, P, P]
             lib.orc_prefill_causal_rows.argtypes = [P, P, P, I, I, I, I, I, I, D, P, I, P, P, I]
+            lib.orc_prefill_chunk_rows.argtypes = [P, P, P, I, P, I, I, I, I, I, I, D, I, P, I, P,
+                                                   P, I]
             for f in (lib.orc_decode, lib.orc_decode_partials, lib.orc_merge_partials,
-                      lib.orc_prefill_causal_rows):
+                      lib.orc_prefill_causal_rows, lib.orc_prefill_chunk_rows):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -179,4 +186,36 @@ def prefill_causal_rows(q, k, v, scale, rows=None, nthreads=None):
                                          float(scale), _ptr(ra), n_rows, _ptr(out), _ptr(lse),
                                          _threads(nthreads))
     _check(rc, "prefill_causal_rows")
+    return out, lse
+
+
+def prefill_chunk_rows(q, k, v, scale, seq_lens=None, window=-1, rows=None, nthreads=None):
+    """q [B,T_q,H_q,d]; k,v [B,S_max,H_kv,d]; seq_lens [B] (None: every sequence is S_max).
+
+    Returns (out [B, n_rows, H_q, d], lse [B, H_q, n_rows]) for chunk rows `rows`
+    (default all T_q rows).
+    """
+    qa, qt = _as_input(q)
+    ka, kt = _as_input(k)
+    va, vt = _as_input(v)
+    if not (qt == kt == vt):
+        raise ValueError("q, k, v must share one dtype")
+    B, T_q, H_q, d = qa.shape
+    _, S_max, H_kv, d2 = ka.shape
+    if d2 != d or va.shape != ka.shape:
+        raise ValueError("shape mismatch")
+    sl = None
+    if seq_lens is not None:
+        sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32).reshape(B))
+    if rows is None:
+        rows = np.arange(T_q, dtype=np.int64)
+    ra = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+    n_rows = ra.shape[0]
+    out = np.empty((B, n_rows, H_q, d))
+    lse = np.empty((B, H_q, n_rows))
+    rc = _load().orc_prefill_chunk_rows(_ptr(qa), _ptr(ka), _ptr(va), qt,
+                                        _ptr(sl) if sl is not None else None, B, T_q, S_max, H_q,
+                                        H_kv, d, float(scale), int(window), _ptr(ra), n_rows,
+                                        _ptr(out), _ptr(lse), _threads(nthreads))
+    _check(rc, "prefill_chunk_rows")
     return out, lse

@@ -31,6 +31,8 @@
  *            out [B, H_q, d] (double); lse [B, H_q] (double)
  *   prefill: q [B, S, H_q, d]; k, v [B, S, H_kv, d]; rows [n_rows] (int64 query positions)
  *            out [B, n_rows, H_q, d] (double); lse [B, H_q, n_rows] (double)
+ *   chunk  : q [B, T_q, H_q, d]; k, v [B, S_max, H_kv, d]; seq_lens [B] or NULL;
+ *            rows [n_rows] (chunk row indices); out, lse as for prefill
  *
  * Every entry point returns 0 on success and a negative number for invalid
  * arguments (nothing is written then).
@@ -355,4 +357,68 @@ int orc_prefill_causal_rows(const void* q, const void* k, const void* v, int dty
   pre_ctx c = {q, k, v, dtype, B, S, H_q, H_kv, d, scale, rows, n_rows, max_row, out, lse};
   size_t scratch = (size_t)d + 3 * (size_t)(max_row + 1) * d;
   return run_pool(pre_task, &c, (int64_t)B * H_q, scratch, nthreads);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Chunked prefill with an optional sliding window.                          */
+/* A chunk of T_q query tokens is the last T_q tokens of sequence b, whose    */
+/* length (cache included) is L_b = seq_lens[b] (L_b = S_max when seq_lens is */
+/* NULL): chunk row i sits at absolute position a = L_b - T_q + i and sees    */
+/* keys j with a - W <= j <= a, W = window (no lower bound when window < 0).  */
+/* Sources: ADR-0060 §0.5.3 (q_block_meta {q_start, T_q}) and §5.4 (query     */
+/* block vs key tile causality); "Attention Kernel 계보" p.13 §1 (causal) and */
+/* §7 (sliding window i - W <= j <= i).                                      */
+typedef struct {
+  const void *q, *k, *v;
+  int dtype;
+  const int32_t* seq_lens;
+  int B, T_q, S_max, H_q, H_kv, d, window;
+  double scale;
+  const int64_t* rows;
+  int n_rows;
+  double *out, *lse;
+} chunk_ctx;
+
+static void chunk_task(void* vctx, int64_t task, double* scratch) {
+  chunk_ctx* c = (chunk_ctx*)vctx;
+  int64_t b = task / c->H_q;
+  int h = (int)(task % c->H_q);
+  int kv = h / (c->H_q / c->H_kv);
+  int d = c->d;
+  int64_t L = c->seq_lens ? c->seq_lens[b] : c->S_max;
+  int64_t q0 = L - c->T_q; /* absolute position of chunk row 0 */
+  double* qrow = scratch;
+  double* kh = qrow + d;
+  double* vh = kh + (size_t)c->S_max * d;
+  double* s = vh + (size_t)c->S_max * d;
+  repeat_head(c->k, c->dtype, b, L, c->S_max, c->H_kv, d, kv, kh);
+  repeat_head(c->v, c->dtype, b, L, c->S_max, c->H_kv, d, kv, vh);
+  for (int r = 0; r < c->n_rows; ++r) {
+    int64_t i = c->rows[r];
+    int64_t a = q0 + i;
+    int64_t lo = (c->window >= 0 && a - c->window > 0) ? a - c->window : 0;
+    for (int t = 0; t < d; ++t)
+      qrow[t] = widen(c->q, ((b * c->T_q + i) * c->H_q + h) * d + t, c->dtype);
+    attend_row(qrow, kh + lo * d, vh + lo * d, a - lo + 1, d, c->scale, s,
+               c->out + ((b * c->n_rows + r) * c->H_q + h) * d,
+               c->lse + (b * c->H_q + h) * c->n_rows + r);
+  }
+}
+
+int orc_prefill_chunk_rows(const void* q, const void* k, const void* v, int dtype,
+                           const int32_t* seq_lens, int B, int T_q, int S_max, int H_q, int H_kv,
+                           int d, double scale, int window, const int64_t* rows, int n_rows,
+                           double* out, double* lse, int nthreads) {
+  int rc = check_heads(B, S_max, H_q, H_kv, d);
+  if (rc) return rc;
+  if (dtype != ORC_F64 && dtype != ORC_BF16) return -3;
+  if (T_q < 1 || T_q > S_max || n_rows < 1) return -5;
+  for (int b = 0; seq_lens && b < B; ++b)
+    if (seq_lens[b] < T_q || seq_lens[b] > S_max) return -4;
+  for (int r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= T_q) return -4;
+  chunk_ctx c = {q, k, v, dtype, seq_lens, B, T_q, S_max, H_q, H_kv, d, window, scale,
+                 rows, n_rows, out, lse};
+  size_t scratch = (size_t)d + 3 * (size_t)S_max * d;
+  return run_pool(chunk_task, &c, (int64_t)B * H_q, scratch, nthreads);
 }

@@ -48,6 +48,10 @@ def _golden_cases():
 def test_golden_closed_forms(oracle_mod, case):
     if case["kind"] == "merge":
         out, lse = oracle_mod.merge_partials(_arr(case["m"]), _arr(case["l"]), _arr(case["O"]))
+    elif case["kind"] == "chunk":
+        out, lse = oracle_mod.prefill_chunk_rows(_arr(case["q"]), _arr(case["k"]), _arr(case["v"]),
+                                                 _ev(case["scale"]), seq_lens=case["seq_lens"],
+                                                 window=case["window"])
     elif case["kind"] == "decode":
         out, lse = oracle_mod.decode(_arr(case["q"]), _arr(case["k"]), _arr(case["v"]),
                                      case["seq_lens"], _ev(case["scale"]))
@@ -335,3 +339,80 @@ def test_input_generators_are_seeded_and_padded():
     rows = inputs.sample_rows(1000, 16, seed=0)
     assert rows[0] == 0 and rows[-1] == 999 and len(rows) == 16
     assert torch.equal(rows, inputs.sample_rows(1000, 16, seed=0))
+
+
+# ------------------------------------------- chunked prefill, sliding window ---
+def test_chunk_equal_to_full_prefill_when_it_is_the_whole_sequence(oracle_mod):
+    rng = np.random.default_rng(20)
+    B, S, H_q, H_kv, d = 2, 33, 4, 2, 8
+    q, k, v = (_rand((B, S, H_q, d), rng), _rand((B, S, H_kv, d), rng),
+               _rand((B, S, H_kv, d), rng))
+    a_o, a_l = oracle_mod.prefill_causal_rows(q, k, v, 0.3)
+    b_o, b_l = oracle_mod.prefill_chunk_rows(q, k, v, 0.3)
+    np.testing.assert_allclose(b_o, a_o, atol=1e-14)
+    np.testing.assert_allclose(b_l, a_l, atol=1e-14)
+
+
+def test_chunk_rows_are_the_tail_rows_of_the_full_prefill(oracle_mod):
+    rng = np.random.default_rng(21)
+    B, S_max, T_q, H_q, H_kv, d = 2, 40, 7, 6, 3, 8
+    lens = [40, 23]
+    k, v = _rand((B, S_max, H_kv, d), rng), _rand((B, S_max, H_kv, d), rng)
+    qc = _rand((B, T_q, H_q, d), rng)
+    out, lse = oracle_mod.prefill_chunk_rows(qc, k, v, 0.4, seq_lens=lens)
+    for b, L in enumerate(lens):
+        qf = _rand((1, L, H_q, d), rng)
+        qf[0, L - T_q:] = qc[b]
+        f_o, f_l = oracle_mod.prefill_causal_rows(qf, k[b:b + 1, :L], v[b:b + 1, :L], 0.4,
+                                                  rows=np.arange(L - T_q, L))
+        np.testing.assert_allclose(out[b], f_o[0], atol=1e-13)
+        np.testing.assert_allclose(lse[b], f_l[0], atol=1e-13)
+
+
+def test_single_query_chunk_is_decode(oracle_mod):
+    rng = np.random.default_rng(22)
+    B, S_max, H_q, H_kv, d = 3, 50, 4, 1, 16
+    k, v, q = _rand((B, S_max, H_kv, d), rng), _rand((B, S_max, H_kv, d), rng), _rand((B, H_q, d), rng)
+    lens = [50, 1, 17]
+    c_o, c_l = oracle_mod.prefill_chunk_rows(q[:, None], k, v, 0.25, seq_lens=lens)
+    d_o, d_l = oracle_mod.decode(q, k, v, lens, 0.25)
+    np.testing.assert_allclose(c_o[:, 0], d_o, atol=1e-14)
+    np.testing.assert_allclose(c_l[:, :, 0], d_l, atol=1e-14)
+
+
+def test_window_limits_and_closed_forms(oracle_mod):
+    rng = np.random.default_rng(23)
+    B, S, H_q, H_kv, d = 1, 30, 2, 1, 8
+    q, k, v = (_rand((B, S, H_q, d), rng), _rand((B, S, H_kv, d), rng),
+               _rand((B, S, H_kv, d), rng))
+    full_o, full_l = oracle_mod.prefill_chunk_rows(q, k, v, 0.5)
+    wide_o, wide_l = oracle_mod.prefill_chunk_rows(q, k, v, 0.5, window=S)
+    np.testing.assert_allclose(wide_o, full_o, atol=1e-14)
+    np.testing.assert_allclose(wide_l, full_l, atol=1e-14)
+    # window 0: only the diagonal key
+    o0, l0 = oracle_mod.prefill_chunk_rows(q, k, v, 0.5, window=0)
+    for i in range(S):
+        np.testing.assert_allclose(o0[0, i, 0], v[0, i, 0], atol=1e-14)
+        assert l0[0, 0, i] == pytest.approx(0.5 * q[0, i, 0] @ k[0, i, 0], abs=1e-13)
+    # zero queries: uniform over the window
+    W = 5
+    oz, lz = oracle_mod.prefill_chunk_rows(np.zeros_like(q), k, v, 0.5, window=W)
+    for i in range(S):
+        lo = max(0, i - W)
+        np.testing.assert_allclose(oz[0, i, 1], v[0, lo:i + 1, 0].mean(axis=0), atol=1e-13)
+        assert lz[0, 1, i] == pytest.approx(math.log(i + 1 - lo), abs=1e-13)
+
+
+def test_window_brute_force_decimal(oracle_mod):
+    rng = np.random.default_rng(24)
+    B, S_max, T_q, H_q, H_kv, d, W = 1, 9, 4, 2, 1, 3, 2
+    k, v = _rand((B, S_max, H_kv, d), rng), _rand((B, S_max, H_kv, d), rng)
+    q = _rand((B, T_q, H_q, d), rng)
+    out, lse = oracle_mod.prefill_chunk_rows(q, k, v, 0.7, seq_lens=[8], window=W)
+    for i in range(T_q):
+        a = 8 - T_q + i
+        lo = max(0, a - W)
+        for h in range(H_q):
+            ref_o, ref_l = _brute_decimal(q[0, i, h], k[0, lo:a + 1, 0], v[0, lo:a + 1, 0], 0.7)
+            np.testing.assert_allclose(out[0, i, h], ref_o, rtol=1e-13, atol=1e-14)
+            assert lse[0, h, i] == pytest.approx(ref_l, rel=1e-13, abs=1e-14)
