@@ -22,11 +22,13 @@ from ._binding import (  # noqa: E402,F401
     gqa_attn_decode_split_chunk,
     gqa_attn_decode_workspace_bytes,
     gqa_attn_prefill_causal,
+    gqa_attn_prefill_chunk,
     gqa_last_device_error,
     gqa_selftest_wait_timeout,
     gqa_set_wait_limit_ns,
     load,
     prefill_causal,
+    prefill_chunk,
     split_workspace,
     status_str,
 )

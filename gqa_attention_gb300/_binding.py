@@ -30,6 +30,7 @@ SIGNATURES = {
     "gqa_attn_decode_combine": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "gqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
     "gqa_attn_prefill_causal": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
+    "gqa_attn_prefill_chunk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
     "gqa_last_device_error": (_I, [_P]),
     "gqa_set_wait_limit_ns": (_U64, [_U64]),
     "gqa_selftest_wait_timeout": (_I, [_U64, _P]),
@@ -122,6 +123,13 @@ def gqa_attn_prefill_causal(q, k, v, B, S, H_q, H_kv, d, scale, out, lse, stream
                                           _ptr(out), _ptr(lse), _stream(stream))
 
 
+def gqa_attn_prefill_chunk(q, k_cache, v_cache, seq_lens, B, T_q, S_max, H_q, H_kv, d, scale,
+                           window, out, lse, stream=None) -> int:
+    return load().gqa_attn_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B,
+                                         T_q, S_max, H_q, H_kv, d, scale, int(window), _ptr(out),
+                                         _ptr(lse), _stream(stream))
+
+
 def gqa_last_device_error(stream=None) -> int:
     return load().gqa_last_device_error(_stream(stream))
 
@@ -189,6 +197,24 @@ def prefill_causal(q, k, v, scale=None, out=None, lse=None, stream=None):
         lse = torch.empty((B, H_q, S), dtype=torch.float32, device=q.device)
     _check(gqa_attn_prefill_causal(q, k, v, B, S, H_q, H_kv, d, scale, out, lse, stream),
            "gqa_attn_prefill_causal")
+    return out, lse
+
+
+def prefill_chunk(q, k_cache, v_cache, seq_lens=None, scale=None, window=-1, out=None, lse=None,
+                  stream=None):
+    """Chunk of T_q queries ending each sequence (optionally windowed); returns (out, lse)."""
+    import torch
+
+    B, T_q, H_q, d = q.shape
+    _, S_max, H_kv, _ = k_cache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, T_q, H_q, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H_q, T_q), dtype=torch.float32, device=q.device)
+    _check(gqa_attn_prefill_chunk(q, k_cache, v_cache, seq_lens, B, T_q, S_max, H_q, H_kv, d, scale,
+                                  window, out, lse, stream), "gqa_attn_prefill_chunk")
     return out, lse
 
 

@@ -208,17 +208,25 @@ gqa_status gqa_attn_decode_combine(const void* workspace, int B, int H_q, int d,
   return cuda_status(gqa::launch_decode_combine(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-gqa_status gqa_attn_prefill_causal(const void* q, const void* k, const void* v, int B, int S,
-                                   int H_q, int H_kv, int d, float scale, void* out, float* lse,
-                                   gqa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared checks and launch of the causal prefill kernel: S query rows per
+// sequence against S_kv key rows (chunk: the queries end each sequence).
+gqa_status run_prefill(bool chunk, const void* q, const void* k, const void* v,
+                       const int32_t* seq_lens, int B, int S, int S_kv, int H_q, int H_kv, int d,
+                       float scale, int window, void* out, float* lse, gqa_stream_t stream) {
   if (!q || !k || !v || !out || !lse) return GQA_ERR_INVALID_ARG;
-  if (B < 1 || S < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || S_kv < S || H_q < 1 || H_kv < 1 || H_q % H_kv != 0)
+    return GQA_ERR_INVALID_ARG;
   if (B > 65535 || H_q > 65535 || !std::isfinite(scale) || !(scale > 0.f))
     return GQA_ERR_INVALID_ARG;
-  if ((long long)B * S * H_q > 0x7fffffffLL) return GQA_ERR_INVALID_ARG;
+  if ((long long)B * S * H_q > 0x7fffffffLL || (long long)B * S_kv > 0x7fffffffLL)
+    return GQA_ERR_INVALID_ARG;
   if (d != 128) return GQA_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
-      !aligned(lse, 4))
+      !aligned(lse, 4) || (seq_lens && !aligned(seq_lens, 4)))
     return GQA_ERR_INVALID_ARG;
   unsigned* err = nullptr;
   gqa_status st = error_word(&err);
@@ -228,8 +236,8 @@ gqa_status gqa_attn_prefill_causal(const void* q, const void* k, const void* v, 
   // wide (two boxes per 128-wide row), 128-byte swizzle; K and V likewise.
   const uint64_t dq[4] = {(uint64_t)d, (uint64_t)H_q, (uint64_t)S, (uint64_t)B};
   const uint64_t sq[3] = {(uint64_t)d * 2, (uint64_t)H_q * d * 2, (uint64_t)S * H_q * d * 2};
-  const uint64_t dk[4] = {(uint64_t)d, (uint64_t)H_kv, (uint64_t)S, (uint64_t)B};
-  const uint64_t sk[3] = {(uint64_t)d * 2, (uint64_t)H_kv * d * 2, (uint64_t)S * H_kv * d * 2};
+  const uint64_t dk[4] = {(uint64_t)d, (uint64_t)H_kv, (uint64_t)S_kv, (uint64_t)B};
+  const uint64_t sk[3] = {(uint64_t)d * 2, (uint64_t)H_kv * d * 2, (uint64_t)S_kv * H_kv * d * 2};
   const uint32_t box[4] = {64u, 1u, 128u, 1u};
   CUtensorMap tm_q, tm_k, tm_v;
   if ((st = encode_bf16(&tm_q, q, 4, dq, sq, box, CU_TENSOR_MAP_SWIZZLE_128B)) != GQA_OK) return st;
@@ -239,6 +247,9 @@ gqa_status gqa_attn_prefill_causal(const void* q, const void* k, const void* v, 
   gqa::PrefillParams p;
   p.B = B;
   p.S = S;
+  p.S_kv = S_kv;
+  p.seq_lens = seq_lens;
+  p.window = window < 0 ? -1 : window;
   p.H_q = H_q;
   p.H_kv = H_kv;
   p.G = H_q / H_kv;
@@ -248,8 +259,28 @@ gqa_status gqa_attn_prefill_causal(const void* q, const void* k, const void* v, 
   p.lse = lse;
   p.err = err;
   p.wait_ns = g_wait_ns.load();
-  return cuda_status(gqa::launch_prefill_causal(p, tm_q, tm_k, tm_v, num_sms_current_device(),
-                                                reinterpret_cast<cudaStream_t>(stream)));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int sms = num_sms_current_device();
+  return cuda_status(chunk ? gqa::launch_prefill_chunk(p, tm_q, tm_k, tm_v, sms, s)
+                           : gqa::launch_prefill_causal(p, tm_q, tm_k, tm_v, sms, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+gqa_status gqa_attn_prefill_causal(const void* q, const void* k, const void* v, int B, int S,
+                                   int H_q, int H_kv, int d, float scale, void* out, float* lse,
+                                   gqa_stream_t stream) {
+  return run_prefill(false, q, k, v, nullptr, B, S, S, H_q, H_kv, d, scale, -1, out, lse, stream);
+}
+
+gqa_status gqa_attn_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* seq_lens, int B, int T_q, int S_max, int H_q,
+                                  int H_kv, int d, float scale, int window, void* out, float* lse,
+                                  gqa_stream_t stream) {
+  return run_prefill(true, q, k_cache, v_cache, seq_lens, B, T_q, S_max, H_q, H_kv, d, scale,
+                     window, out, lse, stream);
 }
 
 gqa_status gqa_last_device_error(gqa_stream_t stream) {

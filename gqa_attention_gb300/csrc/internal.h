@@ -37,7 +37,10 @@ struct CombineParams {
 };
 
 struct PrefillParams {
-  int B, S, H_q, H_kv, G, d;
+  int B, S, H_q, H_kv, G, d;  // S: query rows per sequence (T_q of a chunk)
+  int S_kv;                   // key/value rows per sequence in k, v (S_max of a cache)
+  const int32_t* seq_lens;    // [B] sequence lengths (chunk ends), or null: every one is S_kv
+  int window;                 // sliding window W (keys a-W..a), or -1 for none
   float scale_log2;
   __nv_bfloat16* out;  // [B, S, H_q, d]
   float* lse;          // [B, H_q, S]
@@ -52,6 +55,9 @@ cudaError_t launch_decode_combine(const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_prefill_causal(const PrefillParams& p, const CUtensorMap& tm_q,
                                   const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                   int num_sms, cudaStream_t stream);
+cudaError_t launch_prefill_chunk(const PrefillParams& p, const CUtensorMap& tm_q,
+                                 const CUtensorMap& tm_k, const CUtensorMap& tm_v, int num_sms,
+                                 cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t stream);
 
 // Layout of the decode workspace: byte offset of the O partials.

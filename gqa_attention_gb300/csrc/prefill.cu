@@ -36,6 +36,8 @@
 // (base 2); p = 2^(x - m_ref) then stays <= 2^8, and because l and O always
 // share the same reference m_ref, the final O / l is unchanged (p.3 §5 holds
 // for any reference value, not only the running maximum).
+#include <climits>
+
 #include "tcgen05.cuh"
 
 namespace gqa {
@@ -70,6 +72,39 @@ __device__ __forceinline__ bool item_of(int k, int n_items, int per_qt, int n_qt
   return true;
 }
 
+// Key tiles an item visits.  Causal prefill (GENERAL = false): tiles 0..qt.
+// Chunk (GENERAL = true): the chunk is the last S rows of a sequence of L =
+// seq_lens[b] tokens (ADR-0060 §0.5.3 q_block_meta, §5.4), so tile row r sits at
+// absolute position a = (L - S) + 128 qt + r and sees keys a - W .. a; tiles
+// wholly before the window or after the last row are never loaded.  A bad
+// length is replaced by S (all accesses stay in bounds) and the rows get NaN.
+struct Geom {
+  int j0, n, q_off;
+  bool bad;
+};
+template <bool GENERAL>
+__device__ __forceinline__ Geom item_geom(const PrefillParams& p, const Item& it) {
+  Geom g;
+  if (!GENERAL) {
+    g.j0 = 0;
+    g.n = it.qt + 1;
+    g.q_off = 0;
+    g.bad = false;
+    return g;
+  }
+  int L = p.seq_lens ? p.seq_lens[it.b] : p.S_kv;
+  g.bad = L < p.S || L > p.S_kv;
+  if (g.bad) L = p.S;
+  g.q_off = L - p.S;
+  const int first = g.q_off + it.qt * 128;
+  const int last = g.q_off + min(p.S, it.qt * 128 + 128) - 1;
+  const int lo = p.window >= 0 ? max(0, first - p.window) : 0;
+  g.j0 = lo / 128;
+  g.n = last / 128 - g.j0 + 1;
+  return g;
+}
+
+template <bool GENERAL>
 __global__ void __launch_bounds__(kPThreads, 1)
     gqa_prefill_causal_kernel(const __grid_constant__ CUtensorMap tm_q,
                               const __grid_constant__ CUtensorMap tm_k,
@@ -156,7 +191,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         it.qt * 128, it.b);
         }
         ++q_iter;
-        const int n = it.qt + 1;
+        const Geom gm = item_geom<GENERAL>(p, it);
+        const int n = gm.n;
         for (int j = 0; ok && j < n; ++j) {
           for (int t = 0; t < 2; ++t) {  // K_j then V_j
             const uint32_t slot = ring % kSlots;
@@ -169,7 +205,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const CUtensorMap* m = t == 0 ? &tm_k : &tm_v;
             for (int dh = 0; dh < 2; ++dh)
               tma_load_4d(sb + kOffRing + slot * kTileB + dh * kHalfB, m, fb, dh * 64, it.kv,
-                          j * 128, it.b);
+                          (gm.j0 + j) * 128, it.b);
             ++ring;
           }
         }
@@ -208,7 +244,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, it)) continue;
         const bool pair = 2 * it.hp + 1 < p.G;
         const int nx = pair ? 2 : 1;
-        const int n = it.qt + 1;
+        const int n = item_geom<GENERAL>(p, it).n;
         if (!wait_all(&q_full, q_iter & 1)) break;
         ++q_iter;
         uint32_t kslot = ring % kSlots;
@@ -286,6 +322,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t tO = tmem + lane_base + 256 + 128 * x;
     const float c2 = p.scale_log2;
     uint32_t s_ph = 0, of_ph = 0;
+    uint32_t ring_base = 0;  // ring position of this item's K_0 (chunk mode bookkeeping)
     bool alive = true;
     for (int k = 0; alive && k < n_rounds; ++k) {
       Item it;
@@ -293,7 +330,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const bool pair = 2 * it.hp + 1 < p.G;
       if (x == 1 && !pair) continue;
       const int h = it.kv * p.G + 2 * it.hp + x;
-      const int n = it.qt + 1;
+      const Geom gm = item_geom<GENERAL>(p, it);
+      const int n = gm.n;
       const int q_row = it.qt * 128 + r;
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
@@ -314,10 +352,23 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // Row maximum.  Diagonal tile: key column c is visible from row r iff
         // c <= r (select, only on this tile); other tiles are unmasked.
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (j == it.qt) {
+        if (!GENERAL) {
+          if (j == it.qt) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c > r) sr[c] = __float_as_uint(-INFINITY);
+            for (int c = 0; c < 128; ++c)
+              if (c > r) sr[c] = __float_as_uint(-INFINITY);
+          }
+        } else {
+          // key 128*jt + c is visible from row r iff du + r - W <= c <= du + r
+          const int du = gm.q_off + 128 * (it.qt - gm.j0 - j);
+          const bool upper = du < 127;
+          const bool lower = p.window >= 0 && du + 127 - p.window > 0;
+          if (upper || lower) {
+            const int hi = du + r, lo = p.window >= 0 ? du + r - p.window : INT_MIN;
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c > hi || c < lo) sr[c] = __float_as_uint(-INFINITY);
+          }
         }
 #pragma unroll
         for (int c = 0; c < 128; c += 8) {
@@ -328,14 +379,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const float m_tile = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * c2;  // c2 > 0
         float alpha = 1.f;
         bool rescale = false;
-        if (j == 0) {
+        // First tile (causal: key 0 is always visible), or, in chunk mode, no
+        // visible key in this row so far (l and O are 0, nothing to rescale).
+        if (GENERAL ? m_ref == -INFINITY : j == 0) {
           m_ref = m_tile;
         } else if (m_tile > m_ref + kRescaleLog2) {
           alpha = ex2_approx(m_ref - m_tile);
           m_ref = m_tile;
           rescale = true;
         }
-        const float neg = -m_ref;
+        const float neg = (GENERAL && m_ref == -INFINITY) ? 0.f : -m_ref;
 
         // P = 2^(x c2 - m_ref), summed in fp32, and written as packed bf16 over
         // the first 64 columns of S_x: the A operand of the next P V.  The MMA
@@ -382,6 +435,29 @@ __global__ void __launch_bounds__(kPThreads, 1)
           tmem_wait_st();
         }
 
+        // Chunk mode: cache rows at or past the sequence end may hold anything
+        // (even NaN) and 0 * NaN would reach O through P V, so head A's
+        // warps zero those rows of the last V tile before P is released (the
+        // MMA issues head B's P V only after head A's).
+        if (GENERAL && x == 0 && j == n - 1) {
+          const int jt = gm.j0 + j;
+          const int L_eff = gm.q_off + p.S;
+          if (128 * jt + 127 >= L_eff) {
+            const uint32_t pos = ring_base + 2 * j + 1;
+            if (!wait_all(&slot_full[pos % kSlots], (pos / kSlots) & 1)) {
+              alive = false;
+              break;
+            }
+            if (128 * jt + r >= L_eff) {
+              const uint32_t row = sb + kOffRing + (pos % kSlots) * kTileB + r * 128;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int c16 = 0; c16 < 8; ++c16) st_shared_v4(row + hh * kHalfB + c16 * 16, 0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -393,8 +469,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (!wait_all(&o_full[x], of_ph)) break;
       of_ph ^= 1;
       tc_fence_after();
-      const float inv = 1.f / l;
+      const float inv = (GENERAL && gm.bad) ? NAN : 1.f / l;
       const bool store = q_row < p.S;
+      if (GENERAL && gm.bad && x == 0 && warp == 4 && lane == 0) atomicOr(p.err, kErrBadSeqLen);
       __nv_bfloat16* dst = p.out + ((static_cast<size_t>(it.b) * p.S + q_row) * p.H_q + h) * 128;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
@@ -416,10 +493,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
       }
       if (store)
-        p.lse[(static_cast<size_t>(it.b) * p.H_q + h) * p.S + q_row] = (m_ref + log2f(l)) * kLn2;
+        p.lse[(static_cast<size_t>(it.b) * p.H_q + h) * p.S + q_row] =
+            (GENERAL && gm.bad) ? NAN : (m_ref + log2f(l)) * kLn2;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&o_empty[x]));
+      if (GENERAL) ring_base += 2 * n;
     }
   }
 
@@ -431,26 +510,37 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
 }
 
+template <bool GENERAL>
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                           const CUtensorMap& tm_v, int num_sms, cudaStream_t stream) {
+  static unsigned char attr_done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  auto kern = gqa_prefill_causal_kernel<GENERAL>;
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrefillSmem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = 1;
+  }
+  const long long n_items = (long long)((p.S + 127) / 128) * p.B * p.H_kv * ((p.G + 1) / 2);
+  const int grid = (int)(n_items < num_sms ? n_items : num_sms);
+  kern<<<grid, kPThreads, kPrefillSmem, stream>>>(tm_q, tm_k, tm_v, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_causal(const PrefillParams& p, const CUtensorMap& tm_q,
                                   const CUtensorMap& tm_k, const CUtensorMap& tm_v, int num_sms,
                                   cudaStream_t stream) {
-  static unsigned char attr_done[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    e = cudaFuncSetAttribute(gqa_prefill_causal_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kPrefillSmem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = 1;
-  }
-  const long long n_items =
-      (long long)((p.S + 127) / 128) * p.B * p.H_kv * ((p.G + 1) / 2);
-  const int grid = (int)(n_items < num_sms ? n_items : num_sms);
-  gqa_prefill_causal_kernel<<<grid, kPThreads, kPrefillSmem, stream>>>(tm_q, tm_k, tm_v, p);
-  return cudaGetLastError();
+  return launch_prefill<false>(p, tm_q, tm_k, tm_v, num_sms, stream);
+}
+
+cudaError_t launch_prefill_chunk(const PrefillParams& p, const CUtensorMap& tm_q,
+                                 const CUtensorMap& tm_k, const CUtensorMap& tm_v, int num_sms,
+                                 cudaStream_t stream) {
+  return launch_prefill<true>(p, tm_q, tm_k, tm_v, num_sms, stream);
 }
 
 }  // namespace gqa

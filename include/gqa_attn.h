@@ -163,6 +163,31 @@ gqa_status gqa_attn_prefill_causal(const void* q, const void* k, const void* v, 
                                    int H_q, int H_kv, int d, float scale, void* out, float* lse,
                                    gqa_stream_t stream);
 
+/* Chunked prefill / multi-token decode with an optional sliding window
+ * (ADR-0060 §0.5.3 q_block_meta {q_start, T_q} and §5.4; "Attention Kernel
+ * 계보", p.13 §1 and §7).  The T_q queries of sequence b are its last T_q tokens:
+ * with L_b = seq_lens[b] (the cache already holds their keys and values),
+ * query row i sits at position a = L_b - T_q + i and sees keys j with
+ * a - window <= j <= a (no lower bound when window < 0).  Key tiles wholly
+ * outside every row's range are never loaded; tiles that cross a range edge
+ * are masked by select.
+ *   q         device bf16 [B, T_q, H_q, d]
+ *   k_cache,
+ *   v_cache   device bf16 [B, S_max, H_kv, d]; rows >= L_b are not read
+ *   seq_lens  device int32 [B] with T_q <= L_b <= S_max, or NULL (every L_b =
+ *             S_max).  A bad L_b is caught on the device: that sequence's
+ *             rows are NaN and the GQA_ERR_INVALID_ARG error bit is set.
+ *   H_q % H_kv == 0, d == 128, 1 <= T_q <= S_max, scale finite > 0
+ *   out       device bf16 [B, T_q, H_q, d]
+ *   lse       device fp32 [B, H_q, T_q]
+ * With seq_lens == NULL, T_q == S_max and window < 0 this is exactly
+ * gqa_attn_prefill_causal(); window >= 0 with seq_lens == NULL and T_q ==
+ * S_max is a sliding-window causal prefill. */
+gqa_status gqa_attn_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* seq_lens, int B, int T_q, int S_max, int H_q,
+                                  int H_kv, int d, float scale, int window, void* out, float* lse,
+                                  gqa_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Diagnostics
  * ------------------------------------------------------------------------ */

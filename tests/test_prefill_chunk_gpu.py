@@ -1,0 +1,119 @@
+"""GPU parity of chunked prefill (queries ending a cached sequence) and of the
+sliding-window mask, against the fp64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_attention_gb300 as g
+from gqa_attention_gb300 import inputs
+
+from parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gqa_attention_gb300 import build
+
+    build.build()
+    g.load()
+    yield
+    assert g.gqa_last_device_error() == g.GQA_OK
+
+
+def _chunk_inputs(B, T_q, S_max, H_q, H_kv, lens, seed):
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, T_q, H_q, 128, generator=gen).to(torch.bfloat16)
+    k = torch.randn(B, S_max, H_kv, 128, generator=gen).to(torch.bfloat16)
+    v = torch.randn(B, S_max, H_kv, 128, generator=gen).to(torch.bfloat16)
+    for b, L in enumerate(lens):  # rows past each sequence must never be read
+        k[b, L:] = float("nan")
+        v[b, L:] = float("nan")
+    return q, k, v, torch.tensor(lens, dtype=torch.int32)
+
+
+def _gpu(q, k, v, lens, window):
+    out, lse = g.prefill_chunk(q.to(DEV), k.to(DEV), v.to(DEV),
+                               None if lens is None else lens.to(DEV), window=window)
+    torch.cuda.synchronize()
+    return out.cpu(), lse.cpu()
+
+
+@pytest.mark.parametrize("T_q,S_max,lens", [(1, 300, [300, 1]), (5, 300, [5, 299]),
+                                             (128, 1000, [1000, 128]), (200, 1000, [777, 1000]),
+                                             (300, 300, [300, 300])])
+@pytest.mark.parametrize("window", [-1, 0, 1, 127, 128, 300])
+def test_chunk_small_shapes(oracle_mod, T_q, S_max, lens, window):
+    q, k, v, sl = _chunk_inputs(2, T_q, S_max, 8, 2, lens, seed=T_q + S_max + window)
+    ref_o, ref_l = oracle_mod.prefill_chunk_rows(q, k, v, 1 / math.sqrt(128), seq_lens=sl,
+                                                 window=window)
+    out, lse = _gpu(q, k, v, sl, window)
+    assert_parity(out, lse, ref_o, ref_l, f"T_q={T_q} S_max={S_max} lens={lens} W={window}")
+
+
+@pytest.mark.parametrize("H_q,H_kv", [(2, 2), (3, 1)])
+def test_chunk_odd_groups(oracle_mod, H_q, H_kv):
+    q, k, v, sl = _chunk_inputs(1, 130, 400, H_q, H_kv, [333], seed=3)
+    ref_o, ref_l = oracle_mod.prefill_chunk_rows(q, k, v, 1 / math.sqrt(128), seq_lens=sl,
+                                                 window=100)
+    out, lse = _gpu(q, k, v, sl, 100)
+    assert_parity(out, lse, ref_o, ref_l, f"H_q={H_q} H_kv={H_kv}")
+
+
+def test_chunk_without_lengths_is_the_causal_prefill_bit_for_bit():
+    q, k, v = inputs.prefill_inputs(1, 700, 8, 2, 128, seed=6)
+    a_o, a_l = g.prefill_causal(q.to(DEV), k.to(DEV), v.to(DEV))
+    b_o, b_l = g.prefill_chunk(q.to(DEV), k.to(DEV), v.to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(a_o.view(torch.int16), b_o.view(torch.int16))
+    assert torch.equal(a_l, b_l)
+
+
+def test_chunk_bad_length_gives_nan_and_error_word():
+    q, k, v, sl = _chunk_inputs(2, 64, 256, 4, 2, [256, 100], seed=2)
+    sl[1] = 63  # shorter than the chunk
+    out, lse = _gpu(q, k, v, sl, -1)
+    assert g.gqa_last_device_error() == g.GQA_ERR_INVALID_ARG
+    assert torch.isnan(out[1].float()).all() and torch.isnan(lse[1]).all()
+    assert torch.isfinite(out[0].float()).all()
+
+
+def test_chunk_rejects_bad_host_arguments():
+    x = torch.empty(16, dtype=torch.bfloat16, device=DEV)
+    st = g.gqa_attn_prefill_chunk(x, x, x, None, 1, 300, 200, 8, 2, 128, 0.1, -1, x, x)
+    assert st == g.GQA_ERR_INVALID_ARG  # T_q > S_max
+    st = g.gqa_attn_prefill_chunk(x, x, x, None, 1, 10, 200, 8, 2, 64, 0.1, -1, x, x)
+    assert st == g.GQA_ERR_UNSUPPORTED  # d != 128
+
+
+def test_sliding_window_prefill_8k_sampled_rows(oracle_mod):
+    cfg = inputs.LLAMA70B_PREFILL_8K
+    q, k, v = inputs.prefill_inputs_for(cfg, seed=1)
+    rows = inputs.sample_rows(cfg.S, 128, seed=1)
+    W = 4096
+    ref_o, ref_l = oracle_mod.prefill_chunk_rows(q, k, v, cfg.scale, window=W, rows=rows)
+    out, lse = _gpu(q, k, v, None, W)
+    r = rows.numpy()
+    assert_parity(out[:, r], lse[:, :, r], ref_o, ref_l, "window 4096 over 8K")
+
+
+def test_chunk_2048_at_the_end_of_a_32k_cache_sampled_rows(oracle_mod):
+    B, T_q, S_max, H_q, H_kv = 1, 2048, 32768, 64, 8
+    gen = torch.Generator().manual_seed(9)
+    q = torch.randn(B, T_q, H_q, 128, generator=gen).to(torch.bfloat16)
+    k = torch.randn(B, S_max, H_kv, 128, generator=gen).to(torch.bfloat16)
+    v = torch.randn(B, S_max, H_kv, 128, generator=gen).to(torch.bfloat16)
+    sl = torch.tensor([30000], dtype=torch.int32)
+    rows = inputs.sample_rows(T_q, 64, seed=2)
+    ref_o, ref_l = oracle_mod.prefill_chunk_rows(q, k, v, 1 / math.sqrt(128), seq_lens=sl,
+                                                 rows=rows)
+    out, lse = _gpu(q, k, v, sl, -1)
+    r = rows.numpy()
+    assert_parity(out[:, r], lse[:, :, r], ref_o, ref_l, "chunk 2048 @ 30000")
+    assert np.isfinite(lse.numpy()).all()
