@@ -354,6 +354,106 @@ def run_ours(args, rank, world, dist):
     return line
 
 
+# ---------------------------------------------------- further workloads ---
+WORKLOADS = ("decode_tiny", "decode_ragged", "prefill_64k", "prefill_window", "prefill_chunk")
+
+
+def run_workload(name, args):
+    """One JSON line for a workload other than the headline step (same timing rules)."""
+    import torch
+
+    import gqa_attention_gb300 as g
+    from gqa_attention_gb300 import inputs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    g.load()
+    stream = torch.cuda.current_stream()
+    hbm_gbs, bf16_tf, _, peak_kind = _peaks()
+    steps = max(1, args.steps)
+
+    def timed(fn):
+        for i in range(max(3, args.warmup)):
+            fn(i)
+        torch.cuda.synchronize()
+        ms = _time_region(torch, fn, steps, stream)
+        if g.gqa_last_device_error(stream) != g.GQA_OK:
+            raise RuntimeError("device error")
+        return ms
+
+    if name.startswith("decode"):
+        cfg = inputs.TINY_DECODE if name == "decode_tiny" else inputs.LLAMA70B_DECODE_RAGGED
+        q, k, v, lens = inputs.decode_inputs_for(cfg, seed=0)
+        kv_bytes = 2 * int(lens.sum()) * cfg.H_kv * cfg.d * 2
+        copies = 1 if kv_bytes > 512 << 20 else 3
+        qd, ld = q.to(dev), lens.to(dev)
+        kds = [k.to(dev) for _ in range(copies)]
+        vds = [v.to(dev) for _ in range(copies)]
+        n = g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, cfg.d)
+        ws = g.decode_workspace(cfg.B, cfg.H_q, cfg.d, n, dev)
+        out = torch.empty(cfg.B, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(cfg.B, cfg.H_q, dtype=torch.float32, device=dev)
+
+        def step(i):
+            c = i % copies
+            assert g.gqa_attn_decode(qd, kds[c], vds[c], ld, cfg.B, cfg.S_max, cfg.H_q, cfg.H_kv,
+                                     cfg.d, cfg.scale, n, ws, out, lse, stream) == g.GQA_OK
+            if n > 1:
+                assert g.gqa_attn_decode_combine(ws, cfg.B, cfg.H_q, cfg.d, n, out, lse,
+                                                 stream) == g.GQA_OK
+
+        ms = timed(step)
+        gbs = kv_bytes / (ms * 1e-3) / 1e9
+        return {"metric": f"decode KV GB/s ({cfg.name})", "value": round(gbs, 2), "unit": "GB/s",
+                "ms_per_step": round(ms, 5), "steps": steps, "n_split": n, "kv_bytes": kv_bytes,
+                "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
+                "l2": f"{copies} rotating K/V copies" if copies > 1 else "inputs exceed L2",
+                "dtype": "bf16", "data": "synthetic"}
+
+    # prefill workloads
+    if name == "prefill_64k":
+        cfg = inputs.PREFILL_64K
+        q, k, v = inputs.prefill_inputs_for(cfg, seed=0)
+        B, T_q, S_kv, H_q, H_kv, d, W, L = cfg.B, cfg.S, cfg.S, cfg.H_q, cfg.H_kv, cfg.d, -1, cfg.S
+        label = cfg.name
+    elif name == "prefill_window":
+        cfg = inputs.LLAMA70B_PREFILL_8K
+        q, k, v = inputs.prefill_inputs_for(cfg, seed=0)
+        B, T_q, S_kv, H_q, H_kv, d, W, L = cfg.B, cfg.S, cfg.S, cfg.H_q, cfg.H_kv, cfg.d, 4096, cfg.S
+        label = "prefill_causal_llama70b_s8192_window4096"
+    else:  # chunk of 2048 queries ending a 32768-token sequence
+        B, T_q, S_kv, H_q, H_kv, d, W, L = 1, 2048, 32768, 64, 8, 128, -1, 32768
+        gen = torch.Generator().manual_seed(0)
+        q = torch.randn(B, T_q, H_q, d, generator=gen).to(torch.bfloat16)
+        k = torch.randn(B, S_kv, H_kv, d, generator=gen).to(torch.bfloat16)
+        v = torch.randn(B, S_kv, H_kv, d, generator=gen).to(torch.bfloat16)
+        label = "prefill_chunk_llama70b_t2048_at_32768"
+    scale = 1.0 / math.sqrt(d)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty_like(qd)
+    lse = torch.empty(B, H_q, T_q, dtype=torch.float32, device=dev)
+    lens = torch.full((B,), L, dtype=torch.int32, device=dev)
+    # visible (query, key) pairs: row a = L - T_q + i sees keys max(0, a - W) .. a
+    a = torch.arange(L - T_q, L, dtype=torch.float64)
+    vis = (a + 1) if W < 0 else torch.minimum(a, torch.full_like(a, W)) + 1
+    flops = 4.0 * d * H_q * B * float(vis.sum())
+
+    def step(i):
+        if name == "prefill_64k":
+            st = g.gqa_attn_prefill_causal(qd, kd, vd, B, T_q, H_q, H_kv, d, scale, out, lse, stream)
+        else:
+            st = g.gqa_attn_prefill_chunk(qd, kd, vd, lens, B, T_q, S_kv, H_q, H_kv, d, scale, W,
+                                          out, lse, stream)
+        assert st == g.GQA_OK
+
+    ms = timed(step)
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"metric": f"prefill TFLOPS ({label})", "value": round(tf, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "steps": steps, "flops_per_step": flops,
+            "frac_of_" + peak_kind + "_bf16": round(tf / bf16_tf, 4), "dtype": "bf16",
+            "data": "synthetic"}
+
+
 # ------------------------------------------------------ CPU oracle baseline --
 def cpu_baseline(args, steps=1):
     """Time the fp64 oracle on the host cores on a bounded sample of the decode workload."""
@@ -418,6 +518,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=WORKLOADS, default=None,
+                    help="measure one further workload instead of the headline step")
     ap.add_argument("--only", choices=["decode", "prefill"], default=None,
                     help="run one leg only (for profiler captures); the JSON line is partial")
     args = ap.parse_args()
@@ -427,6 +529,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     dist = None
+    if args.workload is not None:
+        if rank == 0:
+            print(json.dumps(run_workload(args.workload, args)), flush=True)
+        return 0
     if args.impl == "reference":
         if world > 1 and rank != 0:
             return 0
