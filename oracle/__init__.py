@@ -22,6 +22,9 @@ computes, with its sources:
   sequence b sits at position a = seq_lens[b] - T_q + i and sees keys
   a - window <= j <= a (the sliding window of p.13 §7; no lower bound when
   window < 0).
+* :func:`decode_paged`: decode over a paged cache (p.17 §2-§4, p.18): token t
+  of sequence b sits in page ``block_table[b][t // B_p]`` at offset
+  ``t % B_p`` of the K and V pools ``[P, B_p, H_kv, d]``.
 * :func:`merge_partials`: the merge m = max, l = a_a l_a + a_b l_b,
   O = a_a O_a + a_b O_b folded over the splits, then O / l and m + ln l
   (p.4 §3, §8; p.18 §4 stage 2).
@@ -71,8 +74,10 @@ def _load():
             lib.orc_prefill_causal_rows.argtypes = [P, P, P, I, I, I, I, I, I, D, P, I, P, P, I]
             lib.orc_prefill_chunk_rows.argtypes = [P, P, P, I, P, I, I, I, I, I, I, D, I, P, I, P,
                                                    P, I]
+            lib.orc_decode_paged.argtypes = [P, P, P, I, P, I, P, I, I, I, I, I, I, D, P, P, I]
             for f in (lib.orc_decode, lib.orc_decode_partials, lib.orc_merge_partials,
-                      lib.orc_prefill_causal_rows, lib.orc_prefill_chunk_rows):
+                      lib.orc_prefill_causal_rows, lib.orc_prefill_chunk_rows,
+                      lib.orc_decode_paged):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -218,4 +223,28 @@ def prefill_chunk_rows(q, k, v, scale, seq_lens=None, window=-1, rows=None, nthr
                                         H_kv, d, float(scale), int(window), _ptr(ra), n_rows,
                                         _ptr(out), _ptr(lse), _threads(nthreads))
     _check(rc, "prefill_chunk_rows")
+    return out, lse
+
+
+def decode_paged(q, k_pool, v_pool, block_table, seq_lens, scale, nthreads=None):
+    """q [B,H_q,d]; k_pool, v_pool [P,B_p,H_kv,d]; block_table [B,max_blocks]; seq_lens [B]."""
+    qa, qt = _as_input(q)
+    ka, kt = _as_input(k_pool)
+    va, vt = _as_input(v_pool)
+    if not (qt == kt == vt):
+        raise ValueError("q, k, v must share one dtype")
+    B, H_q, d = qa.shape
+    P, B_p, H_kv, d2 = ka.shape
+    if d2 != d or va.shape != ka.shape:
+        raise ValueError("shape mismatch")
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    if bt.ndim != 2 or bt.shape[0] != B:
+        raise ValueError("block_table must be [B, max_blocks]")
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32).reshape(B))
+    out = np.empty((B, H_q, d))
+    lse = np.empty((B, H_q))
+    rc = _load().orc_decode_paged(_ptr(qa), _ptr(ka), _ptr(va), qt, _ptr(bt), bt.shape[1],
+                                  _ptr(sl), B, P, B_p, H_q, H_kv, d, float(scale), _ptr(out),
+                                  _ptr(lse), _threads(nthreads))
+    _check(rc, "decode_paged")
     return out, lse

@@ -33,6 +33,8 @@
  *            out [B, n_rows, H_q, d] (double); lse [B, H_q, n_rows] (double)
  *   chunk  : q [B, T_q, H_q, d]; k, v [B, S_max, H_kv, d]; seq_lens [B] or NULL;
  *            rows [n_rows] (chunk row indices); out, lse as for prefill
+ *   paged  : q [B, H_q, d]; k_pool, v_pool [P, B_p, H_kv, d]; block_table [B, max_blocks]
+ *            (int32); seq_lens [B]; out, lse as for decode
  *
  * Every entry point returns 0 on success and a negative number for invalid
  * arguments (nothing is written then).
@@ -421,4 +423,71 @@ int orc_prefill_chunk_rows(const void* q, const void* k, const void* v, int dtyp
                  rows, n_rows, out, lse};
   size_t scratch = (size_t)d + 3 * (size_t)S_max * d;
   return run_pool(chunk_task, &c, (int64_t)B * H_q, scratch, nthreads);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Paged decode ("Attention Kernel 계보", p.17 §2-§4, p.18 §1-§5): the keys   */
+/* of sequence b live in fixed pages of B_p tokens; logical token t sits in   */
+/* page block_table[b][t / B_p] at offset t % B_p.  The oracle gathers the    */
+/* sequence's keys and values through the table into a contiguous repeated   */
+/* head, then runs the same three-pass softmax as orc_decode.                 */
+typedef struct {
+  const void *q, *kp, *vp;
+  int dtype;
+  const int32_t *table, *seq_lens;
+  int B, P, B_p, max_blocks, H_q, H_kv, d;
+  double scale;
+  double *out, *lse;
+} paged_ctx;
+
+static void paged_gather(const void* pool, int dtype, const int32_t* row_table, int64_t n,
+                         int B_p, int H_kv, int d, int kv, double* dst) {
+  for (int64_t t = 0; t < n; ++t) {
+    int64_t page = row_table[t / B_p];
+    int64_t off = t % B_p;
+    for (int x = 0; x < d; ++x)
+      dst[t * d + x] = widen(pool, ((page * B_p + off) * H_kv + kv) * d + x, dtype);
+  }
+}
+
+static void paged_task(void* vctx, int64_t task, double* scratch) {
+  paged_ctx* c = (paged_ctx*)vctx;
+  int64_t b = task / c->H_q;
+  int h = (int)(task % c->H_q);
+  int kv = h / (c->H_q / c->H_kv);
+  int d = c->d;
+  int64_t n = c->seq_lens[b];
+  int64_t cap = (int64_t)c->max_blocks * c->B_p;
+  double* qrow = scratch;
+  double* kh = qrow + d;
+  double* vh = kh + (size_t)cap * d;
+  double* s = vh + (size_t)cap * d;
+  const int32_t* row_table = c->table + b * c->max_blocks;
+  for (int x = 0; x < d; ++x) qrow[x] = widen(c->q, (b * c->H_q + h) * d + x, c->dtype);
+  paged_gather(c->kp, c->dtype, row_table, n, c->B_p, c->H_kv, d, kv, kh);
+  paged_gather(c->vp, c->dtype, row_table, n, c->B_p, c->H_kv, d, kv, vh);
+  attend_row(qrow, kh, vh, n, d, c->scale, s, c->out + (b * c->H_q + h) * d,
+             c->lse + b * c->H_q + h);
+}
+
+int orc_decode_paged(const void* q, const void* k_pool, const void* v_pool, int dtype,
+                     const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int B,
+                     int P, int B_p, int H_q, int H_kv, int d, double scale, double* out,
+                     double* lse, int nthreads) {
+  int rc = check_heads(B, B_p, H_q, H_kv, d);
+  if (rc) return rc;
+  if (dtype != ORC_F64 && dtype != ORC_BF16) return -3;
+  if (P < 1 || max_blocks < 1) return -5;
+  for (int b = 0; b < B; ++b) {
+    if (seq_lens[b] < 1 || seq_lens[b] > (int64_t)max_blocks * B_p) return -4;
+    for (int j = 0; j < (seq_lens[b] + B_p - 1) / B_p; ++j) {
+      int32_t page = block_table[(int64_t)b * max_blocks + j];
+      if (page < 0 || page >= P) return -6;
+    }
+  }
+  paged_ctx c = {q, k_pool, v_pool, dtype, block_table, seq_lens, B, P, B_p, max_blocks, H_q,
+                 H_kv, d, scale, out, lse};
+  size_t cap = (size_t)max_blocks * B_p;
+  size_t scratch = (size_t)d + 3 * cap * d;
+  return run_pool(paged_task, &c, (int64_t)B * H_q, scratch, nthreads);
 }

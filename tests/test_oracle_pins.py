@@ -416,3 +416,55 @@ def test_window_brute_force_decimal(oracle_mod):
             ref_o, ref_l = _brute_decimal(q[0, i, h], k[0, lo:a + 1, 0], v[0, lo:a + 1, 0], 0.7)
             np.testing.assert_allclose(out[0, i, h], ref_o, rtol=1e-13, atol=1e-14)
             assert lse[0, h, i] == pytest.approx(ref_l, rel=1e-13, abs=1e-14)
+
+
+# ------------------------------------------------------------ paged decode ---
+def _to_pages(k, B_p, rng, extra=3):
+    """Scatter a contiguous cache [B, S, H, d] into a shuffled pool; returns (pool, table)."""
+    B, S, H, d = k.shape
+    nb = S // B_p
+    perm = rng.permutation(B * nb + extra)  # physical page of each logical block
+    pool = rng.standard_normal((B * nb + extra, B_p, H, d)) * 100  # unused pages: junk
+    table = np.zeros((B, nb), dtype=np.int32)
+    for b in range(B):
+        for j in range(nb):
+            p = perm[b * nb + j]
+            pool[p] = k[b, j * B_p:(j + 1) * B_p]
+            table[b, j] = p
+    return pool, table
+
+
+@pytest.mark.parametrize("B_p", [1, 4, 16])
+def test_paged_decode_equals_contiguous_decode(oracle_mod, B_p):
+    rng = np.random.default_rng(30 + B_p)
+    B, S, H_q, H_kv, d = 3, 48, 8, 2, 8
+    q, k, v = _rand((B, H_q, d), rng), _rand((B, S, H_kv, d), rng), _rand((B, S, H_kv, d), rng)
+    lens = [48, 1, 29]
+    kp, table = _to_pages(k, B_p, np.random.default_rng(5))
+    vp, table_v = _to_pages(v, B_p, np.random.default_rng(5))
+    assert np.array_equal(table, table_v)
+    p_o, p_l = oracle_mod.decode_paged(q, kp, vp, table, lens, 0.3)
+    c_o, c_l = oracle_mod.decode(q, k, v, lens, 0.3)
+    np.testing.assert_allclose(p_o, c_o, atol=1e-14)
+    np.testing.assert_allclose(p_l, c_l, atol=1e-14)
+
+
+def test_paged_decode_shared_prefix_pages(oracle_mod):
+    # two requests share their first two pages (copy-on-write prefix, p.17 §7)
+    rng = np.random.default_rng(40)
+    B_p, H_q, H_kv, d = 4, 4, 1, 8
+    kp, vp = _rand((6, B_p, H_kv, d), rng), _rand((6, B_p, H_kv, d), rng)
+    table = np.array([[3, 1, 5], [3, 1, 0]], dtype=np.int32)
+    q = _rand((2, H_q, d), rng)
+    q[1] = q[0]
+    o, l_ = oracle_mod.decode_paged(q, kp, vp, table, [8, 8], 0.5)  # only the shared pages
+    np.testing.assert_allclose(o[0], o[1], atol=0)
+    np.testing.assert_allclose(l_[0], l_[1], atol=0)
+    o2, _ = oracle_mod.decode_paged(q, kp, vp, table, [12, 12], 0.5)  # diverging third page
+    assert not np.allclose(o2[0], o2[1])
+
+
+def test_paged_decode_rejects_bad_pages(oracle_mod):
+    kp = np.zeros((2, 4, 1, 8))
+    with pytest.raises(ValueError):
+        oracle_mod.decode_paged(np.zeros((1, 1, 8)), kp, kp, [[0, 2]], [8], 1.0)
