@@ -29,6 +29,8 @@ SIGNATURES = {
     "gqa_attn_decode": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
     "gqa_attn_decode_combine": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "gqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
+    "gqa_attn_decode_paged": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P,
+                                   _P, _P]),
     "gqa_attn_prefill_causal": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "gqa_attn_prefill_chunk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
     "gqa_last_device_error": (_I, [_P]),
@@ -111,6 +113,15 @@ def gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream=None
                                           _ptr(lse), _stream(stream))
 
 
+def gqa_attn_decode_paged(q, k_pool, v_pool, block_table, seq_lens, B, num_pages, page_size,
+                          max_blocks, H_q, H_kv, d, scale, n_split, workspace, out, lse,
+                          stream=None) -> int:
+    return load().gqa_attn_decode_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                        _ptr(seq_lens), B, num_pages, page_size, max_blocks, H_q,
+                                        H_kv, d, scale, n_split, _ptr(workspace), _ptr(out),
+                                        _ptr(lse), _stream(stream))
+
+
 def gqa_attn_decode_noalloc(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale, n_split,
                             out, lse, stream=None) -> int:
     return load().gqa_attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
@@ -177,6 +188,33 @@ def decode(q, k_cache, v_cache, seq_lens, scale=None, n_split=None, workspace=No
         workspace = decode_workspace(B, H_q, d, n_split, q.device)
     _check(gqa_attn_decode(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale, n_split,
                            workspace, out, lse, stream), "gqa_attn_decode")
+    if n_split > 1:
+        _check(gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream),
+               "gqa_attn_decode_combine")
+    return out, lse
+
+
+def decode_paged(q, k_pool, v_pool, block_table, seq_lens, scale=None, n_split=None,
+                 workspace=None, out=None, lse=None, stream=None):
+    """Paged split-KV decode + combine on CUDA tensors; returns (out, lse)."""
+    import torch
+
+    B, H_q, d = q.shape
+    P, B_p, H_kv, _ = k_pool.shape
+    max_blocks = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if n_split is None:
+        n_split = gqa_attn_decode_default_splits(B, H_kv, max_blocks * B_p, d)
+    if out is None:
+        out = torch.empty((B, H_q, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
+    if n_split > 1 and workspace is None:
+        workspace = decode_workspace(B, H_q, d, n_split, q.device)
+    _check(gqa_attn_decode_paged(q, k_pool, v_pool, block_table, seq_lens, B, P, B_p, max_blocks,
+                                 H_q, H_kv, d, scale, n_split, workspace, out, lse, stream),
+           "gqa_attn_decode_paged")
     if n_split > 1:
         _check(gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream),
                "gqa_attn_decode_combine")

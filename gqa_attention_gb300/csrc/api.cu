@@ -136,15 +136,24 @@ int gqa_attn_decode_default_splits(int B, int H_kv, int S_max, int d) {
   return (int)n;
 }
 
-gqa_status gqa_attn_decode(const void* q, const void* k_cache, const void* v_cache,
-                           const int32_t* seq_lens, int B, int S_max, int H_q, int H_kv, int d,
-                           float scale, int n_split, void* workspace, void* out, float* lse,
-                           gqa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks the decode arguments shared by the contiguous and the paged cache,
+// encodes the K/V tensor maps (cache viewed as [rows][H_kv][d], boxes of
+// box_rows token rows of one head, at most 64 elements / 128 bytes wide,
+// swizzled for ldmatrix) and fills the kernel parameters.
+gqa_status prepare_decode(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* seq_lens, int B, int S_max, long long rows, int box_rows,
+                          int H_q, int H_kv, int d, float scale, int n_split, void* workspace,
+                          void* out, float* lse, CUtensorMap* tm_k, CUtensorMap* tm_v,
+                          gqa::DecodeParams* p) {
   if (!q || !k_cache || !v_cache || !seq_lens || !out || !lse) return GQA_ERR_INVALID_ARG;
   if (B < 1 || S_max < 1 || H_q < 1 || H_kv < 1 || n_split < 1) return GQA_ERR_INVALID_ARG;
   if (B > 65535 || H_kv > 65535 || H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
-  if ((long long)B * S_max > 0xffffffffLL || n_split > 0x7fffffff) return GQA_ERR_INVALID_ARG;
+  if (rows > 0x7fffffffLL || n_split > 0x7fffffff) return GQA_ERR_INVALID_ARG;
   if (!head_dim_ok(d) || H_q / H_kv > 16) return GQA_ERR_UNSUPPORTED;
   if (n_split > 1 && !workspace) return GQA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
@@ -155,38 +164,80 @@ gqa_status gqa_attn_decode(const void* q, const void* k_cache, const void* v_cac
   gqa_status st = error_word(&err);
   if (st != GQA_OK) return st;
 
-  // K/V cache viewed as [B*S_max rows][H_kv][d]; one box = 64 token rows of one
-  // head, at most 64 elements (128 bytes) wide, swizzled for ldmatrix.
   const int box_d = d >= 64 ? 64 : d;
-  const uint64_t dims[3] = {(uint64_t)d, (uint64_t)H_kv, (uint64_t)B * S_max};
+  const uint64_t dims[3] = {(uint64_t)d, (uint64_t)H_kv, (uint64_t)rows};
   const uint64_t strides[2] = {(uint64_t)d * 2, (uint64_t)H_kv * d * 2};
-  const uint32_t box[3] = {(uint32_t)box_d, 1u, (uint32_t)gqa::kDecodeTile};
+  const uint32_t box[3] = {(uint32_t)box_d, 1u, (uint32_t)box_rows};
   const CUtensorMapSwizzle swz = box_d == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  CUtensorMap tm_k, tm_v;
-  if ((st = encode_bf16(&tm_k, k_cache, 3, dims, strides, box, swz)) != GQA_OK) return st;
-  if ((st = encode_bf16(&tm_v, v_cache, 3, dims, strides, box, swz)) != GQA_OK) return st;
+  if ((st = encode_bf16(tm_k, k_cache, 3, dims, strides, box, swz)) != GQA_OK) return st;
+  if ((st = encode_bf16(tm_v, v_cache, 3, dims, strides, box, swz)) != GQA_OK) return st;
 
+  *p = gqa::DecodeParams{};
+  p->q = static_cast<const __nv_bfloat16*>(q);
+  p->seq_lens = seq_lens;
+  p->B = B;
+  p->S_max = S_max;
+  p->H_q = H_q;
+  p->H_kv = H_kv;
+  p->G = H_q / H_kv;
+  p->d = d;
+  p->n_split = n_split;
+  p->chunk = gqa_attn_decode_split_chunk(S_max, n_split);
+  p->scale_log2 = scale * 1.4426950408889634f;
+  p->ws_ml = static_cast<float2*>(workspace);
+  p->ws_O = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                 gqa::decode_ws_O_offset(B, H_q, n_split))
+                      : nullptr;
+  p->out = static_cast<__nv_bfloat16*>(out);
+  p->lse = lse;
+  p->err = err;
+  p->wait_ns = g_wait_ns.load();
+  return GQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gqa_status gqa_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* seq_lens, int B, int S_max, int H_q, int H_kv, int d,
+                           float scale, int n_split, void* workspace, void* out, float* lse,
+                           gqa_stream_t stream) {
+  CUtensorMap tm_k, tm_v;
   gqa::DecodeParams p;
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.seq_lens = seq_lens;
-  p.B = B;
-  p.S_max = S_max;
-  p.H_q = H_q;
-  p.H_kv = H_kv;
-  p.G = H_q / H_kv;
-  p.d = d;
-  p.n_split = n_split;
-  p.chunk = gqa_attn_decode_split_chunk(S_max, n_split);
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.ws_ml = static_cast<float2*>(workspace);
-  p.ws_O = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                                gqa::decode_ws_O_offset(B, H_q, n_split))
-                     : nullptr;
-  p.out = static_cast<__nv_bfloat16*>(out);
-  p.lse = lse;
-  p.err = err;
-  p.wait_ns = g_wait_ns.load();
+  gqa_status st = prepare_decode(q, k_cache, v_cache, seq_lens, B, S_max, (long long)B * S_max,
+                                 gqa::kDecodeTile, H_q, H_kv, d, scale, n_split, workspace, out,
+                                 lse, &tm_k, &tm_v, &p);
+  if (st != GQA_OK) return st;
   return cuda_status(gqa::launch_decode_split(p, tm_k, tm_v, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_attn_decode_paged(const void* q, const void* k_pool, const void* v_pool,
+                                 const int32_t* block_table, const int32_t* seq_lens, int B,
+                                 int num_pages, int page_size, int max_blocks, int H_q, int H_kv,
+                                 int d, float scale, int n_split, void* workspace, void* out,
+                                 float* lse, gqa_stream_t stream) {
+  if (!block_table || !aligned(block_table, 4)) return GQA_ERR_INVALID_ARG;
+  if (num_pages < 1 || max_blocks < 1 || page_size < 1) return GQA_ERR_INVALID_ARG;
+  if (page_size < 16 || (page_size & (page_size - 1)) != 0) return GQA_ERR_UNSUPPORTED;
+  const long long S_max = (long long)max_blocks * page_size;
+  const long long rows = (long long)num_pages * page_size;
+  if (S_max > 0x7fffffffLL || rows > 0x7ffffffeLL) return GQA_ERR_INVALID_ARG;
+  if (n_split >= 1) {
+    const int chunk = gqa_attn_decode_split_chunk((int)S_max, n_split);
+    if (chunk / page_size + 2 > gqa::kMaxPagesPerCta) return GQA_ERR_UNSUPPORTED;
+  }
+  CUtensorMap tm_k, tm_v;
+  gqa::DecodeParams p;
+  gqa_status st = prepare_decode(q, k_pool, v_pool, seq_lens, B, (int)S_max, rows,
+                                 page_size < gqa::kDecodeTile ? page_size : gqa::kDecodeTile, H_q,
+                                 H_kv, d, scale, n_split, workspace, out, lse, &tm_k, &tm_v, &p);
+  if (st != GQA_OK) return st;
+  p.block_table = block_table;
+  p.max_blocks = max_blocks;
+  p.page_size = page_size;
+  p.num_pages = num_pages;
+  return cuda_status(gqa::launch_decode_paged(p, tm_k, tm_v, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 gqa_status gqa_attn_decode_combine(const void* workspace, int B, int H_q, int d, int n_split,
@@ -298,7 +349,7 @@ gqa_status gqa_last_device_error(gqa_stream_t stream) {
       return GQA_ERR_CUDA;
   }
   if (word & gqa::kErrTimeout) return GQA_ERR_TIMEOUT;
-  if (word & gqa::kErrBadSeqLen) return GQA_ERR_INVALID_ARG;
+  if (word & (gqa::kErrBadSeqLen | gqa::kErrBadPage)) return GQA_ERR_INVALID_ARG;
   return GQA_OK;
 }
 

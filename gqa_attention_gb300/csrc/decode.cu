@@ -78,7 +78,11 @@ __device__ __forceinline__ float online_update(float (&x)[4], float& m, float& l
   return alpha;
 }
 
-template <int D, bool ROWS16, int NSTAGE>
+// PAGED = true: the K/V cache is a pool of fixed-size pages reached through a
+// block table ("Attention Kernel 계보" p.17 §2-§4, p.18 §5): the producer warp
+// stages the CTA's page indices in shared memory once, then loads every page
+// segment of a tile with its own TMA box.
+template <int D, bool ROWS16, int NSTAGE, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 2)
     gqa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
@@ -87,6 +91,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ __align__(8) uint64_t full_bar[NSTAGE];
   __shared__ __align__(8) uint64_t empty_bar[NSTAGE];
   __shared__ int abort_flag;
+  __shared__ int bad_page;
+  __shared__ int pages_sm[PAGED ? kMaxPagesPerCta : 1];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -133,12 +139,34 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(smem_u32(&empty_bar[s]), kConsumerWarps);
     }
     abort_flag = 0;
+    bad_page = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
   // ------------------------------------------------------------ producer ----
   if (warp == kConsumerWarps) {
+    const int page0 = PAGED ? t0 / p.page_size : 0;
+    if (PAGED) {
+      // Stage the page indices of tokens [t0, t_end); an index outside the
+      // pool is reported and replaced by 0 (the CTA's outputs become NaN).
+      const int n_pages = (t_end - 1) / p.page_size - page0 + 1;
+      const int32_t* row_table = p.block_table + (size_t)b * p.max_blocks;
+      int bad = 0;
+      for (int j = lane; j < n_pages; j += 32) {
+        int pg = row_table[page0 + j];
+        if (pg < 0 || pg >= p.num_pages) {
+          bad = 1;
+          pg = 0;
+        }
+        pages_sm[j] = pg;
+      }
+      if (__any_sync(0xffffffffu, bad) && lane == 0) {
+        bad_page = 1;
+        atomicOr(p.err, kErrBadPage);
+      }
+      __syncwarp();
+    }
     if (lane == 0) {
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
@@ -155,11 +183,30 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_arrive_expect_tx(fb, Lay::kStageBytes);
         const uint32_t dst_k = smem_base + st * Lay::kStageBytes;
         const uint32_t dst_v = dst_k + Lay::kTileBytes;
-        const int row = b * p.S_max + t0 + i * kTile;
+        if (!PAGED) {
+          const int row = b * p.S_max + t0 + i * kTile;
 #pragma unroll
-        for (int blk = 0; blk < Lay::kBlocks; ++blk) {
-          tma_load_3d(dst_k + blk * Lay::kBlockBytes, &tm_k, fb, blk * Lay::kBox, kv, row);
-          tma_load_3d(dst_v + blk * Lay::kBlockBytes, &tm_v, fb, blk * Lay::kBox, kv, row);
+          for (int blk = 0; blk < Lay::kBlocks; ++blk) {
+            tma_load_3d(dst_k + blk * Lay::kBlockBytes, &tm_k, fb, blk * Lay::kBox, kv, row);
+            tma_load_3d(dst_v + blk * Lay::kBlockBytes, &tm_v, fb, blk * Lay::kBox, kv, row);
+          }
+        } else {
+          // Boxes of h = min(page_size, 64) rows; a box wholly past the split
+          // end reads rows past the pool (TMA fills them with zeros) so that
+          // every stage still receives its full byte count.
+          const int h = min(p.page_size, kTile);
+          for (int sub = 0; sub < kTile / h; ++sub) {
+            const int tok = t0 + i * kTile + sub * h;
+            const int row = tok < t_end ? pages_sm[tok / p.page_size - page0] * p.page_size +
+                                              tok % p.page_size
+                                        : p.num_pages * p.page_size;
+            const uint32_t off = sub * h * Lay::kSpan;
+#pragma unroll
+            for (int blk = 0; blk < Lay::kBlocks; ++blk) {
+              tma_load_3d(dst_k + blk * Lay::kBlockBytes + off, &tm_k, fb, blk * Lay::kBox, kv, row);
+              tma_load_3d(dst_v + blk * Lay::kBlockBytes + off, &tm_v, fb, blk * Lay::kBox, kv, row);
+            }
+          }
         }
         issued = i + 1;
       }
@@ -284,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // ------------------------------------------- merge the four warp partials --
   named_bar_sync(1, kConsumerWarps * 32);
-  const bool failed = *reinterpret_cast<volatile int*>(&abort_flag) != 0;
+  const bool failed = *reinterpret_cast<volatile int*>(&abort_flag) != 0 ||
+                      (PAGED && *reinterpret_cast<volatile int*>(&bad_page) != 0);
   float* mO = reinterpret_cast<float*>(smem);  // [warps][16][D]
   float2* mML = reinterpret_cast<float2*>(smem + kConsumerWarps * 16 * D * 4);  // [warps][16]
   if (!failed) {
@@ -468,11 +516,11 @@ inline cudaError_t set_smem_attr_once(const void* kern, int smem, unsigned char*
   return e;
 }
 
-template <int D, bool ROWS16, int NSTAGE>
+template <int D, bool ROWS16, int NSTAGE, bool PAGED>
 cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                          cudaStream_t stream) {
   constexpr int smem = decode_smem_bytes<D, NSTAGE>();
-  auto kern = gqa_decode_split_kernel<D, ROWS16, NSTAGE>;
+  auto kern = gqa_decode_split_kernel<D, ROWS16, NSTAGE, PAGED>;
   static unsigned char done[64];
   cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem, done);
   if (e != cudaSuccess) return e;
@@ -491,12 +539,12 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tm_k, const C
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool PAGED>
 cudaError_t launch_split_rows(const DecodeParams& p, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, cudaStream_t stream) {
   constexpr int NSTAGE = D >= 128 ? GQA_DECODE_STAGES_D128 : 6;
-  if (p.G > 8) return launch_split<D, true, NSTAGE>(p, tm_k, tm_v, stream);
-  return launch_split<D, false, NSTAGE>(p, tm_k, tm_v, stream);
+  if (p.G > 8) return launch_split<D, true, NSTAGE, PAGED>(p, tm_k, tm_v, stream);
+  return launch_split<D, false, NSTAGE, PAGED>(p, tm_k, tm_v, stream);
 }
 
 template <int D>
@@ -521,9 +569,19 @@ cudaError_t launch_comb(const CombineParams& p, cudaStream_t stream) {
 cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, cudaStream_t stream) {
   switch (p.d) {
-    case 32: return launch_split_rows<32>(p, tm_k, tm_v, stream);
-    case 64: return launch_split_rows<64>(p, tm_k, tm_v, stream);
-    case 128: return launch_split_rows<128>(p, tm_k, tm_v, stream);
+    case 32: return launch_split_rows<32, false>(p, tm_k, tm_v, stream);
+    case 64: return launch_split_rows<64, false>(p, tm_k, tm_v, stream);
+    case 128: return launch_split_rows<128, false>(p, tm_k, tm_v, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_decode_paged(const DecodeParams& p, const CUtensorMap& tm_k,
+                                const CUtensorMap& tm_v, cudaStream_t stream) {
+  switch (p.d) {
+    case 32: return launch_split_rows<32, true>(p, tm_k, tm_v, stream);
+    case 64: return launch_split_rows<64, true>(p, tm_k, tm_v, stream);
+    case 128: return launch_split_rows<128, true>(p, tm_k, tm_v, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -10,7 +10,7 @@
 namespace gqa {
 
 // Bits of the per-device error word.
-enum : unsigned { kErrTimeout = 1u, kErrBadSeqLen = 2u };
+enum : unsigned { kErrTimeout = 1u, kErrBadSeqLen = 2u, kErrBadPage = 4u };
 
 constexpr int kDecodeTile = 64;  // tokens per decode pipeline stage; split chunks are multiples
 
@@ -26,7 +26,13 @@ struct DecodeParams {
   float* lse;              // [B, H_q]         (n_split == 1)
   unsigned* err;           // device error word
   uint64_t wait_ns;        // time limit of every pipeline wait
+  // paged cache only: token t of sequence b is row page*page_size + t % page_size
+  // of the pools, page = block_table[b * max_blocks + t / page_size]
+  const int32_t* block_table;
+  int max_blocks, page_size, num_pages;
 };
+
+constexpr int kMaxPagesPerCta = 512;  // page indices a paged decode CTA stages in shared memory
 
 struct CombineParams {
   const float2* ws_ml;
@@ -52,6 +58,8 @@ struct PrefillParams {
 cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, cudaStream_t stream);
 cudaError_t launch_decode_combine(const CombineParams& p, cudaStream_t stream);
+cudaError_t launch_decode_paged(const DecodeParams& p, const CUtensorMap& tm_k,
+                                const CUtensorMap& tm_v, cudaStream_t stream);
 cudaError_t launch_prefill_causal(const PrefillParams& p, const CUtensorMap& tm_q,
                                   const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                   int num_sms, cudaStream_t stream);

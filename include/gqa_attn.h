@@ -120,6 +120,25 @@ gqa_status gqa_attn_decode(const void* q, const void* k_cache, const void* v_cac
 gqa_status gqa_attn_decode_combine(const void* workspace, int B, int H_q, int d, int n_split,
                                    void* out, float* lse, gqa_stream_t stream);
 
+/* Stage 1 of split-KV decode over a paged KV cache ("Attention Kernel 계보",
+ * p.17 §2-§4 and p.18 §1-§5).  The cache is two pools of fixed-size pages,
+ *   k_pool, v_pool  device bf16 [num_pages, page_size, H_kv, d]
+ * and logical token t of sequence b is row t % page_size of page
+ *   block_table[b * max_blocks + t / page_size]      (device int32 [B, max_blocks]).
+ * page_size is a power of two >= 16; 1 <= seq_lens[b] <= max_blocks * page_size.
+ * Splits, workspace, outputs and the follow-up gqa_attn_decode_combine() are
+ * those of gqa_attn_decode() with S_max = max_blocks * page_size.  Pages may be
+ * shared between sequences (read-only).  Only the table entries of tokens
+ * < seq_lens[b] are read; an entry outside [0, num_pages) is reported through
+ * the error word (GQA_ERR_INVALID_ARG) and makes that split's outputs NaN.
+ * GQA_ERR_UNSUPPORTED if one split would span more than 510 pages (raise
+ * n_split). */
+gqa_status gqa_attn_decode_paged(const void* q, const void* k_pool, const void* v_pool,
+                                 const int32_t* block_table, const int32_t* seq_lens, int B,
+                                 int num_pages, int page_size, int max_blocks, int H_q, int H_kv,
+                                 int d, float scale, int n_split, void* workspace, void* out,
+                                 float* lse, gqa_stream_t stream);
+
 /* Split-KV decode that allocates nothing, for callers that cannot call
  * cudaMalloc when they decode: code inside a CUDA graph capture or an
  * allocator's critical section, or a serving process whose device memory pool
