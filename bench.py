@@ -355,7 +355,28 @@ def run_ours(args, rank, world, dist):
 
 
 # ---------------------------------------------------- further workloads ---
-WORKLOADS = ("decode_tiny", "decode_ragged", "prefill_64k", "prefill_window", "prefill_chunk")
+WORKLOADS = ("decode_tiny", "decode_ragged", "decode_paged16", "decode_paged128", "prefill_64k",
+             "prefill_window", "prefill_chunk")
+
+
+def _shuffled_pages(k, v, page_size, seed):
+    """Scatter a contiguous cache [B, S, H, d] into a pool of pages in a seeded random order."""
+    import torch
+
+    B, S, H, d = k.shape
+    nb = -(-S // page_size)
+    perm = torch.randperm(B * nb, generator=torch.Generator().manual_seed(seed))
+    kp = torch.zeros(B * nb, page_size, H, d, dtype=k.dtype)
+    vp = torch.zeros_like(kp)
+    table = torch.zeros(B, nb, dtype=torch.int32)
+    for b in range(B):
+        for j in range(nb):
+            p = int(perm[b * nb + j])
+            lo, hi = j * page_size, min(S, (j + 1) * page_size)
+            kp[p, : hi - lo] = k[b, lo:hi]
+            vp[p, : hi - lo] = v[b, lo:hi]
+            table[b, j] = p
+    return kp, vp, table
 
 
 def run_workload(name, args):
@@ -380,6 +401,35 @@ def run_workload(name, args):
         if g.gqa_last_device_error(stream) != g.GQA_OK:
             raise RuntimeError("device error")
         return ms
+
+    if name.startswith("decode_paged"):
+        cfg = inputs.LLAMA70B_DECODE
+        page = int(name[len("decode_paged"):])
+        q, k, v, lens = inputs.decode_inputs_for(cfg, seed=0)
+        kv_bytes = 2 * int(lens.sum()) * cfg.H_kv * cfg.d * 2
+        kp, vp, table = _shuffled_pages(k, v, page, seed=0)
+        qd, ld, td = q.to(dev), lens.to(dev), table.to(dev)
+        kps = [kp.to(dev) for _ in range(3)]
+        vps = [vp.to(dev) for _ in range(3)]
+        n = g.paged_default_splits(cfg.B, cfg.H_kv, cfg.S_max, cfg.d, page)
+        ws = g.decode_workspace(cfg.B, cfg.H_q, cfg.d, n, dev)
+        out = torch.empty(cfg.B, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(cfg.B, cfg.H_q, dtype=torch.float32, device=dev)
+
+        def pstep(i):
+            assert g.gqa_attn_decode_paged(qd, kps[i % 3], vps[i % 3], td, ld, cfg.B, kp.shape[0],
+                                           page, table.shape[1], cfg.H_q, cfg.H_kv, cfg.d,
+                                           cfg.scale, n, ws, out, lse, stream) == g.GQA_OK
+            assert g.gqa_attn_decode_combine(ws, cfg.B, cfg.H_q, cfg.d, n, out, lse,
+                                             stream) == g.GQA_OK
+
+        ms = timed(pstep)
+        gbs = kv_bytes / (ms * 1e-3) / 1e9
+        return {"metric": f"paged decode KV GB/s ({cfg.name}, page {page}, shuffled pages)",
+                "value": round(gbs, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
+                "steps": steps, "n_split": n, "kv_bytes": kv_bytes,
+                "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
+                "l2": "3 rotating page pools", "dtype": "bf16", "data": "synthetic"}
 
     if name.startswith("decode"):
         cfg = inputs.TINY_DECODE if name == "decode_tiny" else inputs.LLAMA70B_DECODE_RAGGED

@@ -29,6 +29,7 @@ from ._binding import (  # noqa: E402,F401
     gqa_selftest_wait_timeout,
     gqa_set_wait_limit_ns,
     load,
+    paged_default_splits,
     prefill_causal,
     prefill_chunk,
     split_workspace,

@@ -194,6 +194,13 @@ def decode(q, k_cache, v_cache, seq_lens, scale=None, n_split=None, workspace=No
     return out, lse
 
 
+def paged_default_splits(B, H_kv, S_max, d, page_size):
+    """Split count for the paged decode: the contiguous default, doubled for pages
+    under 64 tokens (their smaller copies need two CTAs per SM in flight)."""
+    n = gqa_attn_decode_default_splits(B, H_kv, S_max, d)
+    return 2 * n if page_size < 64 else n
+
+
 def decode_paged(q, k_pool, v_pool, block_table, seq_lens, scale=None, n_split=None,
                  workspace=None, out=None, lse=None, stream=None):
     """Paged split-KV decode + combine on CUDA tensors; returns (out, lse)."""
@@ -205,7 +212,7 @@ def decode_paged(q, k_pool, v_pool, block_table, seq_lens, scale=None, n_split=N
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if n_split is None:
-        n_split = gqa_attn_decode_default_splits(B, H_kv, max_blocks * B_p, d)
+        n_split = paged_default_splits(B, H_kv, max_blocks * B_p, d, B_p)
     if out is None:
         out = torch.empty((B, H_q, d), dtype=torch.bfloat16, device=q.device)
     if lse is None:

@@ -132,7 +132,9 @@ gqa_status gqa_attn_decode_combine(const void* workspace, int B, int H_q, int d,
  * < seq_lens[b] are read; an entry outside [0, num_pages) is reported through
  * the error word (GQA_ERR_INVALID_ARG) and makes that split's outputs NaN.
  * GQA_ERR_UNSUPPORTED if one split would span more than 510 pages (raise
- * n_split). */
+ * n_split).  For pages shorter than 64 tokens each tile takes several small
+ * copies; twice gqa_attn_decode_default_splits() (two CTAs per SM) measured
+ * best there. */
 gqa_status gqa_attn_decode_paged(const void* q, const void* k_pool, const void* v_pool,
                                  const int32_t* block_table, const int32_t* seq_lens, int B,
                                  int num_pages, int page_size, int max_blocks, int H_q, int H_kv,
