@@ -101,6 +101,44 @@ def decode_inputs(B, H_q, H_kv, d, S_max, seed=0, seq_lens=None, ragged=None, va
     return q, k, v, lens.to(torch.int32)
 
 
+def quantize_e4m3_per_token(x):
+    """Cache quantisation used to build FP8 inputs: x [B, S, H, d] fp32 -> (codes uint8
+    [B, S, H, d], scale fp32 [B, S]) with scale = max |x| over (H, d) / 448, codes from
+    torch's float8_e4m3fn rounding (round to nearest even).  A token whose values
+    are all zero gets scale 1."""
+    amax = x.abs().amax(dim=(2, 3))
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    codes = (x / scale[:, :, None, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return codes.view(torch.uint8), scale.to(torch.float32)
+
+
+def decode_inputs_fp8(B, H_q, H_kv, d, S_max, seed=0, seq_lens=None, ragged=None):
+    """Decode inputs with an E4M3 cache: (q bf16, k8, v8 uint8 [B,S_max,H_kv,d],
+    k_scale, v_scale fp32 [B,S_max], seq_lens int32).  The same draws as
+    decode_inputs (fp32 randn), quantised per token; codes and scales past each
+    sequence end are NaN bytes (0x7f) and NaN scales."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    if ragged is not None:
+        lo, hi = ragged
+        lens = torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64)
+    elif seq_lens is not None:
+        lens = torch.as_tensor(seq_lens, dtype=torch.int64).reshape(B)
+    else:
+        lens = torch.full((B,), S_max, dtype=torch.int64)
+    q = _randn_bf16((B, H_q, d), g, 1.0)
+    k = torch.randn((B, S_max, H_kv, d), generator=g, dtype=torch.float32)
+    v = torch.randn((B, S_max, H_kv, d), generator=g, dtype=torch.float32)
+    k8, ks = quantize_e4m3_per_token(k)
+    v8, vs = quantize_e4m3_per_token(v)
+    for b in range(B):
+        L = int(lens[b])
+        k8[b, L:] = 0x7F
+        v8[b, L:] = 0x7F
+        ks[b, L:] = float("nan")
+        vs[b, L:] = float("nan")
+    return q, k8, v8, ks, vs, lens.to(torch.int32)
+
+
 def decode_inputs_for(cfg: DecodeConfig, seed=0):
     return decode_inputs(cfg.B, cfg.H_q, cfg.H_kv, cfg.d, cfg.S_max, seed=seed,
                          ragged=cfg.ragged, value_scale=cfg.value_scale)

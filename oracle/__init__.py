@@ -25,6 +25,8 @@ computes, with its sources:
 * :func:`decode_paged`: decode over a paged cache (p.17 §2-§4, p.18): token t
   of sequence b sits in page ``block_table[b][t // B_p]`` at offset
   ``t % B_p`` of the K and V pools ``[P, B_p, H_kv, d]``.
+* :func:`decode_fp8`: decode over an FP8 (E4M3) cache with one scale per
+  token (p.17 §7): key j is ``e4m3(k8[j]) * k_scale[j]``, likewise values.
 * :func:`merge_partials`: the merge m = max, l = a_a l_a + a_b l_b,
   O = a_a O_a + a_b O_b folded over the splits, then O / l and m + ln l
   (p.4 §3, §8; p.18 §4 stage 2).
@@ -75,9 +77,12 @@ def _load():
             lib.orc_prefill_chunk_rows.argtypes = [P, P, P, I, P, I, I, I, I, I, I, D, I, P, I, P,
                                                    P, I]
             lib.orc_decode_paged.argtypes = [P, P, P, I, P, I, P, I, I, I, I, I, I, D, P, P, I]
+            lib.orc_decode_fp8.argtypes = [P, I, P, P, P, P, P, I, I, I, I, I, D, P, P, I]
+            lib.orc_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.orc_e4m3_to_double.restype = ctypes.c_double
             for f in (lib.orc_decode, lib.orc_decode_partials, lib.orc_merge_partials,
                       lib.orc_prefill_causal_rows, lib.orc_prefill_chunk_rows,
-                      lib.orc_decode_paged):
+                      lib.orc_decode_paged, lib.orc_decode_fp8):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -247,4 +252,34 @@ def decode_paged(q, k_pool, v_pool, block_table, seq_lens, scale, nthreads=None)
                                   _ptr(sl), B, P, B_p, H_q, H_kv, d, float(scale), _ptr(out),
                                   _ptr(lse), _threads(nthreads))
     _check(rc, "decode_paged")
+    return out, lse
+
+
+def e4m3_to_double(code: int) -> float:
+    """The oracle's decoding of one E4M3 byte."""
+    return _load().orc_e4m3_to_double(int(code))
+
+
+def decode_fp8(q, k8, v8, k_scale, v_scale, seq_lens, scale, nthreads=None):
+    """q [B,H_q,d]; k8, v8 uint8 E4M3 codes [B,S_max,H_kv,d]; k_scale, v_scale [B,S_max]."""
+    qa, qt = _as_input(q)
+    k8a = np.ascontiguousarray(np.asarray(k8.cpu().numpy() if hasattr(k8, "cpu") else k8,
+                                          dtype=np.uint8))
+    v8a = np.ascontiguousarray(np.asarray(v8.cpu().numpy() if hasattr(v8, "cpu") else v8,
+                                          dtype=np.uint8))
+    ksa = np.ascontiguousarray(np.asarray(k_scale.cpu().numpy() if hasattr(k_scale, "cpu")
+                                          else k_scale, dtype=np.float64))
+    vsa = np.ascontiguousarray(np.asarray(v_scale.cpu().numpy() if hasattr(v_scale, "cpu")
+                                          else v_scale, dtype=np.float64))
+    B, H_q, d = qa.shape
+    _, S_max, H_kv, d2 = k8a.shape
+    if d2 != d or v8a.shape != k8a.shape or ksa.shape != (B, S_max) or vsa.shape != (B, S_max):
+        raise ValueError("shape mismatch")
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32).reshape(B))
+    out = np.empty((B, H_q, d))
+    lse = np.empty((B, H_q))
+    rc = _load().orc_decode_fp8(_ptr(qa), qt, _ptr(k8a), _ptr(v8a), _ptr(ksa), _ptr(vsa), _ptr(sl),
+                                B, S_max, H_q, H_kv, d, float(scale), _ptr(out), _ptr(lse),
+                                _threads(nthreads))
+    _check(rc, "decode_fp8")
     return out, lse

@@ -35,6 +35,8 @@
  *            rows [n_rows] (chunk row indices); out, lse as for prefill
  *   paged  : q [B, H_q, d]; k_pool, v_pool [P, B_p, H_kv, d]; block_table [B, max_blocks]
  *            (int32); seq_lens [B]; out, lse as for decode
+ *   fp8    : q [B, H_q, d] (bf16 bits or double); k8, v8 [B, S_max, H_kv, d] (e4m3 bytes);
+ *            k_scale, v_scale [B, S_max] (double); out, lse as for decode
  *
  * Every entry point returns 0 on success and a negative number for invalid
  * arguments (nothing is written then).
@@ -490,4 +492,71 @@ int orc_decode_paged(const void* q, const void* k_pool, const void* v_pool, int 
   size_t cap = (size_t)max_blocks * B_p;
   size_t scratch = (size_t)d + 3 * cap * d;
   return run_pool(paged_task, &c, (int64_t)B * H_q, scratch, nthreads);
+}
+
+/* ------------------------------------------------------------------------- */
+/* FP8 KV cache ("Attention Kernel 계보", p.17 §7): keys and values stored as */
+/* 8-bit floats with one scale per token; the value a kernel must use is      */
+/* e4m3(byte) * scale.  E4M3 (the "fn" variant): 1 sign, 4 exponent bits with  */
+/* bias 7, 3 mantissa bits; exponent 0 is subnormal (m/8 * 2^-6); the pattern  */
+/* S.1111.111 is NaN; there is no infinity.                                    */
+double orc_e4m3_to_double(uint8_t x) {
+  int sign = x >> 7, e = (x >> 3) & 15, m = x & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+typedef struct {
+  const void* q;
+  int qdtype;
+  const uint8_t *k8, *v8;
+  const double *ks, *vs;
+  const int32_t* seq_lens;
+  int B, S_max, H_q, H_kv, d;
+  double scale;
+  double *out, *lse;
+} fp8_ctx;
+
+static void fp8_task(void* vctx, int64_t task, double* scratch) {
+  fp8_ctx* c = (fp8_ctx*)vctx;
+  int64_t b = task / c->H_q;
+  int h = (int)(task % c->H_q);
+  int kv = h / (c->H_q / c->H_kv);
+  int d = c->d;
+  int64_t n = c->seq_lens[b];
+  double* qrow = scratch;
+  double* kh = qrow + d;
+  double* vh = kh + (size_t)c->S_max * d;
+  double* s = vh + (size_t)c->S_max * d;
+  for (int t = 0; t < d; ++t) qrow[t] = widen(c->q, (b * c->H_q + h) * d + t, c->qdtype);
+  for (int64_t j = 0; j < n; ++j) {
+    double ksj = c->ks[b * c->S_max + j], vsj = c->vs[b * c->S_max + j];
+    for (int t = 0; t < d; ++t) {
+      int64_t idx = ((b * c->S_max + j) * c->H_kv + kv) * d + t;
+      kh[j * d + t] = orc_e4m3_to_double(c->k8[idx]) * ksj;
+      vh[j * d + t] = orc_e4m3_to_double(c->v8[idx]) * vsj;
+    }
+  }
+  attend_row(qrow, kh, vh, n, d, c->scale, s, c->out + (b * c->H_q + h) * d,
+             c->lse + b * c->H_q + h);
+}
+
+int orc_decode_fp8(const void* q, int qdtype, const uint8_t* k8, const uint8_t* v8,
+                   const double* k_scale, const double* v_scale, const int32_t* seq_lens, int B,
+                   int S_max, int H_q, int H_kv, int d, double scale, double* out, double* lse,
+                   int nthreads) {
+  int rc = check_heads(B, S_max, H_q, H_kv, d);
+  if (rc) return rc;
+  if (qdtype != ORC_F64 && qdtype != ORC_BF16) return -3;
+  for (int b = 0; b < B; ++b)
+    if (seq_lens[b] < 1 || seq_lens[b] > S_max) return -4;
+  fp8_ctx c = {q, qdtype, k8, v8, k_scale, v_scale, seq_lens, B, S_max, H_q, H_kv, d, scale,
+               out, lse};
+  size_t scratch = (size_t)d + 3 * (size_t)S_max * d;
+  return run_pool(fp8_task, &c, (int64_t)B * H_q, scratch, nthreads);
 }

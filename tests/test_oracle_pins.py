@@ -468,3 +468,25 @@ def test_paged_decode_rejects_bad_pages(oracle_mod):
     kp = np.zeros((2, 4, 1, 8))
     with pytest.raises(ValueError):
         oracle_mod.decode_paged(np.zeros((1, 1, 8)), kp, kp, [[0, 2]], [8], 1.0)
+
+
+# ------------------------------------------------------------- FP8 cache ---
+def test_e4m3_decoding_matches_torch_for_every_code(oracle_mod):
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mine = np.array([oracle_mod.e4m3_to_double(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert (np.isnan(mine) == nan).all() and nan.sum() == 2  # 0x7f and 0xff
+    assert np.array_equal(mine[~nan], ref[~nan])
+    assert oracle_mod.e4m3_to_double(0x7E) == 448.0 and oracle_mod.e4m3_to_double(1) == 2.0 ** -9
+
+
+def test_fp8_decode_equals_decode_of_the_dequantised_cache(oracle_mod):
+    q, k8, v8, ks, vs, lens = inputs.decode_inputs_fp8(2, 8, 2, 32, 40, seed=3, seq_lens=[40, 9])
+    out8, lse8 = oracle_mod.decode_fp8(q, k8, v8, ks, vs, lens, 0.2)
+    kd = k8.view(torch.float8_e4m3fn).double() * ks.double()[:, :, None, None]
+    vd = v8.view(torch.float8_e4m3fn).double() * vs.double()[:, :, None, None]
+    out, lse = oracle_mod.decode(q.double(), kd, vd, lens, 0.2)
+    np.testing.assert_allclose(out8, out, atol=1e-14)
+    np.testing.assert_allclose(lse8, lse, atol=1e-14)
+    assert np.isfinite(out8).all()  # NaN codes and scales past seq_lens are never read
