@@ -14,13 +14,16 @@ from ._binding import (  # noqa: E402,F401
     GQA_OK,
     GQAError,
     decode,
+    decode_fp8,
     decode_paged,
     decode_workspace,
     gqa_attn_decode,
     gqa_attn_decode_combine,
     gqa_attn_decode_default_splits,
+    gqa_attn_decode_fp8,
     gqa_attn_decode_noalloc,
     gqa_attn_decode_paged,
+    gqa_attn_decode_paged_fp8,
     gqa_attn_decode_split_chunk,
     gqa_attn_decode_workspace_bytes,
     gqa_attn_prefill_causal,

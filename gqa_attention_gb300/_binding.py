@@ -31,6 +31,10 @@ SIGNATURES = {
     "gqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
     "gqa_attn_decode_paged": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P,
                                    _P, _P]),
+    "gqa_attn_decode_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P,
+                                 _P]),
+    "gqa_attn_decode_paged_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
+                                       _I, _P, _P, _P, _P]),
     "gqa_attn_prefill_causal": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "gqa_attn_prefill_chunk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
     "gqa_last_device_error": (_I, [_P]),
@@ -120,6 +124,24 @@ def gqa_attn_decode_paged(q, k_pool, v_pool, block_table, seq_lens, B, num_pages
                                         _ptr(seq_lens), B, num_pages, page_size, max_blocks, H_q,
                                         H_kv, d, scale, n_split, _ptr(workspace), _ptr(out),
                                         _ptr(lse), _stream(stream))
+
+
+def gqa_attn_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, seq_lens, B, S_max, H_q, H_kv, d,
+                        scale, n_split, workspace, out, lse, stream=None) -> int:
+    return load().gqa_attn_decode_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                      _ptr(v_scale), _ptr(seq_lens), B, S_max, H_q, H_kv, d, scale,
+                                      n_split, _ptr(workspace), _ptr(out), _ptr(lse),
+                                      _stream(stream))
+
+
+def gqa_attn_decode_paged_fp8(q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, B,
+                              num_pages, page_size, max_blocks, H_q, H_kv, d, scale, n_split,
+                              workspace, out, lse, stream=None) -> int:
+    return load().gqa_attn_decode_paged_fp8(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+                                            _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), B,
+                                            num_pages, page_size, max_blocks, H_q, H_kv, d, scale,
+                                            n_split, _ptr(workspace), _ptr(out), _ptr(lse),
+                                            _stream(stream))
 
 
 def gqa_attn_decode_noalloc(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale, n_split,
@@ -222,6 +244,42 @@ def decode_paged(q, k_pool, v_pool, block_table, seq_lens, scale=None, n_split=N
     _check(gqa_attn_decode_paged(q, k_pool, v_pool, block_table, seq_lens, B, P, B_p, max_blocks,
                                  H_q, H_kv, d, scale, n_split, workspace, out, lse, stream),
            "gqa_attn_decode_paged")
+    if n_split > 1:
+        _check(gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream),
+               "gqa_attn_decode_combine")
+    return out, lse
+
+
+def decode_fp8(q, k8, v8, k_scale, v_scale, seq_lens, scale=None, n_split=None, workspace=None,
+               out=None, lse=None, stream=None, block_table=None):
+    """FP8-cache split-KV decode + combine (paged when block_table is given)."""
+    import torch
+
+    B, H_q, d = q.shape
+    if block_table is None:
+        _, S_max, H_kv, _ = k8.shape
+    else:
+        P, B_p, H_kv, _ = k8.shape
+        S_max = block_table.shape[1] * B_p
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if n_split is None:
+        n_split = (gqa_attn_decode_default_splits(B, H_kv, S_max, d) if block_table is None
+                   else paged_default_splits(B, H_kv, S_max, d, B_p))
+    if out is None:
+        out = torch.empty((B, H_q, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
+    if n_split > 1 and workspace is None:
+        workspace = decode_workspace(B, H_q, d, n_split, q.device)
+    if block_table is None:
+        st = gqa_attn_decode_fp8(q, k8, v8, k_scale, v_scale, seq_lens, B, S_max, H_q, H_kv, d,
+                                 scale, n_split, workspace, out, lse, stream)
+    else:
+        st = gqa_attn_decode_paged_fp8(q, k8, v8, k_scale, v_scale, block_table, seq_lens, B, P,
+                                       B_p, block_table.shape[1], H_q, H_kv, d, scale, n_split,
+                                       workspace, out, lse, stream)
+    _check(st, "gqa_attn_decode_fp8")
     if n_split > 1:
         _check(gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream),
                "gqa_attn_decode_combine")

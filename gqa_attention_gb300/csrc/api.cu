@@ -67,9 +67,19 @@ gqa_status get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
   return GQA_OK;
 }
 
-// A bf16 tensor map of `rank` dims (innermost first); strides in bytes for dims 1.. .
+// A tensor map of `rank` dims (innermost first); strides in bytes for dims 1.. .
+gqa_status encode_map(CUtensorMap* map, CUtensorMapDataType type, const void* base, int rank,
+                      const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                      CUtensorMapSwizzle swz);
+
 gqa_status encode_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                        const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swz) {
+  return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides, box, swz);
+}
+
+gqa_status encode_map(CUtensorMap* map, CUtensorMapDataType type, const void* base, int rank,
+                      const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                      CUtensorMapSwizzle swz) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   gqa_status st = get_encoder(&enc);
   if (st != GQA_OK) return st;
@@ -81,7 +91,7 @@ gqa_status encode_bf16(CUtensorMap* map, const void* base, int rank, const uint6
     estr[i] = 1;
     if (i + 1 < rank) gstr[i] = strides[i];
   }
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim,
+  CUresult r = enc(map, type, rank, const_cast<void*>(base), gdim,
                    gstr, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GQA_OK : GQA_ERR_INVALID_ARG;
@@ -238,6 +248,97 @@ gqa_status gqa_attn_decode_paged(const void* q, const void* k_pool, const void* 
   p.page_size = page_size;
   p.num_pages = num_pages;
   return cuda_status(gqa::launch_decode_paged(p, tm_k, tm_v, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+namespace {
+
+// E4M3 cache maps: codes viewed as [rows][H_kv][d] bytes (boxes of box_rows rows
+// of one head, unswizzled) and the per-token scales as [outer][inner] fp32.
+gqa_status prepare_fp8_maps(const void* k8, const void* v8, const float* k_scale,
+                            const float* v_scale, long long rows, int box_rows, int H_kv, int d,
+                            int sc_inner, int sc_outer, CUtensorMap* tm_k, CUtensorMap* tm_v,
+                            CUtensorMap* tm_ks, CUtensorMap* tm_vs) {
+  if (!k8 || !v8 || !k_scale || !v_scale) return GQA_ERR_INVALID_ARG;
+  if (!aligned(k8, 16) || !aligned(v8, 16) || !aligned(k_scale, 16) || !aligned(v_scale, 16))
+    return GQA_ERR_INVALID_ARG;
+  if ((sc_inner * 4) % 16 != 0) return GQA_ERR_UNSUPPORTED;
+  const uint64_t dims[3] = {(uint64_t)d, (uint64_t)H_kv, (uint64_t)rows};
+  const uint64_t strides[2] = {(uint64_t)d, (uint64_t)H_kv * d};
+  const uint32_t box[3] = {(uint32_t)d, 1u, (uint32_t)box_rows};
+  gqa_status st;
+  if ((st = encode_map(tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, k8, 3, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)) != GQA_OK)
+    return st;
+  if ((st = encode_map(tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, v8, 3, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)) != GQA_OK)
+    return st;
+  const uint64_t sdims[2] = {(uint64_t)sc_inner, (uint64_t)sc_outer};
+  const uint64_t sstr[1] = {(uint64_t)sc_inner * 4};
+  const uint32_t sbox[2] = {(uint32_t)box_rows, 1u};
+  if ((st = encode_map(tm_ks, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, k_scale, 2, sdims, sstr, sbox,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)) != GQA_OK)
+    return st;
+  return encode_map(tm_vs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, v_scale, 2, sdims, sstr, sbox,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+}  // namespace
+
+extern "C" {
+
+gqa_status gqa_attn_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale,
+                               const int32_t* seq_lens, int B, int S_max, int H_q, int H_kv,
+                               int d, float scale, int n_split, void* workspace, void* out,
+                               float* lse, gqa_stream_t stream) {
+  CUtensorMap tm_k, tm_v, tm_ks, tm_vs;
+  gqa::DecodeParams p;
+  // the bf16 maps encoded here are replaced below; this runs the shared checks
+  gqa_status st = prepare_decode(q, k_cache, v_cache, seq_lens, B, S_max, (long long)B * S_max,
+                                 gqa::kDecodeTile, H_q, H_kv, d, scale, n_split, workspace, out,
+                                 lse, &tm_k, &tm_v, &p);
+  if (st != GQA_OK) return st;
+  if ((st = prepare_fp8_maps(k_cache, v_cache, k_scale, v_scale, (long long)B * S_max,
+                             gqa::kDecodeTile, H_kv, d, S_max, B, &tm_k, &tm_v, &tm_ks,
+                             &tm_vs)) != GQA_OK)
+    return st;
+  return cuda_status(
+      gqa::launch_decode_fp8(p, tm_k, tm_v, tm_ks, tm_vs, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_attn_decode_paged_fp8(const void* q, const void* k_pool, const void* v_pool,
+                                     const float* k_scale, const float* v_scale,
+                                     const int32_t* block_table, const int32_t* seq_lens, int B,
+                                     int num_pages, int page_size, int max_blocks, int H_q,
+                                     int H_kv, int d, float scale, int n_split, void* workspace,
+                                     void* out, float* lse, gqa_stream_t stream) {
+  if (!block_table || !aligned(block_table, 4)) return GQA_ERR_INVALID_ARG;
+  if (num_pages < 1 || max_blocks < 1 || page_size < 1) return GQA_ERR_INVALID_ARG;
+  if (page_size < 16 || (page_size & (page_size - 1)) != 0) return GQA_ERR_UNSUPPORTED;
+  const long long S_max = (long long)max_blocks * page_size;
+  const long long rows = (long long)num_pages * page_size;
+  if (S_max > 0x7fffffffLL || rows > 0x7ffffffeLL) return GQA_ERR_INVALID_ARG;
+  if (n_split >= 1) {
+    const int chunk = gqa_attn_decode_split_chunk((int)S_max, n_split);
+    if (chunk / page_size + 2 > gqa::kMaxPagesPerCta) return GQA_ERR_UNSUPPORTED;
+  }
+  const int h = page_size < gqa::kDecodeTile ? page_size : gqa::kDecodeTile;
+  CUtensorMap tm_k, tm_v, tm_ks, tm_vs;
+  gqa::DecodeParams p;
+  gqa_status st = prepare_decode(q, k_pool, v_pool, seq_lens, B, (int)S_max, rows, h, H_q, H_kv,
+                                 d, scale, n_split, workspace, out, lse, &tm_k, &tm_v, &p);
+  if (st != GQA_OK) return st;
+  if ((st = prepare_fp8_maps(k_pool, v_pool, k_scale, v_scale, rows, h, H_kv, d, page_size,
+                             num_pages, &tm_k, &tm_v, &tm_ks, &tm_vs)) != GQA_OK)
+    return st;
+  p.block_table = block_table;
+  p.max_blocks = max_blocks;
+  p.page_size = page_size;
+  p.num_pages = num_pages;
+  return cuda_status(
+      gqa::launch_decode_fp8(p, tm_k, tm_v, tm_ks, tm_vs, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 gqa_status gqa_attn_decode_combine(const void* workspace, int B, int H_q, int d, int n_split,

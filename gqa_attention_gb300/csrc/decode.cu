@@ -49,9 +49,33 @@ struct DecodeLayout {
   }
 };
 
-template <int D, int NSTAGE>
+// FP8 cache stages: the E4M3 K and V tiles as TMA writes them (rows of D bytes,
+// unswizzled) and the tile's per-token K and V scales.  Each consumer warp
+// converts its own 16 rows into f16 tiles (DecodeLayout, 16-bit elements)
+// that the mma path then reads exactly as it reads bf16 tiles.
+// A tensor copy's shared-memory destination must be 128-byte aligned, so the
+// scales of each h-row segment (h = page rows, at least 16) get their own
+// 128-byte-aligned slot of round_up(4h, 128) bytes.
+template <int D>
+struct Fp8Layout {
+  static constexpr int kTile8 = kTile * D;   // bytes of one E4M3 tile
+  static constexpr int kScaleArea = 512;     // one tile's scales in up to 4 slots
+  static constexpr int kOffV8 = kTile8;
+  static constexpr int kOffKs = 2 * kTile8;
+  static constexpr int kOffVs = 2 * kTile8 + kScaleArea;
+  static constexpr int kTxBytes = 2 * kTile8 + 2 * kTile * 4;
+  static constexpr int kStageBytes = (2 * kTile8 + 2 * kScaleArea + 1023) / 1024 * 1024;
+  __host__ __device__ static constexpr int slot_bytes(int h) { return (h * 4 + 127) / 128 * 128; }
+  // byte offset of token `col` (0..63) of a tile inside a scale area
+  __device__ static __forceinline__ int scale_offset(int col, int h) {
+    return (col / h) * slot_bytes(h) + (col % h) * 4;
+  }
+};
+
+template <int D, int NSTAGE, bool FP8>
 constexpr int decode_smem_bytes() {
-  return NSTAGE * DecodeLayout<D>::kStageBytes + 1024;  // + alignment slack
+  return FP8 ? NSTAGE * Fp8Layout<D>::kStageBytes + 2 * DecodeLayout<D>::kTileBytes + 1024
+             : NSTAGE * DecodeLayout<D>::kStageBytes + 1024;  // + alignment slack
 }
 
 __device__ __forceinline__ float quad_max(float v) {
@@ -82,11 +106,21 @@ __device__ __forceinline__ float online_update(float (&x)[4], float& m, float& l
 // block table ("Attention Kernel 계보" p.17 §2-§4, p.18 §5): the producer warp
 // stages the CTA's page indices in shared memory once, then loads every page
 // segment of a tile with its own TMA box.
-template <int D, bool ROWS16, int NSTAGE, bool PAGED>
+// FP8 = true: the cache holds E4M3 codes with one fp32 scale per token
+// ("Attention Kernel 계보" p.17 §7); the scales arrive with the tile and are
+// applied in registers: score column j is multiplied by k_scale[j] and p_j by
+// v_scale[j], so the mma sees the exact E4M3 values (converted to f16, with Q
+// converted to f16 as well).
+template <int D, bool ROWS16, int NSTAGE, bool PAGED, bool FP8>
 __global__ void __launch_bounds__(kThreads, 2)
     gqa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
-                            const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+                            const __grid_constant__ CUtensorMap tm_v,
+                            const __grid_constant__ CUtensorMap tm_ks,
+                            const __grid_constant__ CUtensorMap tm_vs, const DecodeParams p) {
   using Lay = DecodeLayout<D>;
+  using F8 = Fp8Layout<D>;
+  constexpr int kStageBytes = FP8 ? F8::kStageBytes : Lay::kStageBytes;
+  constexpr int kTxBytes = FP8 ? F8::kTxBytes : Lay::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[NSTAGE];
   __shared__ __align__(8) uint64_t empty_bar[NSTAGE];
@@ -170,6 +204,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) {
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
+      if (FP8) {
+        tma_prefetch_map(&tm_ks);
+        tma_prefetch_map(&tm_vs);
+      }
       int issued = 0;
       for (int i = 0; i < n_tiles; ++i) {
         const int st = i % NSTAGE;
@@ -180,10 +218,36 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
         const uint32_t fb = smem_u32(&full_bar[st]);
-        mbar_arrive_expect_tx(fb, Lay::kStageBytes);
-        const uint32_t dst_k = smem_base + st * Lay::kStageBytes;
+        mbar_arrive_expect_tx(fb, kTxBytes);
+        const uint32_t dst_k = smem_base + st * kStageBytes;
         const uint32_t dst_v = dst_k + Lay::kTileBytes;
-        if (!PAGED) {
+        if constexpr (FP8) {
+          // E4M3 rows (D bytes) and the per-token scales; page segments of
+          // h rows when paged.  Rows past the end read as zeros (TMA fill).
+          const int h = PAGED ? min(p.page_size, kTile) : kTile;
+          for (int sub = 0; sub < kTile / h; ++sub) {
+            const int tok = t0 + i * kTile + sub * h;
+            int row, sc_x, sc_y;
+            if (!PAGED) {
+              row = b * p.S_max + tok;
+              sc_x = tok;
+              sc_y = b;
+            } else if (tok < t_end) {
+              const int pg = pages_sm[tok / p.page_size - page0];
+              row = pg * p.page_size + tok % p.page_size;
+              sc_x = tok % p.page_size;
+              sc_y = pg;
+            } else {
+              row = p.num_pages * p.page_size;
+              sc_x = 0;
+              sc_y = p.num_pages;
+            }
+            tma_load_3d(dst_k + sub * h * D, &tm_k, fb, 0, kv, row);
+            tma_load_3d(dst_k + F8::kOffV8 + sub * h * D, &tm_v, fb, 0, kv, row);
+            tma_load_2d(dst_k + F8::kOffKs + sub * F8::slot_bytes(h), &tm_ks, fb, sc_x, sc_y);
+            tma_load_2d(dst_k + F8::kOffVs + sub * F8::slot_bytes(h), &tm_vs, fb, sc_x, sc_y);
+          }
+        } else if (!PAGED) {
           const int row = b * p.S_max + t0 + i * kTile;
 #pragma unroll
           for (int blk = 0; blk < Lay::kBlocks; ++blk) {
@@ -233,8 +297,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       qa[kk][1] = v1 ? q32[rb1 + c] : 0u;
       qa[kk][2] = v0 ? q32[rb0 + c + 4] : 0u;
       qa[kk][3] = v1 ? q32[rb1 + c + 4] : 0u;
+      if constexpr (FP8) {  // bf16 -> f16 (exact inside the f16 range)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat162 bv = *reinterpret_cast<const __nv_bfloat162*>(&qa[kk][e]);
+          const float2 f = __bfloat1622float2(bv);
+          qa[kk][e] = pack_f16x2(f.x, f.y);
+        }
+      }
     }
   }
+  const uint32_t dq_base = smem_base + NSTAGE * F8::kStageBytes;  // FP8: f16 K, V tiles
 
   float o[D / 8][4];
 #pragma unroll
@@ -259,9 +332,49 @@ __global__ void __launch_bounds__(kThreads, 2)
       aborted = true;
       break;
     }
-    const uint32_t kbase = smem_base + st * Lay::kStageBytes;
-    const uint32_t vbase = kbase + Lay::kTileBytes;
+    uint32_t kbase = smem_base + st * kStageBytes;
+    uint32_t vbase = kbase + Lay::kTileBytes;
     const int tok0 = t0 + i * kTile + warp * 16;  // first token of this warp's slice
+    float ksv[4], vsv[4];  // FP8: scales of this thread's 4 score columns
+    if constexpr (FP8) {
+      const uint32_t raw = smem_base + st * kStageBytes;
+      // E4M3 -> f16 for this warp's 16 rows of K and V: lane = (row, half of d).
+      const int row = warp * 16 + (lane >> 1), half = lane & 1;
+#pragma unroll
+      for (int kvsel = 0; kvsel < 2; ++kvsel) {
+        const uint32_t src = raw + kvsel * F8::kOffV8 + row * D + half * (D / 2);
+        const uint32_t dst = dq_base + kvsel * Lay::kTileBytes;
+#pragma unroll
+        for (int q16 = 0; q16 < D / 32; ++q16) {
+          uint32_t w0, w1, w2, w3;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                       : "r"(src + 16 * q16));
+          const int chunk = half * (D / 16) + 2 * q16;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + Lay::offset(row, chunk)),
+                       "r"(e4m3x2_to_f16x2(w0)), "r"(e4m3x2_to_f16x2(w0 >> 16)),
+                       "r"(e4m3x2_to_f16x2(w1)), "r"(e4m3x2_to_f16x2(w1 >> 16))
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + Lay::offset(row, chunk + 1)),
+                       "r"(e4m3x2_to_f16x2(w2)), "r"(e4m3x2_to_f16x2(w2 >> 16)),
+                       "r"(e4m3x2_to_f16x2(w3)), "r"(e4m3x2_to_f16x2(w3 >> 16))
+                       : "memory");
+        }
+      }
+      const uint8_t* sc_sm = smem + st * kStageBytes;
+      const int h = PAGED ? min(p.page_size, kTile) : kTile;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int col = warp * 16 + (e >> 1) * 8 + 2 * t + (e & 1);
+        const int off = F8::scale_offset(col, h);
+        ksv[e] = *reinterpret_cast<const float*>(sc_sm + F8::kOffKs + off);
+        vsv[e] = *reinterpret_cast<const float*>(sc_sm + F8::kOffVs + off);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));  // raw stage no longer needed
+      kbase = dq_base;
+      vbase = dq_base + Lay::kTileBytes;
+    }
 
     // S = Q K^T over this warp's 16 tokens (two n8 tiles).
     float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -269,8 +382,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int kk = 0; kk < D / 16; ++kk) {
       uint32_t b00, b01, b10, b11;
       ldsm_x4(kbase + Lay::offset(k_row, kk * 2 + k_chk), b00, b01, b10, b11);
-      mma_bf16_16816(sacc[0], qa[kk], b00, b01);
-      mma_bf16_16816(sacc[1], qa[kk], b10, b11);
+      if constexpr (FP8) {
+        mma_f16_16816(sacc[0], qa[kk], b00, b01);
+        mma_f16_16816(sacc[1], qa[kk], b10, b11);
+      } else {
+        mma_bf16_16816(sacc[0], qa[kk], b00, b01);
+        mma_bf16_16816(sacc[1], qa[kk], b10, b11);
+      }
     }
 
     // Scores in base-2 units; tokens past the split end are masked by select.
@@ -282,8 +400,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int c = 0; c < 2; ++c) {
         const int tk = tok0 + nt * 8 + 2 * t + c;
         const bool ok = !partial || tk < t_end;
-        x0[nt * 2 + c] = ok ? sacc[nt][c] * p.scale_log2 : -INFINITY;
-        x1[nt * 2 + c] = ok ? sacc[nt][2 + c] * p.scale_log2 : -INFINITY;
+        const float sc = FP8 ? ksv[nt * 2 + c] * p.scale_log2 : p.scale_log2;
+        x0[nt * 2 + c] = ok ? sacc[nt][c] * sc : -INFINITY;
+        x1[nt * 2 + c] = ok ? sacc[nt][2 + c] * sc : -INFINITY;
+        if (FP8) vsv[nt * 2 + c] = ok ? vsv[nt * 2 + c] : 0.f;  // p * v_scale = 0 when masked
       }
     }
     float p0[4], p1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -301,10 +421,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     // P as the A operand of P V (k = this warp's 16 tokens).
     uint32_t pa[4];
-    pa[0] = pack_bf16x2(p0[0], p0[1]);
-    pa[1] = pack_bf16x2(p1[0], p1[1]);
-    pa[2] = pack_bf16x2(p0[2], p0[3]);
-    pa[3] = pack_bf16x2(p1[2], p1[3]);
+    if constexpr (FP8) {  // fold the value scales into P (f16)
+      pa[0] = pack_f16x2(p0[0] * vsv[0], p0[1] * vsv[1]);
+      pa[1] = pack_f16x2(p1[0] * vsv[0], p1[1] * vsv[1]);
+      pa[2] = pack_f16x2(p0[2] * vsv[2], p0[3] * vsv[3]);
+      pa[3] = pack_f16x2(p1[2] * vsv[2], p1[3] * vsv[3]);
+    } else {
+      pa[0] = pack_bf16x2(p0[0], p0[1]);
+      pa[1] = pack_bf16x2(p1[0], p1[1]);
+      pa[2] = pack_bf16x2(p0[2], p0[3]);
+      pa[3] = pack_bf16x2(p1[2], p1[3]);
+    }
 
     // Values of masked tokens may be anything (even NaN): zero them in the
     // B fragments so that 0 * V cannot produce NaN.
@@ -318,11 +445,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int jj = 0; jj < D / 16; ++jj) {
       uint32_t v0, v1, v2, v3;
       ldsm_x4_trans(vbase + Lay::offset(v_row, jj * 2 + v_chk), v0, v1, v2, v3);
-      mma_bf16_16816(o[2 * jj], pa, v0 & vm0, v1 & vm1);
-      mma_bf16_16816(o[2 * jj + 1], pa, v2 & vm0, v3 & vm1);
+      if constexpr (FP8) {
+        mma_f16_16816(o[2 * jj], pa, v0 & vm0, v1 & vm1);
+        mma_f16_16816(o[2 * jj + 1], pa, v2 & vm0, v3 & vm1);
+      } else {
+        mma_bf16_16816(o[2 * jj], pa, v0 & vm0, v1 & vm1);
+        mma_bf16_16816(o[2 * jj + 1], pa, v2 & vm0, v3 & vm1);
+      }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
+    if (!FP8 && lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
   }
   (void)aborted;
 
@@ -516,11 +648,11 @@ inline cudaError_t set_smem_attr_once(const void* kern, int smem, unsigned char*
   return e;
 }
 
-template <int D, bool ROWS16, int NSTAGE, bool PAGED>
+template <int D, bool ROWS16, int NSTAGE, bool PAGED, bool FP8>
 cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                         cudaStream_t stream) {
-  constexpr int smem = decode_smem_bytes<D, NSTAGE>();
-  auto kern = gqa_decode_split_kernel<D, ROWS16, NSTAGE, PAGED>;
+                         const CUtensorMap& tm_ks, const CUtensorMap& tm_vs, cudaStream_t stream) {
+  constexpr int smem = decode_smem_bytes<D, NSTAGE, FP8>();
+  auto kern = gqa_decode_split_kernel<D, ROWS16, NSTAGE, PAGED, FP8>;
   static unsigned char done[64];
   cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem, done);
   if (e != cudaSuccess) return e;
@@ -534,17 +666,30 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tm_k, const C
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = GQA_SPLIT_PDL ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, kern, tm_k, tm_v, p);
+  e = cudaLaunchKernelEx(&cfg, kern, tm_k, tm_v, tm_ks, tm_vs, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool FP8>
 cudaError_t launch_split_rows(const DecodeParams& p, const CUtensorMap& tm_k,
-                              const CUtensorMap& tm_v, cudaStream_t stream) {
+                              const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
+                              const CUtensorMap& tm_vs, cudaStream_t stream) {
   constexpr int NSTAGE = D >= 128 ? GQA_DECODE_STAGES_D128 : 6;
-  if (p.G > 8) return launch_split<D, true, NSTAGE, PAGED>(p, tm_k, tm_v, stream);
-  return launch_split<D, false, NSTAGE, PAGED>(p, tm_k, tm_v, stream);
+  if (p.G > 8) return launch_split<D, true, NSTAGE, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+  return launch_split<D, false, NSTAGE, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+}
+
+template <bool PAGED, bool FP8>
+cudaError_t launch_split_d(const DecodeParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                           const CUtensorMap& tm_ks, const CUtensorMap& tm_vs,
+                           cudaStream_t stream) {
+  switch (p.d) {
+    case 32: return launch_split_rows<32, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+    case 64: return launch_split_rows<64, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+    case 128: return launch_split_rows<128, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int D>
@@ -568,22 +713,19 @@ cudaError_t launch_comb(const CombineParams& p, cudaStream_t stream) {
 
 cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, cudaStream_t stream) {
-  switch (p.d) {
-    case 32: return launch_split_rows<32, false>(p, tm_k, tm_v, stream);
-    case 64: return launch_split_rows<64, false>(p, tm_k, tm_v, stream);
-    case 128: return launch_split_rows<128, false>(p, tm_k, tm_v, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  return launch_split_d<false, false>(p, tm_k, tm_v, tm_k, tm_v, stream);
 }
 
 cudaError_t launch_decode_paged(const DecodeParams& p, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, cudaStream_t stream) {
-  switch (p.d) {
-    case 32: return launch_split_rows<32, true>(p, tm_k, tm_v, stream);
-    case 64: return launch_split_rows<64, true>(p, tm_k, tm_v, stream);
-    case 128: return launch_split_rows<128, true>(p, tm_k, tm_v, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  return launch_split_d<true, false>(p, tm_k, tm_v, tm_k, tm_v, stream);
+}
+
+cudaError_t launch_decode_fp8(const DecodeParams& p, const CUtensorMap& tm_k,
+                              const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
+                              const CUtensorMap& tm_vs, cudaStream_t stream) {
+  if (p.block_table) return launch_split_d<true, true>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+  return launch_split_d<false, true>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
 }
 
 cudaError_t launch_decode_combine(const CombineParams& p, cudaStream_t stream) {

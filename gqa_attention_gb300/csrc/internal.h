@@ -60,6 +60,10 @@ cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tm_k,
 cudaError_t launch_decode_combine(const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_decode_paged(const DecodeParams& p, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, cudaStream_t stream);
+// E4M3 cache with per-token scales; paged when p.block_table is set.
+cudaError_t launch_decode_fp8(const DecodeParams& p, const CUtensorMap& tm_k,
+                              const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
+                              const CUtensorMap& tm_vs, cudaStream_t stream);
 cudaError_t launch_prefill_causal(const PrefillParams& p, const CUtensorMap& tm_q,
                                   const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                   int num_sms, cudaStream_t stream);

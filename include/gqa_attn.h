@@ -141,6 +141,37 @@ gqa_status gqa_attn_decode_paged(const void* q, const void* k_pool, const void* 
                                  int d, float scale, int n_split, void* workspace, void* out,
                                  float* lse, gqa_stream_t stream);
 
+/* Stage 1 of split-KV decode over an FP8 KV cache ("Attention Kernel 계보",
+ * p.17 §7): keys and values are E4M3 codes (1 sign, 4 exponent bits with bias
+ * 7, 3 mantissa bits; 0x7f/0xff are NaN) with one fp32 scale per token shared
+ * by all KV heads; the key used is e4m3(k_cache[...]) * k_scale[b, t] (values
+ * likewise).  The dequantisation is fused into the sweep: the codes are
+ * converted exactly to f16 on chip, the key scale multiplies the score column
+ * and the value scale multiplies p before the P V product.  Q is converted to
+ * f16 for the Q K^T product, so |q| must stay below 65504.
+ *   k_cache, v_cache  device uint8 [B, S_max, H_kv, d] (16-byte aligned)
+ *   k_scale, v_scale  device fp32 [B, S_max] (16-byte aligned); S_max % 4 == 0
+ *                     (else GQA_ERR_UNSUPPORTED)
+ * Every other argument, the workspace and the follow-up combine are those of
+ * gqa_attn_decode().  Codes and scales past seq_lens[b] are never used. */
+gqa_status gqa_attn_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale,
+                               const int32_t* seq_lens, int B, int S_max, int H_q, int H_kv,
+                               int d, float scale, int n_split, void* workspace, void* out,
+                               float* lse, gqa_stream_t stream);
+
+/* The FP8 cache of gqa_attn_decode_fp8() in pages, as in gqa_attn_decode_paged():
+ *   k_pool, v_pool    device uint8 [num_pages, page_size, H_kv, d]
+ *   k_scale, v_scale  device fp32 [num_pages, page_size]: the scales of a page's
+ *                     tokens stored with the page (its B_p per-token scalars)
+ * and block_table, seq_lens, page_size, max_blocks as for the paged decode. */
+gqa_status gqa_attn_decode_paged_fp8(const void* q, const void* k_pool, const void* v_pool,
+                                     const float* k_scale, const float* v_scale,
+                                     const int32_t* block_table, const int32_t* seq_lens, int B,
+                                     int num_pages, int page_size, int max_blocks, int H_q,
+                                     int H_kv, int d, float scale, int n_split, void* workspace,
+                                     void* out, float* lse, gqa_stream_t stream);
+
 /* Split-KV decode that allocates nothing, for callers that cannot call
  * cudaMalloc when they decode: code inside a CUDA graph capture or an
  * allocator's critical section, or a serving process whose device memory pool

@@ -54,6 +54,8 @@ def test_paged_matches_oracle_and_contiguous(oracle_mod, page_size, n_split):
                                          seq_lens=[1024, 1, 517])
     kp, vp, table = _paginate(k, v, page_size, seed=page_size)
     ref_o, ref_l = oracle_mod.decode_paged(q, kp, vp, table, lens, 1 / math.sqrt(d))
+    if n_split is None:  # the paged default; the contiguous call below uses the same
+        n_split = g.paged_default_splits(B, H_kv, table.shape[1] * page_size, d, page_size)
     out, lse = g.decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), lens.to(DEV),
                               n_split=n_split)
     torch.cuda.synchronize()
