@@ -355,8 +355,8 @@ def run_ours(args, rank, world, dist):
 
 
 # ---------------------------------------------------- further workloads ---
-WORKLOADS = ("decode_tiny", "decode_ragged", "decode_paged16", "decode_paged128", "prefill_64k",
-             "prefill_window", "prefill_chunk")
+WORKLOADS = ("decode_tiny", "decode_ragged", "decode_paged16", "decode_paged128", "decode_fp8",
+             "decode_fp8_ragged", "prefill_64k", "prefill_window", "prefill_chunk")
 
 
 def _shuffled_pages(k, v, page_size, seed):
@@ -401,6 +401,38 @@ def run_workload(name, args):
         if g.gqa_last_device_error(stream) != g.GQA_OK:
             raise RuntimeError("device error")
         return ms
+
+    if name.startswith("decode_fp8"):
+        cfg = inputs.LLAMA70B_DECODE if name == "decode_fp8" else inputs.LLAMA70B_DECODE_RAGGED
+        q, k8, v8, ks, vs, lens = inputs.decode_inputs_fp8(cfg.B, cfg.H_q, cfg.H_kv, cfg.d,
+                                                           cfg.S_max, seed=0, ragged=cfg.ragged)
+        # bytes the sweep must read: E4M3 codes + one fp32 scale per token, for K and V
+        kv_bytes = 2 * int(lens.sum()) * (cfg.H_kv * cfg.d + 4)
+        copies = 1 if kv_bytes > 512 << 20 else 3
+        qd, ld = q.to(dev), lens.to(dev)
+        caches = [tuple(x.to(dev) for x in (k8, v8, ks, vs)) for _ in range(copies)]
+        n = 2 * g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, cfg.d)
+        ws = g.decode_workspace(cfg.B, cfg.H_q, cfg.d, n, dev)
+        out = torch.empty(cfg.B, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(cfg.B, cfg.H_q, dtype=torch.float32, device=dev)
+
+        def fstep(i):
+            kc, vc, ksc, vsc = caches[i % copies]
+            assert g.gqa_attn_decode_fp8(qd, kc, vc, ksc, vsc, ld, cfg.B, cfg.S_max, cfg.H_q,
+                                         cfg.H_kv, cfg.d, cfg.scale, n, ws, out, lse,
+                                         stream) == g.GQA_OK
+            assert g.gqa_attn_decode_combine(ws, cfg.B, cfg.H_q, cfg.d, n, out, lse,
+                                             stream) == g.GQA_OK
+
+        ms = timed(fstep)
+        gbs = kv_bytes / (ms * 1e-3) / 1e9
+        bf16_equiv = 2 * int(lens.sum()) * cfg.H_kv * cfg.d * 2
+        return {"metric": f"FP8-cache decode GB/s ({cfg.name})", "value": round(gbs, 2),
+                "unit": "GB/s", "ms_per_step": round(ms, 5), "steps": steps, "n_split": n,
+                "fp8_bytes": kv_bytes, "bf16_equivalent_GBs": round(bf16_equiv / (ms * 1e-3) / 1e9, 2),
+                "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
+                "l2": f"{copies} rotating cache copies" if copies > 1 else "inputs exceed L2",
+                "dtype": "e4m3 cache, bf16 q/out", "data": "synthetic"}
 
     if name.startswith("decode_paged"):
         cfg = inputs.LLAMA70B_DECODE

@@ -338,27 +338,26 @@ __global__ void __launch_bounds__(kThreads, 2)
     float ksv[4], vsv[4];  // FP8: scales of this thread's 4 score columns
     if constexpr (FP8) {
       const uint32_t raw = smem_base + st * kStageBytes;
-      // E4M3 -> f16 for this warp's 16 rows of K and V: lane = (row, half of d).
-      const int row = warp * 16 + (lane >> 1), half = lane & 1;
+      // E4M3 -> f16 for this warp's 16 rows of K and V.  Consecutive lanes take
+      // consecutive 16-byte pieces of a row (conflict-free reads); each piece
+      // becomes two 16-byte f16 chunks of the swizzled tile.
+      constexpr int kLanesPerRow = D / 16;
+      constexpr int kRowsPerPass = 32 / kLanesPerRow;
+      const int c16 = lane % kLanesPerRow;
 #pragma unroll
       for (int kvsel = 0; kvsel < 2; ++kvsel) {
-        const uint32_t src = raw + kvsel * F8::kOffV8 + row * D + half * (D / 2);
+        const uint8_t* src = smem + st * kStageBytes + kvsel * F8::kOffV8;
         const uint32_t dst = dq_base + kvsel * Lay::kTileBytes;
 #pragma unroll
-        for (int q16 = 0; q16 < D / 32; ++q16) {
-          uint32_t w0, w1, w2, w3;
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                       : "r"(src + 16 * q16));
-          const int chunk = half * (D / 16) + 2 * q16;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + Lay::offset(row, chunk)),
-                       "r"(e4m3x2_to_f16x2(w0)), "r"(e4m3x2_to_f16x2(w0 >> 16)),
-                       "r"(e4m3x2_to_f16x2(w1)), "r"(e4m3x2_to_f16x2(w1 >> 16))
-                       : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + Lay::offset(row, chunk + 1)),
-                       "r"(e4m3x2_to_f16x2(w2)), "r"(e4m3x2_to_f16x2(w2 >> 16)),
-                       "r"(e4m3x2_to_f16x2(w3)), "r"(e4m3x2_to_f16x2(w3 >> 16))
-                       : "memory");
+        for (int pass = 0; pass < 16 / kRowsPerPass; ++pass) {
+          const int row = warp * 16 + pass * kRowsPerPass + lane / kLanesPerRow;
+          const uint4 w = *reinterpret_cast<const uint4*>(src + row * D + 16 * c16);
+          st_shared_v4(dst + Lay::offset(row, 2 * c16), e4m3x2_to_f16x2(w.x),
+                       e4m3x2_to_f16x2(w.x >> 16), e4m3x2_to_f16x2(w.y),
+                       e4m3x2_to_f16x2(w.y >> 16));
+          st_shared_v4(dst + Lay::offset(row, 2 * c16 + 1), e4m3x2_to_f16x2(w.z),
+                       e4m3x2_to_f16x2(w.z >> 16), e4m3x2_to_f16x2(w.w),
+                       e4m3x2_to_f16x2(w.w >> 16));
         }
       }
       const uint8_t* sc_sm = smem + st * kStageBytes;

@@ -153,7 +153,9 @@ gqa_status gqa_attn_decode_paged(const void* q, const void* k_pool, const void* 
  *   k_scale, v_scale  device fp32 [B, S_max] (16-byte aligned); S_max % 4 == 0
  *                     (else GQA_ERR_UNSUPPORTED)
  * Every other argument, the workspace and the follow-up combine are those of
- * gqa_attn_decode().  Codes and scales past seq_lens[b] are never used. */
+ * gqa_attn_decode().  Codes and scales past seq_lens[b] are never used.  The
+ * on-chip conversion favours two CTAs per SM: twice
+ * gqa_attn_decode_default_splits() measured best. */
 gqa_status gqa_attn_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
                                const float* k_scale, const float* v_scale,
                                const int32_t* seq_lens, int B, int S_max, int H_q, int H_kv,
