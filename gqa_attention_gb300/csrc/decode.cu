@@ -24,6 +24,10 @@ namespace {
 #define GQA_COMBINE_PDL 1  // launch the combine as a programmatic dependent of the split kernel
 #endif
 
+#ifndef GQA_DECODE_STAGES_FP8
+#define GQA_DECODE_STAGES_FP8 3  // FP8 stages are half as large as bf16 ones
+#endif
+
 #ifndef GQA_DECODE_STAGES_D128
 #define GQA_DECODE_STAGES_D128 3  // 3 x 32 KB stages: two CTAs fit on one SM
 #endif
@@ -674,7 +678,7 @@ template <int D, bool PAGED, bool FP8>
 cudaError_t launch_split_rows(const DecodeParams& p, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
                               const CUtensorMap& tm_vs, cudaStream_t stream) {
-  constexpr int NSTAGE = D >= 128 ? GQA_DECODE_STAGES_D128 : 6;
+  constexpr int NSTAGE = FP8 ? GQA_DECODE_STAGES_FP8 : (D >= 128 ? GQA_DECODE_STAGES_D128 : 6);
   if (p.G > 8) return launch_split<D, true, NSTAGE, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
   return launch_split<D, false, NSTAGE, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
 }
