@@ -341,7 +341,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int tok0 = t0 + i * kTile + warp * 16;  // first token of this warp's slice
     float ksv[4], vsv[4];  // FP8: scales of this thread's 4 score columns
     if constexpr (FP8) {
-      const uint32_t raw = smem_base + st * kStageBytes;
       // E4M3 -> f16 for this warp's 16 rows of K and V.  Consecutive lanes take
       // consecutive 16-byte pieces of a row (conflict-free reads); each piece
       // becomes two 16-byte f16 chunks of the swizzled tile.

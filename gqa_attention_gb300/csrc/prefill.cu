@@ -51,6 +51,11 @@ constexpr uint32_t kOffQ = 0;                  // Q_A, Q_B
 constexpr uint32_t kOffRing = 2 * kTileB;      // K/V slots
 constexpr uint32_t kPrefillSmem = kOffRing + kSlots * kTileB + 1024;
 constexpr float kRescaleLog2 = 8.f;
+// Registers per thread: 168 at launch (384 threads, one CTA per SM); warps
+// 0-3 (TMA, MMA, idle) give theirs up to the two softmax warpgroups.
+constexpr int kRegsLaunch = 168, kRegsCtl = 88, kRegsSoftmax = 208;
+static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kPThreads * kRegsLaunch,
+              "the register split must fit in the launch's registers");
 
 struct Item {
   int b, kv, hp, qt;
@@ -168,151 +173,155 @@ __global__ void __launch_bounds__(kPThreads, 1)
     return __all_sync(0xffffffffu, ok);
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------- TMA producer --
-    if (lane == 0) {
-      tma_prefetch_map(&tm_q);
-      tma_prefetch_map(&tm_k);
-      tma_prefetch_map(&tm_v);
-      uint32_t ring = 0, q_iter = 0;
-      bool ok = true;
-      for (int k = 0; ok && k < n_rounds; ++k) {
-        Item it;
-        if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, it)) continue;
-        const bool pair = 2 * it.hp + 1 < p.G;
-        const int hA = it.kv * p.G + 2 * it.hp;
-        if (q_iter > 0 && !wait(&q_empty, (q_iter - 1) & 1)) break;
-        const uint32_t qb = smem_u32(&q_full);
-        mbar_arrive_expect_tx(qb, pair ? 2 * kTileB : kTileB);
-        for (int dh = 0; dh < 2; ++dh) {
-          tma_load_4d(sb + kOffQ + dh * kHalfB, &tm_q, qb, dh * 64, hA, it.qt * 128, it.b);
-          if (pair)
-            tma_load_4d(sb + kOffQ + kTileB + dh * kHalfB, &tm_q, qb, dh * 64, hA + 1,
-                        it.qt * 128, it.b);
-        }
-        ++q_iter;
-        const Geom gm = item_geom<GENERAL>(p, it);
-        const int n = gm.n;
-        for (int j = 0; ok && j < n; ++j) {
-          for (int t = 0; t < 2; ++t) {  // K_j then V_j
-            const uint32_t slot = ring % kSlots;
-            if (ring >= kSlots && !wait(&slot_empty[slot], ((ring / kSlots) - 1) & 1)) {
-              ok = false;
-              break;
-            }
-            const uint32_t fb = smem_u32(&slot_full[slot]);
-            mbar_arrive_expect_tx(fb, kTileB);
-            const CUtensorMap* m = t == 0 ? &tm_k : &tm_v;
-            for (int dh = 0; dh < 2; ++dh)
-              tma_load_4d(sb + kOffRing + slot * kTileB + dh * kHalfB, m, fb, dh * 64, it.kv,
-                          (gm.j0 + j) * 128, it.b);
-            ++ring;
+  if (warp < 4) {
+    regs_dec<kRegsCtl>();
+    if (warp == 0) {
+      // ------------------------------------------------------- TMA producer --
+      if (lane == 0) {
+        tma_prefetch_map(&tm_q);
+        tma_prefetch_map(&tm_k);
+        tma_prefetch_map(&tm_v);
+        uint32_t ring = 0, q_iter = 0;
+        bool ok = true;
+        for (int k = 0; ok && k < n_rounds; ++k) {
+          Item it;
+          if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, it)) continue;
+          const bool pair = 2 * it.hp + 1 < p.G;
+          const int hA = it.kv * p.G + 2 * it.hp;
+          if (q_iter > 0 && !wait(&q_empty, (q_iter - 1) & 1)) break;
+          const uint32_t qb = smem_u32(&q_full);
+          mbar_arrive_expect_tx(qb, pair ? 2 * kTileB : kTileB);
+          for (int dh = 0; dh < 2; ++dh) {
+            tma_load_4d(sb + kOffQ + dh * kHalfB, &tm_q, qb, dh * 64, hA, it.qt * 128, it.b);
+            if (pair)
+              tma_load_4d(sb + kOffQ + kTileB + dh * kHalfB, &tm_q, qb, dh * 64, hA + 1,
+                          it.qt * 128, it.b);
           }
-        }
-      }
-      // No copy may still target shared memory when the CTA exits.
-      for (uint32_t r = ring > kSlots ? ring - kSlots : 0; r < ring; ++r)
-        mbar_wait(smem_u32(&slot_full[r % kSlots]), (r / kSlots) & 1, p.wait_ns, p.err);
-      if (q_iter > 0) mbar_wait(smem_u32(&q_full), (q_iter - 1) & 1, p.wait_ns, p.err);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------- MMA issuer (warp 1) --
-    {
-      constexpr uint32_t idS = instr_desc_bf16_f32(128, 128, false);
-      constexpr uint32_t idPV = instr_desc_bf16_f32(128, 128, true);
-      auto issue_s = [&](int x, uint32_t slot) {  // S_x = Q_x K^T
-        const uint32_t qa = sb + kOffQ + x * kTileB, kb = sb + kOffRing + slot * kTileB;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfB + (kk & 3) * 32;
-          tc_mma_ss(tmem + 128 * x, smem_desc_sw128(qa + off, 16, 1024),
-                    smem_desc_sw128(kb + off, 16, 1024), idS, kk > 0);
-        }
-      };
-      auto issue_pv = [&](int x, uint32_t slot, bool acc) {  // O_x (+)= P_x V, P_x in TMEM
-        const uint32_t vb = sb + kOffRing + slot * kTileB;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma_ts(tmem + 256 + 128 * x, tmem + 128 * x + 8 * kk,
-                    smem_desc_sw128(vb + kk * 2048, kHalfB, 1024), idPV, (acc || kk > 0) ? 1 : 0);
-      };
-      uint32_t ring = 0, q_iter = 0, pr_ph[2] = {0, 0}, oe_ph[2] = {0, 0};
-      bool o_busy[2] = {false, false};
-      bool ok = true;
-      for (int k = 0; ok && k < n_rounds; ++k) {
-        Item it;
-        if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, it)) continue;
-        const bool pair = 2 * it.hp + 1 < p.G;
-        const int nx = pair ? 2 : 1;
-        const int n = item_geom<GENERAL>(p, it).n;
-        if (!wait_all(&q_full, q_iter & 1)) break;
-        ++q_iter;
-        uint32_t kslot = ring % kSlots;
-        if (!wait_all(&slot_full[kslot], (ring / kSlots) & 1)) break;
-        ++ring;
-        tc_fence_after();
-        for (int x = 0; x < nx; ++x) {
-          issue_s(x, kslot);
-          tc_commit(smem_u32(&s_full[x]));
-        }
-        tc_commit(smem_u32(&slot_empty[kslot]));
-        if (n == 1) tc_commit(smem_u32(&q_empty));
-        for (int j = 0; ok && j < n; ++j) {
-          const uint32_t vslot = ring % kSlots;
-          if (!wait_all(&slot_full[vslot], (ring / kSlots) & 1)) {
-            ok = false;
-            break;
-          }
-          ++ring;
-          const bool more = j + 1 < n;
-          for (int x = 0; x < nx; ++x) {
-            if (!wait_all(&p_ready[x], pr_ph[x])) {
-              ok = false;
-              break;
-            }
-            pr_ph[x] ^= 1;
-            if (j == 0 && o_busy[x]) {  // the previous item's epilogue must have read O_x
-              if (!wait_all(&o_empty[x], oe_ph[x])) {
+          ++q_iter;
+          const Geom gm = item_geom<GENERAL>(p, it);
+          const int n = gm.n;
+          for (int j = 0; ok && j < n; ++j) {
+            for (int t = 0; t < 2; ++t) {  // K_j then V_j
+              const uint32_t slot = ring % kSlots;
+              if (ring >= kSlots && !wait(&slot_empty[slot], ((ring / kSlots) - 1) & 1)) {
                 ok = false;
                 break;
               }
-              oe_ph[x] ^= 1;
-              o_busy[x] = false;
+              const uint32_t fb = smem_u32(&slot_full[slot]);
+              mbar_arrive_expect_tx(fb, kTileB);
+              const CUtensorMap* m = t == 0 ? &tm_k : &tm_v;
+              for (int dh = 0; dh < 2; ++dh)
+                tma_load_4d(sb + kOffRing + slot * kTileB + dh * kHalfB, m, fb, dh * 64, it.kv,
+                            (gm.j0 + j) * 128, it.b);
+              ++ring;
             }
-            tc_fence_after();
-            issue_pv(x, vslot, j > 0);
-            if (more) {
-              if (x == 0) {
-                kslot = ring % kSlots;
-                if (!wait_all(&slot_full[kslot], (ring / kSlots) & 1)) {
+          }
+        }
+        // No copy may still target shared memory when the CTA exits.
+        for (uint32_t r = ring > kSlots ? ring - kSlots : 0; r < ring; ++r)
+          mbar_wait(smem_u32(&slot_full[r % kSlots]), (r / kSlots) & 1, p.wait_ns, p.err);
+        if (q_iter > 0) mbar_wait(smem_u32(&q_full), (q_iter - 1) & 1, p.wait_ns, p.err);
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------- MMA issuer (warp 1) --
+      {
+        constexpr uint32_t idS = instr_desc_bf16_f32(128, 128, false);
+        constexpr uint32_t idPV = instr_desc_bf16_f32(128, 128, true);
+        auto issue_s = [&](int x, uint32_t slot) {  // S_x = Q_x K^T
+          const uint32_t qa = sb + kOffQ + x * kTileB, kb = sb + kOffRing + slot * kTileB;
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfB + (kk & 3) * 32;
+            tc_mma_ss(tmem + 128 * x, smem_desc_sw128(qa + off, 16, 1024),
+                      smem_desc_sw128(kb + off, 16, 1024), idS, kk > 0);
+          }
+        };
+        auto issue_pv = [&](int x, uint32_t slot, bool acc) {  // O_x (+)= P_x V, P_x in TMEM
+          const uint32_t vb = sb + kOffRing + slot * kTileB;
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_ts(tmem + 256 + 128 * x, tmem + 128 * x + 8 * kk,
+                      smem_desc_sw128(vb + kk * 2048, kHalfB, 1024), idPV, (acc || kk > 0) ? 1 : 0);
+        };
+        uint32_t ring = 0, q_iter = 0, pr_ph[2] = {0, 0}, oe_ph[2] = {0, 0};
+        bool o_busy[2] = {false, false};
+        bool ok = true;
+        for (int k = 0; ok && k < n_rounds; ++k) {
+          Item it;
+          if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, it)) continue;
+          const bool pair = 2 * it.hp + 1 < p.G;
+          const int nx = pair ? 2 : 1;
+          const int n = item_geom<GENERAL>(p, it).n;
+          if (!wait_all(&q_full, q_iter & 1)) break;
+          ++q_iter;
+          uint32_t kslot = ring % kSlots;
+          if (!wait_all(&slot_full[kslot], (ring / kSlots) & 1)) break;
+          ++ring;
+          tc_fence_after();
+          for (int x = 0; x < nx; ++x) {
+            issue_s(x, kslot);
+            tc_commit(smem_u32(&s_full[x]));
+          }
+          tc_commit(smem_u32(&slot_empty[kslot]));
+          if (n == 1) tc_commit(smem_u32(&q_empty));
+          for (int j = 0; ok && j < n; ++j) {
+            const uint32_t vslot = ring % kSlots;
+            if (!wait_all(&slot_full[vslot], (ring / kSlots) & 1)) {
+              ok = false;
+              break;
+            }
+            ++ring;
+            const bool more = j + 1 < n;
+            for (int x = 0; x < nx; ++x) {
+              if (!wait_all(&p_ready[x], pr_ph[x])) {
+                ok = false;
+                break;
+              }
+              pr_ph[x] ^= 1;
+              if (j == 0 && o_busy[x]) {  // the previous item's epilogue must have read O_x
+                if (!wait_all(&o_empty[x], oe_ph[x])) {
                   ok = false;
                   break;
                 }
-                ++ring;
-                tc_fence_after();
+                oe_ph[x] ^= 1;
+                o_busy[x] = false;
               }
-              issue_s(x, kslot);
-              tc_commit(smem_u32(&s_full[x]));
-            } else {
-              tc_commit(smem_u32(&o_full[x]));
-              o_busy[x] = true;
+              tc_fence_after();
+              issue_pv(x, vslot, j > 0);
+              if (more) {
+                if (x == 0) {
+                  kslot = ring % kSlots;
+                  if (!wait_all(&slot_full[kslot], (ring / kSlots) & 1)) {
+                    ok = false;
+                    break;
+                  }
+                  ++ring;
+                  tc_fence_after();
+                }
+                issue_s(x, kslot);
+                tc_commit(smem_u32(&s_full[x]));
+              } else {
+                tc_commit(smem_u32(&o_full[x]));
+                o_busy[x] = true;
+              }
+            }
+            if (!ok) break;
+            tc_commit(smem_u32(&slot_empty[vslot]));
+            if (more) {
+              tc_commit(smem_u32(&slot_empty[kslot]));
+              if (j + 2 == n) tc_commit(smem_u32(&q_empty));
             }
           }
-          if (!ok) break;
-          tc_commit(smem_u32(&slot_empty[vslot]));
-          if (more) {
-            tc_commit(smem_u32(&slot_empty[kslot]));
-            if (j + 2 == n) tc_commit(smem_u32(&q_empty));
-          }
         }
+        // Every MMA issued here has completed (and every commit has landed)
+        // before tensor memory is released.
+        tc_commit(smem_u32(&drain));
+        mbar_wait(smem_u32(&drain), 0, p.wait_ns, p.err);
+        __syncwarp();
       }
-      // Every MMA issued here has completed (and every commit has landed)
-      // before tensor memory is released.
-      tc_commit(smem_u32(&drain));
-      mbar_wait(smem_u32(&drain), 0, p.wait_ns, p.err);
-      __syncwarp();
     }
-  } else if (warp >= 4) {
+  } else {
+    regs_inc<kRegsSoftmax>();
     // ------------------------------------------------ softmax + epilogue ----
     const int x = (warp - 4) >> 2;  // 0: head A, 1: head B
     const int quarter = warp & 3;   // tensor-memory lanes 32*quarter ..
