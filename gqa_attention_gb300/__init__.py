@@ -15,12 +15,15 @@ from ._binding import (  # noqa: E402,F401
     GQAError,
     decode,
     decode_fp8,
+    decode_fused,
     decode_paged,
     decode_workspace,
     gqa_attn_decode,
     gqa_attn_decode_combine,
     gqa_attn_decode_default_splits,
     gqa_attn_decode_fp8,
+    gqa_attn_decode_fused,
+    gqa_attn_decode_fused_splits,
     gqa_attn_decode_noalloc,
     gqa_attn_decode_paged,
     gqa_attn_decode_paged_fp8,

@@ -35,6 +35,8 @@ SIGNATURES = {
                                  _P]),
     "gqa_attn_decode_paged_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                        _I, _P, _P, _P, _P]),
+    "gqa_attn_decode_fused_splits": (_I, [_I, _I, _I, _I]),
+    "gqa_attn_decode_fused": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "gqa_attn_prefill_causal": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "gqa_attn_prefill_chunk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
     "gqa_last_device_error": (_I, [_P]),
@@ -115,6 +117,17 @@ def gqa_attn_decode(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale
 def gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream=None) -> int:
     return load().gqa_attn_decode_combine(_ptr(workspace), B, H_q, d, n_split, _ptr(out),
                                           _ptr(lse), _stream(stream))
+
+
+def gqa_attn_decode_fused_splits(B, H_q, H_kv, d) -> int:
+    return load().gqa_attn_decode_fused_splits(B, H_q, H_kv, d)
+
+
+def gqa_attn_decode_fused(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale, out, lse,
+                          stream=None) -> int:
+    return load().gqa_attn_decode_fused(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B,
+                                        S_max, H_q, H_kv, d, scale, _ptr(out), _ptr(lse),
+                                        _stream(stream))
 
 
 def gqa_attn_decode_paged(q, k_pool, v_pool, block_table, seq_lens, B, num_pages, page_size,
@@ -216,6 +229,23 @@ def decode(q, k_cache, v_cache, seq_lens, scale=None, n_split=None, workspace=No
     return out, lse
 
 
+def decode_fused(q, k_cache, v_cache, seq_lens, scale=None, out=None, lse=None, stream=None):
+    """Split-KV decode with the merge inside thread-block clusters (one launch, no workspace)."""
+    import torch
+
+    B, H_q, d = q.shape
+    _, S_max, H_kv, _ = k_cache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H_q, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
+    _check(gqa_attn_decode_fused(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale, out,
+                                 lse, stream), "gqa_attn_decode_fused")
+    return out, lse
+
+
 def paged_default_splits(B, H_kv, S_max, d, page_size):
     """Split count for the paged decode: the contiguous default, doubled for pages
     under 64 tokens (their smaller copies need two CTAs per SM in flight)."""
@@ -247,6 +277,23 @@ def decode_paged(q, k_pool, v_pool, block_table, seq_lens, scale=None, n_split=N
     if n_split > 1:
         _check(gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream),
                "gqa_attn_decode_combine")
+    return out, lse
+
+
+def decode_fused(q, k_cache, v_cache, seq_lens, scale=None, out=None, lse=None, stream=None):
+    """Split-KV decode with the merge inside thread-block clusters (one launch, no workspace)."""
+    import torch
+
+    B, H_q, d = q.shape
+    _, S_max, H_kv, _ = k_cache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H_q, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
+    _check(gqa_attn_decode_fused(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale, out,
+                                 lse, stream), "gqa_attn_decode_fused")
     return out, lse
 
 
@@ -282,6 +329,23 @@ def decode_fp8(q, k8, v8, k_scale, v_scale, seq_lens, scale=None, n_split=None, 
     if n_split > 1:
         _check(gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream),
                "gqa_attn_decode_combine")
+    return out, lse
+
+
+def decode_fused(q, k_cache, v_cache, seq_lens, scale=None, out=None, lse=None, stream=None):
+    """Split-KV decode with the merge inside thread-block clusters (one launch, no workspace)."""
+    import torch
+
+    B, H_q, d = q.shape
+    _, S_max, H_kv, _ = k_cache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H_q, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
+    _check(gqa_attn_decode_fused(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale, out,
+                                 lse, stream), "gqa_attn_decode_fused")
     return out, lse
 
 

@@ -158,14 +158,14 @@ gqa_status prepare_decode(const void* q, const void* k_cache, const void* v_cach
                           const int32_t* seq_lens, int B, int S_max, long long rows, int box_rows,
                           int H_q, int H_kv, int d, float scale, int n_split, void* workspace,
                           void* out, float* lse, CUtensorMap* tm_k, CUtensorMap* tm_v,
-                          gqa::DecodeParams* p) {
+                          gqa::DecodeParams* p, bool needs_workspace = true) {
   if (!q || !k_cache || !v_cache || !seq_lens || !out || !lse) return GQA_ERR_INVALID_ARG;
   if (B < 1 || S_max < 1 || H_q < 1 || H_kv < 1 || n_split < 1) return GQA_ERR_INVALID_ARG;
   if (B > 65535 || H_kv > 65535 || H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
   if (rows > 0x7fffffffLL || n_split > 0x7fffffff) return GQA_ERR_INVALID_ARG;
   if (!head_dim_ok(d) || H_q / H_kv > 16) return GQA_ERR_UNSUPPORTED;
-  if (n_split > 1 && !workspace) return GQA_ERR_INVALID_ARG;
+  if (needs_workspace && n_split > 1 && !workspace) return GQA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(lse, 4) || !aligned(seq_lens, 4) || (workspace && !aligned(workspace, 256)))
     return GQA_ERR_INVALID_ARG;
@@ -220,6 +220,52 @@ gqa_status gqa_attn_decode(const void* q, const void* k_cache, const void* v_cac
                                  lse, &tm_k, &tm_v, &p);
   if (st != GQA_OK) return st;
   return cuda_status(gqa::launch_decode_split(p, tm_k, tm_v, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int gqa_attn_decode_fused_splits(int B, int H_q, int H_kv, int d) {
+  if (B < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || !head_dim_ok(d) || H_q / H_kv > 16)
+    return 0;
+  // The largest cluster (16, else 8) whose CTAs can be resident together,
+  // probed once per device and head shape class.
+  static int cache[64][3][2];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const int di = d == 32 ? 0 : d == 64 ? 1 : 2, gi = H_q / H_kv > 8 ? 1 : 0;
+  if (dev >= 0 && dev < 64 && cache[dev][di][gi] != 0) return cache[dev][di][gi] > 0 ? cache[dev][di][gi] : 0;
+  int found = -1;
+  for (int c : {16, 8}) {
+    gqa::DecodeParams p{};
+    p.B = 1;
+    p.H_kv = 1;
+    p.G = H_q / H_kv;
+    p.d = d;
+    p.n_split = c;
+    CUtensorMap dummy{};
+    if (gqa::launch_decode_fused(p, dummy, dummy, true, nullptr) == cudaSuccess) {
+      found = c;
+      break;
+    }
+    cudaGetLastError();  // clear a failed probe
+  }
+  if (dev >= 0 && dev < 64) cache[dev][di][gi] = found;
+  return found > 0 ? found : 0;
+}
+
+gqa_status gqa_attn_decode_fused(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* seq_lens, int B, int S_max, int H_q, int H_kv,
+                                 int d, float scale, void* out, float* lse, gqa_stream_t stream) {
+  if (B < 1 || H_q < 1 || H_kv < 1) return GQA_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
+  const int c = gqa_attn_decode_fused_splits(B, H_q, H_kv, d);
+  if (c == 0) return GQA_ERR_UNSUPPORTED;
+  CUtensorMap tm_k, tm_v;
+  gqa::DecodeParams p;
+  gqa_status st = prepare_decode(q, k_cache, v_cache, seq_lens, B, S_max, (long long)B * S_max,
+                                 gqa::kDecodeTile, H_q, H_kv, d, scale, c, nullptr, out, lse,
+                                 &tm_k, &tm_v, &p, /*needs_workspace=*/false);
+  if (st != GQA_OK) return st;
+  return cuda_status(
+      gqa::launch_decode_fused(p, tm_k, tm_v, false, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 gqa_status gqa_attn_decode_paged(const void* q, const void* k_pool, const void* v_pool,

@@ -28,11 +28,16 @@ namespace {
 #define GQA_DECODE_STAGES_FP8 3  // FP8 stages are half as large as bf16 ones
 #endif
 
+#ifndef GQA_DECODE_FUSED_STAGES_D128
+#define GQA_DECODE_FUSED_STAGES_D128 3
+#endif
+
 #ifndef GQA_DECODE_STAGES_D128
 #define GQA_DECODE_STAGES_D128 3  // 3 x 32 KB stages: two CTAs fit on one SM
 #endif
 
 constexpr int kTile = kDecodeTile;  // tokens per stage
+constexpr int kMaxClusterSplits = 16;
 constexpr int kConsumerWarps = 4;   // 16 tokens each
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
@@ -76,6 +81,11 @@ struct Fp8Layout {
   }
 };
 
+// Shared-memory offset of a CTA's partial in the cluster merge: after the
+// four warps' partials (mO, mML) of the final in-CTA merge.
+template <int D>
+constexpr int kClusterPartOff = (4 * 16 * D * 4 + 4 * 16 * 8 + 15) / 16 * 16;
+
 template <int D, int NSTAGE, bool FP8>
 constexpr int decode_smem_bytes() {
   return FP8 ? NSTAGE * Fp8Layout<D>::kStageBytes + 2 * DecodeLayout<D>::kTileBytes + 1024
@@ -115,12 +125,20 @@ __device__ __forceinline__ float online_update(float (&x)[4], float& m, float& l
 // applied in registers: score column j is multiplied by k_scale[j] and p_j by
 // v_scale[j], so the mma sees the exact E4M3 values (converted to f16, with Q
 // converted to f16 as well).
-template <int D, bool ROWS16, int NSTAGE, bool PAGED, bool FP8>
+// CLUSTER = true: the n_split CTAs of one (KV head, sequence) form a thread-
+// block cluster and merge their partials themselves: each CTA leaves its
+// (m, l, O) in its own shared memory, and after a cluster barrier CTA `rank`
+// folds slice `rank` of the G x D outputs over all n_split partials, read
+// through distributed shared memory (the same associative merge as the
+// combine kernel, p.4 of "Attention Kernel 계보").  No workspace, no second
+// launch.
+template <int D, bool ROWS16, int NSTAGE, bool PAGED, bool FP8, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 2)
     gqa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v,
                             const __grid_constant__ CUtensorMap tm_ks,
                             const __grid_constant__ CUtensorMap tm_vs, const DecodeParams p) {
+  static_assert(!(CLUSTER && (PAGED || FP8)), "the cluster merge serves the contiguous bf16 cache");
   using Lay = DecodeLayout<D>;
   using F8 = Fp8Layout<D>;
   constexpr int kStageBytes = FP8 ? F8::kStageBytes : Lay::kStageBytes;
@@ -151,7 +169,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int e = threadIdx.x; e < G * D; e += kThreads) {
       const int r = e / D, c = e % D;
       const size_t row = (size_t)b * p.H_q + h0 + r;
-      if (p.n_split == 1) {
+      if (p.n_split == 1 || CLUSTER) {
+        // (a cluster's CTAs all see the same length and all return here)
+        if (CLUSTER && split != 0) continue;
         p.out[row * D + c] = __float2bfloat16(NAN);
         if (c == 0) p.lse[row] = NAN;
       } else if (c == 0) {
@@ -161,13 +181,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     return;
   }
   const int t0 = split * p.chunk;
-  if (t0 >= L) {  // empty split: the merge identity (-inf, 0); O is not written
+  if (!CLUSTER && t0 >= L) {  // empty split: the merge identity (-inf, 0); O is not written
     for (int r = threadIdx.x; r < G; r += kThreads)
       p.ws_ml[((size_t)b * p.H_q + h0 + r) * p.n_split + split] = make_float2(-INFINITY, 0.f);
     return;
   }
+  // (in a cluster an empty split still takes part: no tiles, partial (-inf, 0, 0))
   const int t_end = min(t0 + p.chunk, L);
-  const int n_tiles = (t_end - t0 + kTile - 1) / kTile;
+  const int n_tiles = t_end > t0 ? (t_end - t0 + kTile - 1) / kTile : 0;
 
   // Let a dependent combine launch get scheduled now; it waits for this grid.
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -281,6 +302,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       // No copy may still target this CTA's shared memory when it exits.
       for (int i = max(0, issued - NSTAGE); i < issued; ++i)
         mbar_wait(smem_u32(&full_bar[i % NSTAGE]), (i / NSTAGE) & 1, p.wait_ns, p.err);
+    }
+    if constexpr (CLUSTER) {  // the consumers' two cluster barriers
+      __syncwarp();
+      cluster_sync();
+      cluster_sync();
     }
     return;
   }
@@ -511,7 +537,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       Lsum = NAN;
       acc = make_float4(NAN, NAN, NAN, NAN);
     }
-    if (p.n_split == 1) {
+    if constexpr (CLUSTER) {
+      // this CTA's partial, kept for the cluster merge (m in base-2 units)
+      float* cO = reinterpret_cast<float*>(smem + kClusterPartOff<D>);
+      float2* cML = reinterpret_cast<float2*>(smem + kClusterPartOff<D> + 16 * D * 4);
+      *reinterpret_cast<float4*>(&cO[r * D + c4 * 4]) = acc;
+      if (c4 == 0) cML[r] = make_float2(M, Lsum);
+    } else if (p.n_split == 1) {
       const float inv = 1.f / Lsum;
       uint2 packed;
       packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
@@ -523,6 +555,47 @@ __global__ void __launch_bounds__(kThreads, 2)
       *reinterpret_cast<float4*>(&p.ws_O[idx * D + c4 * 4]) = acc;
       if (c4 == 0) p.ws_ml[idx] = make_float2(M * kLn2, Lsum);
     }
+  }
+
+  if constexpr (CLUSTER) {
+    __syncwarp();
+    cluster_sync();  // every partial of the cluster is in place
+    const int C = p.n_split;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t cO = smem_base + kClusterPartOff<D>;
+    const uint32_t cML = cO + 16 * D * 4;
+    const int total = G * D, per = (total + C - 1) / C;
+    for (int e = threadIdx.x; e < per; e += kConsumerWarps * 32) {
+      const int idx = static_cast<int>(rank) * per + e;
+      if (idx >= total) break;
+      const int r = idx / D, c = idx % D;
+      float2 ml[kMaxClusterSplits];
+      float Mx = -INFINITY;
+      bool bad = false;
+#pragma unroll
+      for (int q = 0; q < kMaxClusterSplits; ++q) {
+        if (q >= C) break;
+        ml[q] = ld_dsmem_f32x2(mapa_shared(cML + r * 8, q));
+        bad |= isnan(ml[q].x) || isnan(ml[q].y);
+        Mx = fmaxf(Mx, ml[q].x);
+      }
+      const float ref = (Mx == -INFINITY) ? 0.f : Mx;
+      float Lt = 0.f, acc = 0.f;
+#pragma unroll
+      for (int q = 0; q < kMaxClusterSplits; ++q) {
+        if (q >= C) break;
+        if (ml[q].x == -INFINITY) continue;  // empty split: weight 0
+        const float w = exp2f(ml[q].x - ref);
+        Lt += w * ml[q].y;
+        acc += w * ld_dsmem_f32(mapa_shared(cO + (r * D + c) * 4, q));
+      }
+      const bool poisoned = bad || !(Lt > 0.f);
+      const size_t row = (size_t)b * p.H_q + h0 + r;
+      p.out[row * D + c] = __float2bfloat16(poisoned ? NAN : acc / Lt);
+      if (c == 0) p.lse[row] = poisoned ? NAN : (Mx + log2f(Lt)) * kLn2;
+    }
+    __syncwarp();
+    cluster_sync();  // no CTA leaves while another may still read its partial
   }
 }
 
@@ -654,7 +727,7 @@ template <int D, bool ROWS16, int NSTAGE, bool PAGED, bool FP8>
 cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                          const CUtensorMap& tm_ks, const CUtensorMap& tm_vs, cudaStream_t stream) {
   constexpr int smem = decode_smem_bytes<D, NSTAGE, FP8>();
-  auto kern = gqa_decode_split_kernel<D, ROWS16, NSTAGE, PAGED, FP8>;
+  auto kern = gqa_decode_split_kernel<D, ROWS16, NSTAGE, PAGED, FP8, false>;
   static unsigned char done[64];
   cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem, done);
   if (e != cudaSuccess) return e;
@@ -694,6 +767,49 @@ cudaError_t launch_split_d(const DecodeParams& p, const CUtensorMap& tm_k, const
   }
 }
 
+// The cluster-merge launch: grid (C, H_kv, B) in clusters of (C, 1, 1), C =
+// p.n_split.  `probe` only reports whether such clusters can be resident.
+template <int D, bool ROWS16>
+cudaError_t launch_fused(const DecodeParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                         bool probe, cudaStream_t stream) {
+  constexpr int NSTAGE = D >= 128 ? GQA_DECODE_FUSED_STAGES_D128 : 6;
+  constexpr int smem = decode_smem_bytes<D, NSTAGE, false>();
+  static_assert(kClusterPartOff<D> + 16 * D * 4 + 16 * 8 <= NSTAGE * DecodeLayout<D>::kStageBytes,
+                "the cluster partial fits in the stage buffers");
+  auto kern = gqa_decode_split_kernel<D, ROWS16, NSTAGE, false, false, true>;
+  static unsigned char done[64];
+  cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem, done);
+  if (e != cudaSuccess) return e;
+  if (p.n_split > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_split, p.H_kv, p.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.n_split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = GQA_SPLIT_PDL ? 2 : 1;
+  if (probe) {
+    int n = 0;
+    cfg.numAttrs = 1;  // the cluster shape alone decides residency
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    return n >= 1 ? cudaSuccess : cudaErrorInvalidConfiguration;
+  }
+  e = cudaLaunchKernelEx(&cfg, kern, tm_k, tm_v, tm_k, tm_v, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_comb(const CombineParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -728,6 +844,24 @@ cudaError_t launch_decode_fp8(const DecodeParams& p, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_vs, cudaStream_t stream) {
   if (p.block_table) return launch_split_d<true, true>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
   return launch_split_d<false, true>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+}
+
+cudaError_t launch_decode_fused(const DecodeParams& p, const CUtensorMap& tm_k,
+                                const CUtensorMap& tm_v, bool probe, cudaStream_t stream) {
+  if (p.n_split < 1 || p.n_split > kMaxClusterSplits) return cudaErrorInvalidValue;
+  const bool rows16 = p.G > 8;
+  switch (p.d) {
+    case 32:
+      return rows16 ? launch_fused<32, true>(p, tm_k, tm_v, probe, stream)
+                    : launch_fused<32, false>(p, tm_k, tm_v, probe, stream);
+    case 64:
+      return rows16 ? launch_fused<64, true>(p, tm_k, tm_v, probe, stream)
+                    : launch_fused<64, false>(p, tm_k, tm_v, probe, stream);
+    case 128:
+      return rows16 ? launch_fused<128, true>(p, tm_k, tm_v, probe, stream)
+                    : launch_fused<128, false>(p, tm_k, tm_v, probe, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_decode_combine(const CombineParams& p, cudaStream_t stream) {

@@ -58,6 +58,11 @@ struct PrefillParams {
 cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, cudaStream_t stream);
 cudaError_t launch_decode_combine(const CombineParams& p, cudaStream_t stream);
+// Split decode whose n_split (<= 16) CTAs per (KV head, sequence) form a
+// cluster and merge in-cluster; probe = true only checks that such clusters
+// can be resident on the current device.
+cudaError_t launch_decode_fused(const DecodeParams& p, const CUtensorMap& tm_k,
+                                const CUtensorMap& tm_v, bool probe, cudaStream_t stream);
 cudaError_t launch_decode_paged(const DecodeParams& p, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, cudaStream_t stream);
 // E4M3 cache with per-token scales; paged when p.block_table is set.

@@ -243,6 +243,32 @@ gqa_status gqa_attn_prefill_chunk(const void* q, const void* k_cache, const void
                                   gqa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Decode with the merge inside thread-block clusters
+ * ------------------------------------------------------------------------ */
+
+/* Number of KV splits gqa_attn_decode_fused uses on the current device for
+ * this head shape: the largest cluster size (16, else 8) whose CTAs can be
+ * resident together; 0 when the shape is unsupported (d not 32/64/128, G > 16,
+ * H_q not a multiple of H_kv) or no such cluster fits. */
+int gqa_attn_decode_fused_splits(int B, int H_q, int H_kv, int d);
+
+/* The same computation as gqa_attn_decode followed by gqa_attn_decode_combine
+ * (split-KV sweep, then the log-sum-exp merge of the split partials;
+ * "Attention Kernel 계보" p.18 §4 and p.4), in one launch and without a
+ * workspace.  The n_split = gqa_attn_decode_fused_splits(...) CTAs of one
+ * (KV head, sequence) form a thread-block cluster; each keeps its partial
+ * (m, l, O) in shared memory, and the cluster folds them through distributed
+ * shared memory.  Arguments, layouts, outputs and error behaviour are those
+ * of gqa_attn_decode with n_split = 1 (out [B, H_q, d] bf16, lse [B, H_q]
+ * fp32, natural log; a bad seq_lens entry gives NaN rows and
+ * GQA_ERR_INVALID_ARG from gqa_last_device_error).  GQA_ERR_UNSUPPORTED when
+ * gqa_attn_decode_fused_splits returns 0.  Results differ from the two-kernel
+ * path only by rounding (a different split count). */
+gqa_status gqa_attn_decode_fused(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* seq_lens, int B, int S_max, int H_q, int H_kv,
+                                 int d, float scale, void* out, float* lse, gqa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics
  * ------------------------------------------------------------------------ */
 
