@@ -283,6 +283,10 @@ def run_ours(args, rank, world, dist):
         return None
 
     value = whole_job_rate(world, kv_bytes, dec_ms * 1e-3) / 1e9
+    ws_bytes = g.gqa_attn_decode_workspace_bytes(dc.B, dc.H_q, dc.d, n_split) if n_split > 1 else 0
+    all_bytes = (kv_bytes + dc.B * dc.H_q * dc.d * 2          # K/V read, Q read
+                 + 2 * ws_bytes                                # partials written, read back
+                 + dc.B * dc.H_q * (dc.d * 2 + 4))             # O (bf16) and LSE written
     achieved = kv_bytes / (split_ms * 1e-3) / 1e9
     traffic = _recorded_traffic("decode_split_llama70b_ctx32768.md",
                                 ["decode.cu", "common.cuh", "internal.h"])
@@ -303,6 +307,10 @@ def run_ours(args, rank, world, dist):
             "workload": f"{dc.name} (value) + {pc.name} (prefill)",
             "decode": {"B": dc.B, "H_q": dc.H_q, "H_kv": dc.H_kv, "d": dc.d, "ctx": dc.S_max,
                        "n_split": n_split, "kv_bytes": kv_bytes,
+                       # every byte the two launches move: K/V, Q, the split partials
+                       # written and read back, O and LSE
+                       "all_bytes": all_bytes,
+                       "all_bytes_GBs": round(all_bytes / (dec_ms * 1e-3) / 1e9, 2),
                        "ms_split_plus_combine": round(dec_ms, 5),
                        "ms_split_kernel": round(split_ms, 5),
                        "hbm_frac_of_" + peak_kind: round(value / world / hbm_gbs, 4),
@@ -553,10 +561,15 @@ def cpu_baseline(args, steps=1):
         oracle.decode(q, k, v, lens, dc.scale, nthreads=cores)
         times.append(time.perf_counter() - t0)
     t = statistics.median(times)
+    # the same sample on one core (the oracle's thread pool of one)
+    t0 = time.perf_counter()
+    oracle.decode(q, k, v, lens, dc.scale, nthreads=1)
+    t1 = time.perf_counter() - t0
     return {"value": round(kv_bytes / t / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle",
             "sample": f"whole {dc.name} decode (all 64 query heads, 32768 keys), fp64, "
-                      f"median of {len(times)} run(s), {t:.3f} s each"}
+                      f"median of {len(times)} run(s), {t:.3f} s each",
+            "value_1core": round(kv_bytes / t1 / 1e9, 4)}
 
 
 def run_reference(args, rank, world):

@@ -301,7 +301,7 @@ gqa_status gqa_attn_decode_paged(const void* q, const void* k_pool, const void* 
 namespace {
 
 // E4M3 cache maps: codes viewed as [rows][H_kv][d] bytes (boxes of box_rows rows
-// of one head, unswizzled) and the per-token scales as [outer][inner] fp32.
+// of one head, swizzled over d bytes) and the per-token scales as [outer][inner] fp32.
 gqa_status prepare_fp8_maps(const void* k8, const void* v8, const float* k_scale,
                             const float* v_scale, long long rows, int box_rows, int H_kv, int d,
                             int sc_inner, int sc_outer, CUtensorMap* tm_k, CUtensorMap* tm_v,
@@ -313,12 +313,17 @@ gqa_status prepare_fp8_maps(const void* k8, const void* v8, const float* k_scale
   const uint64_t dims[3] = {(uint64_t)d, (uint64_t)H_kv, (uint64_t)rows};
   const uint64_t strides[2] = {(uint64_t)d, (uint64_t)H_kv * d};
   const uint32_t box[3] = {(uint32_t)d, 1u, (uint32_t)box_rows};
+  // rows of d bytes, swizzled over all of them (the kernel reads 4-byte pieces
+  // of eight different rows per instruction without bank conflicts)
+  const CUtensorMapSwizzle swz = d == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : d == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                           : CU_TENSOR_MAP_SWIZZLE_32B;
   gqa_status st;
-  if ((st = encode_map(tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, k8, 3, dims, strides, box,
-                       CU_TENSOR_MAP_SWIZZLE_NONE)) != GQA_OK)
+  if ((st = encode_map(tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, k8, 3, dims, strides, box, swz)) !=
+      GQA_OK)
     return st;
-  if ((st = encode_map(tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, v8, 3, dims, strides, box,
-                       CU_TENSOR_MAP_SWIZZLE_NONE)) != GQA_OK)
+  if ((st = encode_map(tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, v8, 3, dims, strides, box, swz)) !=
+      GQA_OK)
     return st;
   const uint64_t sdims[2] = {(uint64_t)sc_inner, (uint64_t)sc_outer};
   const uint64_t sstr[1] = {(uint64_t)sc_inner * 4};

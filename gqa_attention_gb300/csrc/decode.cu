@@ -58,10 +58,12 @@ struct DecodeLayout {
   }
 };
 
-// FP8 cache stages: the E4M3 K and V tiles as TMA writes them (rows of D bytes,
-// unswizzled) and the tile's per-token K and V scales.  Each consumer warp
-// converts its own 16 rows into f16 tiles (DecodeLayout, 16-bit elements)
-// that the mma path then reads exactly as it reads bf16 tiles.
+// FP8 cache stages: the E4M3 K and V tiles as TMA writes them (rows of D
+// bytes, swizzled over min(D, 128) bytes) and the tile's per-token K and V
+// scales.  Both are read straight into mma fragments and converted to f16 in
+// registers (no f16 copy of the tile): a K fragment is 4 bytes of one key
+// row; a V fragment is one byte of 4 key rows, gathered as 4-byte pieces of
+// those rows and transposed with byte permutes.
 // A tensor copy's shared-memory destination must be 128-byte aligned, so the
 // scales of each h-row segment (h = page rows, at least 16) get their own
 // 128-byte-aligned slot of round_up(4h, 128) bytes.
@@ -74,6 +76,7 @@ struct Fp8Layout {
   static constexpr int kOffVs = 2 * kTile8 + kScaleArea;
   static constexpr int kTxBytes = 2 * kTile8 + 2 * kTile * 4;
   static constexpr int kStageBytes = (2 * kTile8 + 2 * kScaleArea + 1023) / 1024 * 1024;
+  static constexpr int kSpan = D < 128 ? D : 128;  // swizzle span of an E4M3 row
   __host__ __device__ static constexpr int slot_bytes(int h) { return (h * 4 + 127) / 128 * 128; }
   // byte offset of token `col` (0..63) of a tile inside a scale area
   __device__ static __forceinline__ int scale_offset(int col, int h) {
@@ -88,7 +91,7 @@ constexpr int kClusterPartOff = (4 * 16 * D * 4 + 4 * 16 * 8 + 15) / 16 * 16;
 
 template <int D, int NSTAGE, bool FP8>
 constexpr int decode_smem_bytes() {
-  return FP8 ? NSTAGE * Fp8Layout<D>::kStageBytes + 2 * DecodeLayout<D>::kTileBytes + 1024
+  return FP8 ? NSTAGE * Fp8Layout<D>::kStageBytes + 1024
              : NSTAGE * DecodeLayout<D>::kStageBytes + 1024;  // + alignment slack
 }
 
@@ -322,11 +325,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     const bool v0 = g < G, v1 = g + 8 < G;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      const int c = kk * 8 + t;  // 32-bit word index of columns (kk*16 + 2t, +1)
+      // bf16: 32-bit word c holds columns (kk*16 + 2t, +1), word c + 4 holds
+      // (kk*16 + 2t + 8, +1).  FP8: the k index of the fragment runs over d in
+      // the order its K fragment is loaded (4 consecutive bytes per lane):
+      // words kk*8 + 2t and kk*8 + 2t + 1 (columns kk*16 + 4t .. + 3).
+      const int c = FP8 ? kk * 8 + 2 * t : kk * 8 + t;
+      const int c2 = FP8 ? c + 1 : c + 4;
       qa[kk][0] = v0 ? q32[rb0 + c] : 0u;
       qa[kk][1] = v1 ? q32[rb1 + c] : 0u;
-      qa[kk][2] = v0 ? q32[rb0 + c + 4] : 0u;
-      qa[kk][3] = v1 ? q32[rb1 + c + 4] : 0u;
+      qa[kk][2] = v0 ? q32[rb0 + c2] : 0u;
+      qa[kk][3] = v1 ? q32[rb1 + c2] : 0u;
       if constexpr (FP8) {  // bf16 -> f16 (exact inside the f16 range)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -337,7 +345,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   }
-  const uint32_t dq_base = smem_base + NSTAGE * F8::kStageBytes;  // FP8: f16 K, V tiles
 
   float o[D / 8][4];
 #pragma unroll
@@ -367,53 +374,38 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int tok0 = t0 + i * kTile + warp * 16;  // first token of this warp's slice
     float ksv[4], vsv[4];  // FP8: scales of this thread's 4 score columns
     if constexpr (FP8) {
-      // E4M3 -> f16 for this warp's 16 rows of K and V.  Consecutive lanes take
-      // consecutive 16-byte pieces of a row (conflict-free reads); each piece
-      // becomes two 16-byte f16 chunks of the swizzled tile.
-      constexpr int kLanesPerRow = D / 16;
-      constexpr int kRowsPerPass = 32 / kLanesPerRow;
-      const int c16 = lane % kLanesPerRow;
-#pragma unroll
-      for (int kvsel = 0; kvsel < 2; ++kvsel) {
-        const uint8_t* src = smem + st * kStageBytes + kvsel * F8::kOffV8;
-        const uint32_t dst = dq_base + kvsel * Lay::kTileBytes;
-#pragma unroll
-        for (int pass = 0; pass < 16 / kRowsPerPass; ++pass) {
-          const int row = warp * 16 + pass * kRowsPerPass + lane / kLanesPerRow;
-          const uint4 w = *reinterpret_cast<const uint4*>(src + row * D + 16 * c16);
-          st_shared_v4(dst + Lay::offset(row, 2 * c16), e4m3x2_to_f16x2(w.x),
-                       e4m3x2_to_f16x2(w.x >> 16), e4m3x2_to_f16x2(w.y),
-                       e4m3x2_to_f16x2(w.y >> 16));
-          st_shared_v4(dst + Lay::offset(row, 2 * c16 + 1), e4m3x2_to_f16x2(w.z),
-                       e4m3x2_to_f16x2(w.z >> 16), e4m3x2_to_f16x2(w.w),
-                       e4m3x2_to_f16x2(w.w >> 16));
-        }
-      }
+      // Key order inside a warp's 16-key slice (FP8 only): the lane with
+      // fragment column g of score tile nt holds key 2g - (g & 1) + 2 nt, so
+      // lane (g, t) ends up with the scores of keys 4t .. 4t + 3, which are the
+      // A-fragment k indices 2t, 2t + 1, 2t + 8, 2t + 9 of P V.
       const uint8_t* sc_sm = smem + st * kStageBytes;
       const int h = PAGED ? min(p.page_size, kTile) : kTile;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int col = warp * 16 + (e >> 1) * 8 + 2 * t + (e & 1);
+        const int col = warp * 16 + 4 * t + e;  // key of score column e of this lane
         const int off = F8::scale_offset(col, h);
         ksv[e] = *reinterpret_cast<const float*>(sc_sm + F8::kOffKs + off);
         vsv[e] = *reinterpret_cast<const float*>(sc_sm + F8::kOffVs + off);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));  // raw stage no longer needed
-      kbase = dq_base;
-      vbase = dq_base + Lay::kTileBytes;
     }
 
     // S = Q K^T over this warp's 16 tokens (two n8 tiles).
     float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      uint32_t b00, b01, b10, b11;
-      ldsm_x4(kbase + Lay::offset(k_row, kk * 2 + k_chk), b00, b01, b10, b11);
       if constexpr (FP8) {
-        mma_f16_16816(sacc[0], qa[kk], b00, b01);
-        mma_f16_16816(sacc[1], qa[kk], b10, b11);
+        // K fragment straight from the E4M3 rows: 4 bytes (d = kk*16 + 4t ..)
+        // of key 2g - (g & 1) + 2 nt become the two f16 pairs of the fragment.
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int row = warp * 16 + 2 * g - (g & 1) + 2 * nt;
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(
+              smem + st * kStageBytes + swizzle<F8::kSpan>(row * D + kk * 16 + 4 * t));
+          mma_f16_16816(sacc[nt], qa[kk], e4m3x2_to_f16x2(w), e4m3x2_to_f16x2(w >> 16));
+        }
       } else {
+        uint32_t b00, b01, b10, b11;
+        ldsm_x4(kbase + Lay::offset(k_row, kk * 2 + k_chk), b00, b01, b10, b11);
         mma_bf16_16816(sacc[0], qa[kk], b00, b01);
         mma_bf16_16816(sacc[1], qa[kk], b10, b11);
       }
@@ -426,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        const int tk = tok0 + nt * 8 + 2 * t + c;
+        const int tk = FP8 ? tok0 + 4 * t + 2 * nt + c : tok0 + nt * 8 + 2 * t + c;
         const bool ok = !partial || tk < t_end;
         const float sc = FP8 ? ksv[nt * 2 + c] * p.scale_log2 : p.scale_log2;
         x0[nt * 2 + c] = ok ? sacc[nt][c] * sc : -INFINITY;
@@ -465,24 +457,45 @@ __global__ void __launch_bounds__(kThreads, 2)
     // B fragments so that 0 * V cannot produce NaN.
     uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
     if (partial) {
-      const int tk = tok0 + 2 * t;
+      // k indices 2t, 2t + 1 (vm0) and 2t + 8, 2t + 9 (vm1): keys tok0 + 2t ..
+      // (FP8 order: keys tok0 + 4t .. 4t + 3)
+      const int tk = FP8 ? tok0 + 4 * t : tok0 + 2 * t;
+      const int tk8 = FP8 ? tk + 2 : tk + 8;
       vm0 = (tk < t_end ? 0x0000ffffu : 0u) | (tk + 1 < t_end ? 0xffff0000u : 0u);
-      vm1 = (tk + 8 < t_end ? 0x0000ffffu : 0u) | (tk + 9 < t_end ? 0xffff0000u : 0u);
+      vm1 = (tk8 < t_end ? 0x0000ffffu : 0u) | (tk8 + 1 < t_end ? 0xffff0000u : 0u);
     }
+    if constexpr (FP8) {
+      // n-tile 4J + jj, fragment column g is d = 32J + 4g + jj: lane (g, t)
+      // reads d = 32J + 4g .. + 3 of keys 4t .. 4t + 3 (four 4-byte pieces)
+      // and transposes them so that byte e of word jj is key 4t + e at d + jj.
+      const uint8_t* vraw = smem + st * kStageBytes + F8::kOffV8;
 #pragma unroll
-    for (int jj = 0; jj < D / 16; ++jj) {
-      uint32_t v0, v1, v2, v3;
-      ldsm_x4_trans(vbase + Lay::offset(v_row, jj * 2 + v_chk), v0, v1, v2, v3);
-      if constexpr (FP8) {
-        mma_f16_16816(o[2 * jj], pa, v0 & vm0, v1 & vm1);
-        mma_f16_16816(o[2 * jj + 1], pa, v2 & vm0, v3 & vm1);
-      } else {
+      for (int J = 0; J < D / 32; ++J) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          w[e] = *reinterpret_cast<const uint32_t*>(
+              vraw + swizzle<F8::kSpan>((warp * 16 + 4 * t + e) * D + 32 * J + 4 * g));
+        const uint32_t lo01 = __byte_perm(w[0], w[1], 0x5140), hi01 = __byte_perm(w[0], w[1], 0x7362);
+        const uint32_t lo23 = __byte_perm(w[2], w[3], 0x5140), hi23 = __byte_perm(w[2], w[3], 0x7362);
+        const uint32_t x[4] = {__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo01, lo23, 0x7632),
+                               __byte_perm(hi01, hi23, 0x5410), __byte_perm(hi01, hi23, 0x7632)};
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+          mma_f16_16816(o[4 * J + jj], pa, e4m3x2_to_f16x2(x[jj]) & vm0,
+                        e4m3x2_to_f16x2(x[jj] >> 16) & vm1);
+      }
+    } else {
+#pragma unroll
+      for (int jj = 0; jj < D / 16; ++jj) {
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_trans(vbase + Lay::offset(v_row, jj * 2 + v_chk), v0, v1, v2, v3);
         mma_bf16_16816(o[2 * jj], pa, v0 & vm0, v1 & vm1);
         mma_bf16_16816(o[2 * jj + 1], pa, v2 & vm0, v3 & vm1);
       }
     }
     __syncwarp();
-    if (!FP8 && lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
+    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
   }
   (void)aborted;
 
@@ -498,11 +511,21 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (!failed) {
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) {
-      const int col = n * 8 + 2 * t;
-      *reinterpret_cast<float2*>(&mO[(warp * 16 + g) * D + col]) = make_float2(o[n][0], o[n][1]);
-      if (ROWS16)
-        *reinterpret_cast<float2*>(&mO[(warp * 16 + g + 8) * D + col]) =
-            make_float2(o[n][2], o[n][3]);
+      if constexpr (FP8) {  // fragment column c of n-tile 4J + jj is d = 32J + 4c + jj
+        const int col = (n >> 2) * 32 + 8 * t + (n & 3);
+        mO[(warp * 16 + g) * D + col] = o[n][0];
+        mO[(warp * 16 + g) * D + col + 4] = o[n][1];
+        if (ROWS16) {
+          mO[(warp * 16 + g + 8) * D + col] = o[n][2];
+          mO[(warp * 16 + g + 8) * D + col + 4] = o[n][3];
+        }
+      } else {
+        const int col = n * 8 + 2 * t;
+        *reinterpret_cast<float2*>(&mO[(warp * 16 + g) * D + col]) = make_float2(o[n][0], o[n][1]);
+        if (ROWS16)
+          *reinterpret_cast<float2*>(&mO[(warp * 16 + g + 8) * D + col]) =
+              make_float2(o[n][2], o[n][3]);
+      }
     }
     if (t == 0) {
       mML[warp * 16 + g] = make_float2(m0, l0);
