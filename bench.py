@@ -528,18 +528,24 @@ def run_workload(name, args):
     vis = (a + 1) if W < 0 else torch.minimum(a, torch.full_like(a, W)) + 1
     flops = 4.0 * d * H_q * B * float(vis.sum())
 
+    n_part = 1 if name == "prefill_64k" else g.gqa_attn_prefill_chunk_default_parts(
+        B, T_q, S_kv, H_q, H_kv)
+    ws = torch.empty(max(1, g.gqa_attn_prefill_chunk_workspace_bytes(B, T_q, H_q, d, n_part)),
+                     dtype=torch.uint8, device=dev)
+
     def step(i):
         if name == "prefill_64k":
             st = g.gqa_attn_prefill_causal(qd, kd, vd, B, T_q, H_q, H_kv, d, scale, out, lse, stream)
         else:
-            st = g.gqa_attn_prefill_chunk(qd, kd, vd, lens, B, T_q, S_kv, H_q, H_kv, d, scale, W,
-                                          out, lse, stream)
+            st = g.gqa_attn_prefill_chunk_split(qd, kd, vd, lens, B, T_q, S_kv, H_q, H_kv, d, scale,
+                                                W, n_part, ws, out, lse, stream)
         assert st == g.GQA_OK
 
     ms = timed(step)
     tf = flops / (ms * 1e-3) / 1e12
     return {"metric": f"prefill TFLOPS ({label})", "value": round(tf, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": steps, "flops_per_step": flops,
+            "n_part": n_part,
             "frac_of_" + peak_kind + "_bf16": round(tf / bf16_tf, 4), "dtype": "bf16",
             "data": "synthetic"}
 

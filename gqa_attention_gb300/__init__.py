@@ -31,6 +31,9 @@ from ._binding import (  # noqa: E402,F401
     gqa_attn_decode_workspace_bytes,
     gqa_attn_prefill_causal,
     gqa_attn_prefill_chunk,
+    gqa_attn_prefill_chunk_default_parts,
+    gqa_attn_prefill_chunk_split,
+    gqa_attn_prefill_chunk_workspace_bytes,
     gqa_last_device_error,
     gqa_selftest_wait_timeout,
     gqa_set_wait_limit_ns,

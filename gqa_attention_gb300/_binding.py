@@ -39,6 +39,10 @@ SIGNATURES = {
     "gqa_attn_decode_fused": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "gqa_attn_prefill_causal": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "gqa_attn_prefill_chunk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
+    "gqa_attn_prefill_chunk_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "gqa_attn_prefill_chunk_default_parts": (_I, [_I, _I, _I, _I, _I]),
+    "gqa_attn_prefill_chunk_split": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P,
+                                          _P, _P, _P]),
     "gqa_last_device_error": (_I, [_P]),
     "gqa_set_wait_limit_ns": (_U64, [_U64]),
     "gqa_selftest_wait_timeout": (_I, [_U64, _P]),
@@ -174,6 +178,21 @@ def gqa_attn_prefill_chunk(q, k_cache, v_cache, seq_lens, B, T_q, S_max, H_q, H_
     return load().gqa_attn_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B,
                                          T_q, S_max, H_q, H_kv, d, scale, int(window), _ptr(out),
                                          _ptr(lse), _stream(stream))
+
+
+def gqa_attn_prefill_chunk_workspace_bytes(B, T_q, H_q, d, n_part) -> int:
+    return load().gqa_attn_prefill_chunk_workspace_bytes(B, T_q, H_q, d, n_part)
+
+
+def gqa_attn_prefill_chunk_default_parts(B, T_q, S_max, H_q, H_kv) -> int:
+    return load().gqa_attn_prefill_chunk_default_parts(B, T_q, S_max, H_q, H_kv)
+
+
+def gqa_attn_prefill_chunk_split(q, k_cache, v_cache, seq_lens, B, T_q, S_max, H_q, H_kv, d, scale,
+                                 window, n_part, workspace, out, lse, stream=None) -> int:
+    return load().gqa_attn_prefill_chunk_split(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B, T_q, S_max, H_q, H_kv, d, scale,
+        int(window), int(n_part), _ptr(workspace), _ptr(out), _ptr(lse), _stream(stream))
 
 
 def gqa_last_device_error(stream=None) -> int:
@@ -367,8 +386,11 @@ def prefill_causal(q, k, v, scale=None, out=None, lse=None, stream=None):
 
 
 def prefill_chunk(q, k_cache, v_cache, seq_lens=None, scale=None, window=-1, out=None, lse=None,
-                  stream=None):
-    """Chunk of T_q queries ending each sequence (optionally windowed); returns (out, lse)."""
+                  stream=None, n_part=None, workspace=None):
+    """Chunk of T_q queries ending each sequence (optionally windowed); returns (out, lse).
+
+    n_part None picks gqa_attn_prefill_chunk_default_parts; n_part > 1 splits each work
+    item's key tiles into parts merged afterwards (workspace allocated when not given)."""
     import torch
 
     B, T_q, H_q, d = q.shape
@@ -379,8 +401,18 @@ def prefill_chunk(q, k_cache, v_cache, seq_lens=None, scale=None, window=-1, out
         out = torch.empty((B, T_q, H_q, d), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, H_q, T_q), dtype=torch.float32, device=q.device)
-    _check(gqa_attn_prefill_chunk(q, k_cache, v_cache, seq_lens, B, T_q, S_max, H_q, H_kv, d, scale,
-                                  window, out, lse, stream), "gqa_attn_prefill_chunk")
+    if n_part is None:
+        n_part = gqa_attn_prefill_chunk_default_parts(B, T_q, S_max, H_q, H_kv)
+    if n_part == 1:
+        _check(gqa_attn_prefill_chunk(q, k_cache, v_cache, seq_lens, B, T_q, S_max, H_q, H_kv, d,
+                                      scale, window, out, lse, stream), "gqa_attn_prefill_chunk")
+        return out, lse
+    if workspace is None:
+        nbytes = gqa_attn_prefill_chunk_workspace_bytes(B, T_q, H_q, d, n_part)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check(gqa_attn_prefill_chunk_split(q, k_cache, v_cache, seq_lens, B, T_q, S_max, H_q, H_kv, d,
+                                        scale, window, n_part, workspace, out, lse, stream),
+           "gqa_attn_prefill_chunk_split")
     return out, lse
 
 

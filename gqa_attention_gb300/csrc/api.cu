@@ -419,8 +419,11 @@ namespace {
 // sequence against S_kv key rows (chunk: the queries end each sequence).
 gqa_status run_prefill(bool chunk, const void* q, const void* k, const void* v,
                        const int32_t* seq_lens, int B, int S, int S_kv, int H_q, int H_kv, int d,
-                       float scale, int window, void* out, float* lse, gqa_stream_t stream) {
+                       float scale, int window, int n_part, void* workspace, void* out, float* lse,
+                       gqa_stream_t stream) {
   if (!q || !k || !v || !out || !lse) return GQA_ERR_INVALID_ARG;
+  if (n_part < 1 || n_part > 8 || (n_part > 1 && (!chunk || !workspace))) return GQA_ERR_INVALID_ARG;
+  if (workspace && !aligned(workspace, 256)) return GQA_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || S_kv < S || H_q < 1 || H_kv < 1 || H_q % H_kv != 0)
     return GQA_ERR_INVALID_ARG;
   if (B > 65535 || H_q > 65535 || !std::isfinite(scale) || !(scale > 0.f))
@@ -462,10 +465,17 @@ gqa_status run_prefill(bool chunk, const void* q, const void* k, const void* v,
   p.lse = lse;
   p.err = err;
   p.wait_ns = g_wait_ns.load();
+  p.n_part = n_part;
+  p.ws_ml = n_part > 1 ? static_cast<float2*>(workspace) : nullptr;
+  p.ws_O = n_part > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                 gqa::prefill_ws_O_offset((size_t)B * S * H_q, n_part))
+                      : nullptr;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int sms = num_sms_current_device();
-  return cuda_status(chunk ? gqa::launch_prefill_chunk(p, tm_q, tm_k, tm_v, sms, s)
-                           : gqa::launch_prefill_causal(p, tm_q, tm_k, tm_v, sms, s));
+  if (!chunk) return cuda_status(gqa::launch_prefill_causal(p, tm_q, tm_k, tm_v, sms, s));
+  st = cuda_status(gqa::launch_prefill_chunk(p, tm_q, tm_k, tm_v, sms, s));
+  if (st != GQA_OK || n_part == 1) return st;
+  return cuda_status(gqa::launch_prefill_merge(p, s));
 }
 
 }  // namespace
@@ -475,7 +485,8 @@ extern "C" {
 gqa_status gqa_attn_prefill_causal(const void* q, const void* k, const void* v, int B, int S,
                                    int H_q, int H_kv, int d, float scale, void* out, float* lse,
                                    gqa_stream_t stream) {
-  return run_prefill(false, q, k, v, nullptr, B, S, S, H_q, H_kv, d, scale, -1, out, lse, stream);
+  return run_prefill(false, q, k, v, nullptr, B, S, S, H_q, H_kv, d, scale, -1, 1, nullptr, out, lse,
+                     stream);
 }
 
 gqa_status gqa_attn_prefill_chunk(const void* q, const void* k_cache, const void* v_cache,
@@ -483,7 +494,41 @@ gqa_status gqa_attn_prefill_chunk(const void* q, const void* k_cache, const void
                                   int H_kv, int d, float scale, int window, void* out, float* lse,
                                   gqa_stream_t stream) {
   return run_prefill(true, q, k_cache, v_cache, seq_lens, B, T_q, S_max, H_q, H_kv, d, scale,
-                     window, out, lse, stream);
+                     window, 1, nullptr, out, lse, stream);
+}
+
+size_t gqa_attn_prefill_chunk_workspace_bytes(int B, int T_q, int H_q, int d, int n_part) {
+  if (B < 1 || T_q < 1 || H_q < 1 || d < 1 || n_part <= 1) return 0;
+  const size_t rows = (size_t)B * T_q * H_q;
+  return gqa::prefill_ws_O_offset(rows, n_part) + rows * n_part * d * sizeof(float);
+}
+
+int gqa_attn_prefill_chunk_default_parts(int B, int T_q, int S_max, int H_q, int H_kv) {
+  if (B < 1 || T_q < 1 || S_max < T_q || H_q < 1 || H_kv < 1 || H_q % H_kv != 0) return 1;
+  // Split only long items (>= 16 key tiles if the chunk ends the cache), and
+  // only when it evens out the last round of the persistent grid: the part
+  // count P in 1..4 maximising x / ceil(x), x = items * P / SMs, must beat
+  // P = 1 by at least 5% (a split costs a partial write, read and merge).
+  if (S_max / 128 < 16) return 1;
+  const long long items = (long long)((T_q + 127) / 128) * B * H_kv * ((H_q / H_kv + 1) / 2);
+  const int sms = num_sms_current_device();
+  auto eff = [&](int P) {
+    const double x = (double)items * P / sms;
+    return x / std::ceil(x);
+  };
+  int best = 1;
+  for (int P = 2; P <= 4; ++P)
+    if (eff(P) > eff(best) + 1e-9) best = P;
+  return eff(best) >= eff(1) + 0.05 ? best : 1;
+}
+
+gqa_status gqa_attn_prefill_chunk_split(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* seq_lens, int B, int T_q, int S_max,
+                                        int H_q, int H_kv, int d, float scale, int window,
+                                        int n_part, void* workspace, void* out, float* lse,
+                                        gqa_stream_t stream) {
+  return run_prefill(true, q, k_cache, v_cache, seq_lens, B, T_q, S_max, H_q, H_kv, d, scale,
+                     window, n_part, workspace, out, lse, stream);
 }
 
 gqa_status gqa_last_device_error(gqa_stream_t stream) {

@@ -52,7 +52,19 @@ struct PrefillParams {
   float* lse;          // [B, H_q, S]
   unsigned* err;
   uint64_t wait_ns;
+  // Chunk mode only: each item's key tiles are split into n_part parts run as
+  // separate work units; a part writes its unnormalised (m in base-2 units, l)
+  // and O for rows (b, i, h) -> (b * S + i) * H_q + h into the workspace, and
+  // launch_prefill_merge folds the parts.  n_part = 1: no split, no workspace.
+  int n_part;
+  float2* ws_ml;  // [rows][n_part]
+  float* ws_O;    // [rows][n_part][d]
 };
+
+// Byte offset of the O partials in a chunk-split prefill workspace.
+inline size_t prefill_ws_O_offset(size_t rows, int n_part) {
+  return (rows * n_part * sizeof(float2) + 255) / 256 * 256;
+}
 
 // Kernel launchers; each returns the launch status (cudaGetLastError).
 cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tm_k,
@@ -75,6 +87,7 @@ cudaError_t launch_prefill_causal(const PrefillParams& p, const CUtensorMap& tm_
 cudaError_t launch_prefill_chunk(const PrefillParams& p, const CUtensorMap& tm_q,
                                  const CUtensorMap& tm_k, const CUtensorMap& tm_v, int num_sms,
                                  cudaStream_t stream);
+cudaError_t launch_prefill_merge(const PrefillParams& p, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t stream);
 
 // Layout of the decode workspace: byte offset of the O partials.

@@ -58,18 +58,21 @@ static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kPThreads * kRegsLaunch,
               "the register split must fit in the launch's registers");
 
 struct Item {
-  int b, kv, hp, qt;
+  int b, kv, hp, qt, part;
 };
 
 // k-th item of this CTA: rounds of `grid` items, alternating direction, items
-// ordered by descending query tile (the heaviest first).
+// ordered by descending query tile (the heaviest first); the parts of one
+// split item are neighbours.
 __device__ __forceinline__ bool item_of(int k, int n_items, int per_qt, int n_qt, int n_pairs,
-                                        int H_kv, Item& it) {
+                                        int H_kv, int n_part, Item& it) {
   const int grid = gridDim.x, cta = blockIdx.x;
   const int idx = k * grid + ((k & 1) ? (grid - 1 - cta) : cta);
   if (idx >= n_items) return false;
   it.qt = n_qt - 1 - idx / per_qt;
   int r = idx % per_qt;
+  it.part = r % n_part;
+  r /= n_part;
   it.hp = r % n_pairs;
   r /= n_pairs;
   it.kv = r % H_kv;
@@ -106,6 +109,12 @@ __device__ __forceinline__ Geom item_geom(const PrefillParams& p, const Item& it
   const int lo = p.window >= 0 ? max(0, first - p.window) : 0;
   g.j0 = lo / 128;
   g.n = last / 128 - g.j0 + 1;
+  if (p.n_part > 1) {  // this part's share of the key tiles (possibly none)
+    const int a = g.j0 + (it.part * g.n) / p.n_part;
+    const int b = g.j0 + ((it.part + 1) * g.n) / p.n_part;
+    g.j0 = a;
+    g.n = b - a;
+  }
   return g;
 }
 
@@ -128,7 +137,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
   const int n_qt = (p.S + 127) / 128;
   const int n_pairs = (p.G + 1) / 2;
-  const int per_qt = p.B * p.H_kv * n_pairs;
+  const int per_qt = p.B * p.H_kv * n_pairs * p.n_part;
   const int n_items = n_qt * per_qt;
   const int n_rounds = (n_items + gridDim.x - 1) / gridDim.x;
   volatile int* abort_v = &abort_flag;
@@ -185,9 +194,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
         bool ok = true;
         for (int k = 0; ok && k < n_rounds; ++k) {
           Item it;
-          if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, it)) continue;
+          if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, p.n_part, it)) continue;
           const bool pair = 2 * it.hp + 1 < p.G;
           const int hA = it.kv * p.G + 2 * it.hp;
+          const Geom gm = item_geom<GENERAL>(p, it);
+          if (GENERAL && gm.n == 0) continue;  // an empty part: nothing to load
           if (q_iter > 0 && !wait(&q_empty, (q_iter - 1) & 1)) break;
           const uint32_t qb = smem_u32(&q_full);
           mbar_arrive_expect_tx(qb, pair ? 2 * kTileB : kTileB);
@@ -198,7 +209,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
                           it.qt * 128, it.b);
           }
           ++q_iter;
-          const Geom gm = item_geom<GENERAL>(p, it);
           const int n = gm.n;
           for (int j = 0; ok && j < n; ++j) {
             for (int t = 0; t < 2; ++t) {  // K_j then V_j
@@ -248,10 +258,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
         bool ok = true;
         for (int k = 0; ok && k < n_rounds; ++k) {
           Item it;
-          if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, it)) continue;
+          if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, p.n_part, it)) continue;
           const bool pair = 2 * it.hp + 1 < p.G;
           const int nx = pair ? 2 : 1;
           const int n = item_geom<GENERAL>(p, it).n;
+          if (GENERAL && n == 0) continue;  // an empty part: no work
           if (!wait_all(&q_full, q_iter & 1)) break;
           ++q_iter;
           uint32_t kslot = ring % kSlots;
@@ -335,13 +346,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
     bool alive = true;
     for (int k = 0; alive && k < n_rounds; ++k) {
       Item it;
-      if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, it)) continue;
+      if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, p.n_part, it)) continue;
       const bool pair = 2 * it.hp + 1 < p.G;
       if (x == 1 && !pair) continue;
       const int h = it.kv * p.G + 2 * it.hp + x;
       const Geom gm = item_geom<GENERAL>(p, it);
       const int n = gm.n;
       const int q_row = it.qt * 128 + r;
+      const size_t ws_row = (static_cast<size_t>(it.b) * p.S + q_row) * p.H_q + h;
+      if (GENERAL && n == 0) {  // an empty part: the merge identity (-inf, 0)
+        if (q_row < p.S) p.ws_ml[ws_row * p.n_part + it.part] = make_float2(-INFINITY, 0.f);
+        continue;
+      }
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
         if (!wait_all(&s_full[x], s_ph)) {
@@ -482,13 +498,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const bool store = q_row < p.S;
       if (GENERAL && gm.bad && x == 0 && warp == 4 && lane == 0) atomicOr(p.err, kErrBadSeqLen);
       __nv_bfloat16* dst = p.out + ((static_cast<size_t>(it.b) * p.S + q_row) * p.H_q + h) * 128;
+      const bool split = GENERAL && p.n_part > 1;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
         tmem_ld32(tO + 32 * c, o);
         tmem_wait_ld();
         reg_fence32(o);
-        if (store) {
+        if (split && store) {  // this part's unnormalised O, fp32
+          float4* d4 = reinterpret_cast<float4*>(p.ws_O + (ws_row * p.n_part + it.part) * 128 + 32 * c);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            d4[v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+        } else if (store) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
@@ -501,7 +524,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
           }
         }
       }
-      if (store)
+      if (split && store)
+        p.ws_ml[ws_row * p.n_part + it.part] =
+            gm.bad ? make_float2(NAN, NAN) : make_float2(m_ref, l);
+      else if (store)
         p.lse[(static_cast<size_t>(it.b) * p.H_q + h) * p.S + q_row] =
             (GENERAL && gm.bad) ? NAN : (m_ref + log2f(l)) * kLn2;
       tc_fence_before();
@@ -532,13 +558,68 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tm_q, cons
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = 1;
   }
-  const long long n_items = (long long)((p.S + 127) / 128) * p.B * p.H_kv * ((p.G + 1) / 2);
+  const long long n_items =
+      (long long)((p.S + 127) / 128) * p.B * p.H_kv * ((p.G + 1) / 2) * (GENERAL ? p.n_part : 1);
   const int grid = (int)(n_items < num_sms ? n_items : num_sms);
   kern<<<grid, kPThreads, kPrefillSmem, stream>>>(tm_q, tm_k, tm_v, p);
   return cudaGetLastError();
 }
 
+// Folds the n_part partials of every (b, i, h) row of a split chunk prefill
+// (the associative merge of "Attention Kernel 계보" p.4): one warp per row,
+// four columns per lane.  A part whose rows saw no key is the identity
+// (m = -inf, l = 0); a NaN partial (bad sequence length) makes the row NaN.
+__global__ void __launch_bounds__(256) gqa_prefill_merge_kernel(const PrefillParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t rows = static_cast<size_t>(p.B) * p.S * p.H_q;
+  const size_t row = static_cast<size_t>(blockIdx.x) * 8 + warp;
+  if (row >= rows) return;
+  const int P = p.n_part;
+  float M = -INFINITY;
+  bool bad = false;
+  for (int q = 0; q < P; ++q) {
+    const float2 ml = p.ws_ml[row * P + q];
+    bad |= isnan(ml.x) || isnan(ml.y);
+    M = fmaxf(M, ml.x);
+  }
+  const float ref = (M == -INFINITY) ? 0.f : M;
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int q = 0; q < P; ++q) {
+    const float2 ml = p.ws_ml[row * P + q];
+    if (ml.x == -INFINITY) continue;  // never written O is not read
+    const float w = exp2f(ml.x - ref);
+    L += w * ml.y;
+    const float4 o = reinterpret_cast<const float4*>(p.ws_O + (row * P + q) * 128)[lane];
+    acc.x += w * o.x;
+    acc.y += w * o.y;
+    acc.z += w * o.z;
+    acc.w += w * o.w;
+  }
+  const bool poisoned = bad || !(L > 0.f);
+  const float inv = poisoned ? NAN : 1.f / L;
+  uint2 packed;
+  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  reinterpret_cast<uint2*>(p.out + row * 128)[lane] = packed;
+  if (lane == 0) {
+    const int h = static_cast<int>(row % p.H_q);
+    const size_t bi = row / p.H_q;
+    const int i = static_cast<int>(bi % p.S);
+    const size_t b = bi / p.S;
+    p.lse[(b * p.H_q + h) * p.S + i] = poisoned ? NAN : (M + log2f(L)) * kLn2;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_prefill_merge(const PrefillParams& p, cudaStream_t stream) {
+  const long long rows = (long long)p.B * p.S * p.H_q;
+  const long long blocks = (rows + 7) / 8;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  gqa_prefill_merge_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prefill_causal(const PrefillParams& p, const CUtensorMap& tm_q,
                                   const CUtensorMap& tm_k, const CUtensorMap& tm_v, int num_sms,

@@ -242,6 +242,33 @@ gqa_status gqa_attn_prefill_chunk(const void* q, const void* k_cache, const void
                                   int H_kv, int d, float scale, int window, void* out, float* lse,
                                   gqa_stream_t stream);
 
+/* Bytes of workspace gqa_attn_prefill_chunk_split needs: per (b, query row,
+ * head) and part, the part's (m, l) pair (fp32) and its unnormalised O
+ * (d fp32), the O partials at a 256-byte-aligned offset.  0 when n_part <= 1. */
+size_t gqa_attn_prefill_chunk_workspace_bytes(int B, int T_q, int H_q, int d, int n_part);
+
+/* A part count for gqa_attn_prefill_chunk_split on the current device: 1 (no
+ * split) unless the work items are long (S_max >= 16 * 128) and splitting them
+ * evens out the last round of the persistent grid; at most 4. */
+int gqa_attn_prefill_chunk_default_parts(int B, int T_q, int S_max, int H_q, int H_kv);
+
+/* gqa_attn_prefill_chunk with each work item's key tiles split into n_part
+ * (1..8) contiguous parts that run as separate work units, so that few long
+ * items still spread evenly over the SMs.  Each part keeps its unnormalised
+ * (m, l, O) in `workspace` (device, 256-byte aligned, at least
+ * gqa_attn_prefill_chunk_workspace_bytes(B, T_q, H_q, d, n_part) bytes); a
+ * second launch merges the parts with the log-sum-exp merge ("Attention
+ * Kernel 계보" p.4) into out and lse.  Same arguments, layouts, outputs and
+ * errors as gqa_attn_prefill_chunk; n_part = 1 is exactly that call (workspace
+ * unused).  GQA_ERR_INVALID_ARG for n_part outside 1..8 or a missing or
+ * misaligned workspace with n_part > 1.  The result differs from the unsplit
+ * one only by rounding. */
+gqa_status gqa_attn_prefill_chunk_split(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* seq_lens, int B, int T_q, int S_max,
+                                        int H_q, int H_kv, int d, float scale, int window,
+                                        int n_part, void* workspace, void* out, float* lse,
+                                        gqa_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Decode with the merge inside thread-block clusters
  * ------------------------------------------------------------------------ */
