@@ -269,7 +269,7 @@ def paged_default_splits(B, H_kv, S_max, d, page_size):
     """Split count for the paged decode: the contiguous default, doubled for pages
     under 64 tokens (their smaller copies need two CTAs per SM in flight)."""
     n = gqa_attn_decode_default_splits(B, H_kv, S_max, d)
-    return 2 * n if page_size < 64 else n
+    return 2 * n if page_size < 64 and n > 1 else n
 
 
 def decode_paged(q, k_pool, v_pool, block_table, seq_lens, scale=None, n_split=None,

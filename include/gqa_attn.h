@@ -84,8 +84,9 @@ int gqa_attn_decode_split_chunk(int S_max, int n_split);
 size_t gqa_attn_decode_workspace_bytes(int B, int H_q, int d, int n_split);
 
 /* Deterministic split count for a (B, H_kv, S_max, d) decode on the current
- * device: about one CTA per SM, with splits of 128 to 8192 tokens.  Returns
- * >= 1 (1 for invalid input). */
+ * device: 1 for S_max <= 1024 (one CTA per sequence and KV head; no combine
+ * needed), otherwise about one CTA per SM, with splits of 128 to 8192 tokens.
+ * Returns >= 1 (1 for invalid input). */
 int gqa_attn_decode_default_splits(int B, int H_kv, int S_max, int d);
 
 /* Stage 1 of split-KV decode.
