@@ -90,8 +90,11 @@ struct Geom {
   int j0, n, q_off;
   bool bad;
 };
+constexpr int kLensSm = 256;  // sequence lengths kept in shared memory
+
 template <bool GENERAL>
-__device__ __forceinline__ Geom item_geom(const PrefillParams& p, const Item& it) {
+__device__ __forceinline__ Geom item_geom(const PrefillParams& p, const Item& it,
+                                          const int* lens_sm) {
   Geom g;
   if (!GENERAL) {
     g.j0 = 0;
@@ -100,7 +103,7 @@ __device__ __forceinline__ Geom item_geom(const PrefillParams& p, const Item& it
     g.bad = false;
     return g;
   }
-  int L = p.seq_lens ? p.seq_lens[it.b] : p.S_kv;
+  int L = !p.seq_lens ? p.S_kv : it.b < kLensSm ? lens_sm[it.b] : p.seq_lens[it.b];
   g.bad = L < p.S || L > p.S_kv;
   if (g.bad) L = p.S;
   g.q_off = L - p.S;
@@ -129,6 +132,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
   __shared__ __align__(8) uint64_t s_full[2], p_ready[2], o_full[2], o_empty[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  // every role derives each item's key range from seq_lens[b]: read it once
+  __shared__ int lens_sm[GENERAL ? kLensSm : 1];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -159,6 +164,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     abort_flag = 0;
     fence_barrier_init();
   }
+  if (GENERAL && p.seq_lens)
+    for (int i = threadIdx.x; i < min(p.B, kLensSm); i += kPThreads) lens_sm[i] = p.seq_lens[i];
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_base_sh), 512);
     tmem_relinquish();
@@ -197,7 +204,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, p.n_part, it)) continue;
           const bool pair = 2 * it.hp + 1 < p.G;
           const int hA = it.kv * p.G + 2 * it.hp;
-          const Geom gm = item_geom<GENERAL>(p, it);
+          const Geom gm = item_geom<GENERAL>(p, it, lens_sm);
           if (GENERAL && gm.n == 0) continue;  // an empty part: nothing to load
           if (q_iter > 0 && !wait(&q_empty, (q_iter - 1) & 1)) break;
           const uint32_t qb = smem_u32(&q_full);
@@ -261,7 +268,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (!item_of(k, n_items, per_qt, n_qt, n_pairs, p.H_kv, p.n_part, it)) continue;
           const bool pair = 2 * it.hp + 1 < p.G;
           const int nx = pair ? 2 : 1;
-          const int n = item_geom<GENERAL>(p, it).n;
+          const int n = item_geom<GENERAL>(p, it, lens_sm).n;
           if (GENERAL && n == 0) continue;  // an empty part: no work
           if (!wait_all(&q_full, q_iter & 1)) break;
           ++q_iter;
@@ -350,7 +357,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const bool pair = 2 * it.hp + 1 < p.G;
       if (x == 1 && !pair) continue;
       const int h = it.kv * p.G + 2 * it.hp + x;
-      const Geom gm = item_geom<GENERAL>(p, it);
+      const Geom gm = item_geom<GENERAL>(p, it, lens_sm);
       const int n = gm.n;
       const int q_row = it.qt * 128 + r;
       const size_t ws_row = (static_cast<size_t>(it.b) * p.S + q_row) * p.H_q + h;
