@@ -16,6 +16,7 @@ from ._binding import (  # noqa: E402,F401
     decode,
     decode_fp8,
     decode_fused,
+    decode_multi,
     decode_paged,
     decode_workspace,
     gqa_attn_decode,
@@ -24,6 +25,7 @@ from ._binding import (  # noqa: E402,F401
     gqa_attn_decode_fp8,
     gqa_attn_decode_fused,
     gqa_attn_decode_fused_splits,
+    gqa_attn_decode_multi,
     gqa_attn_decode_noalloc,
     gqa_attn_decode_paged,
     gqa_attn_decode_paged_fp8,

@@ -35,6 +35,7 @@ SIGNATURES = {
                                  _P]),
     "gqa_attn_decode_paged_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                        _I, _P, _P, _P, _P]),
+    "gqa_attn_decode_multi": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
     "gqa_attn_decode_fused_splits": (_I, [_I, _I, _I, _I]),
     "gqa_attn_decode_fused": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "gqa_attn_prefill_causal": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
@@ -121,6 +122,13 @@ def gqa_attn_decode(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale
 def gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream=None) -> int:
     return load().gqa_attn_decode_combine(_ptr(workspace), B, H_q, d, n_split, _ptr(out),
                                           _ptr(lse), _stream(stream))
+
+
+def gqa_attn_decode_multi(q, k_cache, v_cache, seq_lens, B, T_q, S_max, H_q, H_kv, d, scale,
+                          n_split, workspace, out, lse, stream=None) -> int:
+    return load().gqa_attn_decode_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B,
+                                        T_q, S_max, H_q, H_kv, d, scale, n_split, _ptr(workspace),
+                                        _ptr(out), _ptr(lse), _stream(stream))
 
 
 def gqa_attn_decode_fused_splits(B, H_q, H_kv, d) -> int:
@@ -248,6 +256,32 @@ def decode(q, k_cache, v_cache, seq_lens, scale=None, n_split=None, workspace=No
     return out, lse
 
 
+def decode_multi(q, k_cache, v_cache, seq_lens, scale=None, n_split=None, workspace=None, out=None,
+                 lse=None, stream=None):
+    """Decode of the last T_q positions of each sequence (q [B, T_q, H_q, d]); returns
+    (out bf16 [B, T_q, H_q, d], lse fp32 [B, T_q, H_q])."""
+    import torch
+
+    B, T_q, H_q, d = q.shape
+    _, S_max, H_kv, _ = k_cache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if n_split is None:
+        n_split = gqa_attn_decode_default_splits(B, H_kv, S_max, d)
+    if out is None:
+        out = torch.empty((B, T_q, H_q, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, T_q, H_q), dtype=torch.float32, device=q.device)
+    if n_split > 1 and workspace is None:
+        workspace = decode_workspace(B * T_q, H_q, d, n_split, q.device)
+    _check(gqa_attn_decode_multi(q, k_cache, v_cache, seq_lens, B, T_q, S_max, H_q, H_kv, d, scale,
+                                 n_split, workspace, out, lse, stream), "gqa_attn_decode_multi")
+    if n_split > 1:
+        _check(gqa_attn_decode_combine(workspace, B * T_q, H_q, d, n_split, out, lse, stream),
+               "gqa_attn_decode_combine")
+    return out, lse
+
+
 def decode_fused(q, k_cache, v_cache, seq_lens, scale=None, out=None, lse=None, stream=None):
     """Split-KV decode with the merge inside thread-block clusters (one launch, no workspace)."""
     import torch
@@ -299,23 +333,6 @@ def decode_paged(q, k_pool, v_pool, block_table, seq_lens, scale=None, n_split=N
     return out, lse
 
 
-def decode_fused(q, k_cache, v_cache, seq_lens, scale=None, out=None, lse=None, stream=None):
-    """Split-KV decode with the merge inside thread-block clusters (one launch, no workspace)."""
-    import torch
-
-    B, H_q, d = q.shape
-    _, S_max, H_kv, _ = k_cache.shape
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
-    if out is None:
-        out = torch.empty((B, H_q, d), dtype=torch.bfloat16, device=q.device)
-    if lse is None:
-        lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
-    _check(gqa_attn_decode_fused(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale, out,
-                                 lse, stream), "gqa_attn_decode_fused")
-    return out, lse
-
-
 def decode_fp8(q, k8, v8, k_scale, v_scale, seq_lens, scale=None, n_split=None, workspace=None,
                out=None, lse=None, stream=None, block_table=None):
     """FP8-cache split-KV decode + combine (paged when block_table is given)."""
@@ -348,23 +365,6 @@ def decode_fp8(q, k8, v8, k_scale, v_scale, seq_lens, scale=None, n_split=None, 
     if n_split > 1:
         _check(gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream),
                "gqa_attn_decode_combine")
-    return out, lse
-
-
-def decode_fused(q, k_cache, v_cache, seq_lens, scale=None, out=None, lse=None, stream=None):
-    """Split-KV decode with the merge inside thread-block clusters (one launch, no workspace)."""
-    import torch
-
-    B, H_q, d = q.shape
-    _, S_max, H_kv, _ = k_cache.shape
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
-    if out is None:
-        out = torch.empty((B, H_q, d), dtype=torch.bfloat16, device=q.device)
-    if lse is None:
-        lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
-    _check(gqa_attn_decode_fused(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale, out,
-                                 lse, stream), "gqa_attn_decode_fused")
     return out, lse
 
 

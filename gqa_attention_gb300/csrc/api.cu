@@ -189,6 +189,7 @@ gqa_status prepare_decode(const void* q, const void* k_cache, const void* v_cach
   *p = gqa::DecodeParams{};
   p->q = static_cast<const __nv_bfloat16*>(q);
   p->seq_lens = seq_lens;
+  p->T_q = 1;
   p->B = B;
   p->S_max = S_max;
   p->H_q = H_q;
@@ -223,6 +224,29 @@ gqa_status gqa_attn_decode(const void* q, const void* k_cache, const void* v_cac
                                  gqa::kDecodeTile, H_q, H_kv, d, scale, n_split, workspace, out,
                                  lse, &tm_k, &tm_v, &p);
   if (st != GQA_OK) return st;
+  return cuda_status(gqa::launch_decode_split(p, tm_k, tm_v, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_attn_decode_multi(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* seq_lens, int B, int T_q, int S_max, int H_q,
+                                 int H_kv, int d, float scale, int n_split, void* workspace,
+                                 void* out, float* lse, gqa_stream_t stream) {
+  if (T_q < 1 || T_q > 16 || T_q > S_max) return GQA_ERR_INVALID_ARG;
+  if (H_kv < 1 || H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
+  if (T_q * (H_q / H_kv) > 16) return GQA_ERR_UNSUPPORTED;  // one mma M tile of rows
+  if ((long long)B * T_q > 65535) return GQA_ERR_INVALID_ARG;
+  CUtensorMap tm_k, tm_v;
+  gqa::DecodeParams p;
+  gqa_status st = prepare_decode(q, k_cache, v_cache, seq_lens, B, S_max, (long long)B * S_max,
+                                 gqa::kDecodeTile, H_q, H_kv, d, scale, n_split, workspace, out,
+                                 lse, &tm_k, &tm_v, &p);
+  if (st != GQA_OK) return st;
+  p.T_q = T_q;
+  p.G = H_q / H_kv;
+  // the partials are laid out for B * T_q rows of H_q heads
+  p.ws_O = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                gqa::decode_ws_O_offset(B * T_q, H_q, n_split))
+                     : nullptr;
   return cuda_status(gqa::launch_decode_split(p, tm_k, tm_v, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -161,17 +161,23 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
   const int h0 = kv * G;
+  // mma row r (0..15) is query t = r / G of head h0 + r % G; rows past
+  // T_q * G are padding.
+  const int R = p.T_q * G;
+  auto out_row = [&](int r) -> size_t {
+    return ((size_t)b * p.T_q + r / G) * p.H_q + h0 + r % G;
+  };
   // Launched as a programmatic dependent of the previous kernel in the stream:
   // nothing is read or written before that kernel has completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int L = p.seq_lens[b];
 
   // ---- device-side argument check and empty splits (no pipeline needed) ----
-  if (L < 1 || L > p.S_max) {
+  if (L < p.T_q || L > p.S_max || L < 1) {
     if (threadIdx.x == 0 && split == 0 && kv == 0) atomicOr(p.err, kErrBadSeqLen);
-    for (int e = threadIdx.x; e < G * D; e += kThreads) {
+    for (int e = threadIdx.x; e < R * D; e += kThreads) {
       const int r = e / D, c = e % D;
-      const size_t row = (size_t)b * p.H_q + h0 + r;
+      const size_t row = out_row(r);
       if (p.n_split == 1 || CLUSTER) {
         // (a cluster's CTAs all see the same length and all return here)
         if (CLUSTER && split != 0) continue;
@@ -185,8 +191,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   const int t0 = split * p.chunk;
   if (!CLUSTER && t0 >= L) {  // empty split: the merge identity (-inf, 0); O is not written
-    for (int r = threadIdx.x; r < G; r += kThreads)
-      p.ws_ml[((size_t)b * p.H_q + h0 + r) * p.n_split + split] = make_float2(-INFINITY, 0.f);
+    for (int r = threadIdx.x; r < R; r += kThreads)
+      p.ws_ml[out_row(r) * p.n_split + split] = make_float2(-INFINITY, 0.f);
     return;
   }
   // (in a cluster an empty split still takes part: no tiles, partial (-inf, 0, 0))
@@ -320,9 +326,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint32_t qa[D / 16][4];
   {
     const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q);
-    const size_t rb0 = ((size_t)b * p.H_q + h0 + g) * (D / 2);
-    const size_t rb1 = rb0 + 8 * (D / 2);
-    const bool v0 = g < G, v1 = g + 8 < G;
+    const bool v0 = g < R, v1 = g + 8 < R;
+    const size_t rb0 = v0 ? out_row(g) * (D / 2) : 0;
+    const size_t rb1 = v1 ? out_row(g + 8) * (D / 2) : 0;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       // bf16: 32-bit word c holds columns (kk*16 + 2t, +1), word c + 4 holds
@@ -357,6 +363,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int k_chk = (lane >> 3) & 1;
   const int v_row = warp * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
   const int v_chk = lane >> 4;
+
+  // Key limits of rows g and g + 8 in this split: query t sees keys below
+  // L - T_q + 1 + t (the split end t_end for plain decode).
+  const int lim0 = min(t_end, L - p.T_q + 1 + g / G);
+  const int lim1 = min(t_end, L - p.T_q + 1 + (g + 8) / G);
+  const int lim_lo = min(lim0, lim1);
 
   bool aborted = false;
   for (int i = 0; i < n_tiles; ++i) {
@@ -412,18 +424,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     // Scores in base-2 units; tokens past the split end are masked by select.
-    const bool partial = tok0 + 16 > t_end;
+    const bool partial = tok0 + 16 > lim_lo;
     float x0[4], x1[4];  // row g (x0) and row g+8 (x1)
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int tk = FP8 ? tok0 + 4 * t + 2 * nt + c : tok0 + nt * 8 + 2 * t + c;
-        const bool ok = !partial || tk < t_end;
+        const bool ok0 = !partial || tk < lim0, ok1 = !partial || tk < lim1;
         const float sc = FP8 ? ksv[nt * 2 + c] * p.scale_log2 : p.scale_log2;
-        x0[nt * 2 + c] = ok ? sacc[nt][c] * sc : -INFINITY;
-        x1[nt * 2 + c] = ok ? sacc[nt][2 + c] * sc : -INFINITY;
-        if (FP8) vsv[nt * 2 + c] = ok ? vsv[nt * 2 + c] : 0.f;  // p * v_scale = 0 when masked
+        x0[nt * 2 + c] = ok0 ? sacc[nt][c] * sc : -INFINITY;
+        x1[nt * 2 + c] = ok1 ? sacc[nt][2 + c] * sc : -INFINITY;
+        // p * v_scale = 0 past the split end (the scale there may be anything)
+        if (FP8) vsv[nt * 2 + c] = (!partial || tk < t_end) ? vsv[nt * 2 + c] : 0.f;
       }
     }
     float p0[4], p1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -535,9 +548,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   named_bar_sync(1, kConsumerWarps * 32);
 
   constexpr int V4 = D / 4;
-  for (int e = threadIdx.x; e < G * V4; e += kConsumerWarps * 32) {
+  for (int e = threadIdx.x; e < R * V4; e += kConsumerWarps * 32) {
     const int r = e / V4, c4 = e % V4;
-    const size_t row = (size_t)b * p.H_q + h0 + r;
+    const size_t row = out_row(r);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float M = -INFINITY, Lsum = 0.f;
     if (!failed) {
@@ -587,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t rank = cluster_ctarank();
     const uint32_t cO = smem_base + kClusterPartOff<D>;
     const uint32_t cML = cO + 16 * D * 4;
-    const int total = G * D, per = (total + C - 1) / C;
+    const int total = R * D, per = (total + C - 1) / C;
     for (int e = threadIdx.x; e < per; e += kConsumerWarps * 32) {
       const int idx = static_cast<int>(rank) * per + e;
       if (idx >= total) break;
@@ -613,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         acc += w * ld_dsmem_f32(mapa_shared(cO + (r * D + c) * 4, q));
       }
       const bool poisoned = bad || !(Lt > 0.f);
-      const size_t row = (size_t)b * p.H_q + h0 + r;
+      const size_t row = out_row(r);
       p.out[row * D + c] = __float2bfloat16(poisoned ? NAN : acc / Lt);
       if (c == 0) p.lse[row] = poisoned ? NAN : (Mx + log2f(Lt)) * kLn2;
     }
@@ -774,7 +787,8 @@ cudaError_t launch_split_rows(const DecodeParams& p, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
                               const CUtensorMap& tm_vs, cudaStream_t stream) {
   constexpr int NSTAGE = FP8 ? GQA_DECODE_STAGES_FP8 : (D >= 128 ? GQA_DECODE_STAGES_D128 : 6);
-  if (p.G > 8) return launch_split<D, true, NSTAGE, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+  if (p.T_q * p.G > 8)  // rows g + 8 are live
+    return launch_split<D, true, NSTAGE, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
   return launch_split<D, false, NSTAGE, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
 }
 
@@ -872,7 +886,7 @@ cudaError_t launch_decode_fp8(const DecodeParams& p, const CUtensorMap& tm_k,
 cudaError_t launch_decode_fused(const DecodeParams& p, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, bool probe, cudaStream_t stream) {
   if (p.n_split < 1 || p.n_split > kMaxClusterSplits) return cudaErrorInvalidValue;
-  const bool rows16 = p.G > 8;
+  const bool rows16 = p.T_q * p.G > 8;
   switch (p.d) {
     case 32:
       return rows16 ? launch_fused<32, true>(p, tm_k, tm_v, probe, stream)

@@ -15,9 +15,14 @@ enum : unsigned { kErrTimeout = 1u, kErrBadSeqLen = 2u, kErrBadPage = 4u };
 constexpr int kDecodeTile = 64;  // tokens per decode pipeline stage; split chunks are multiples
 
 struct DecodeParams {
-  const __nv_bfloat16* q;  // [B, H_q, d]
+  const __nv_bfloat16* q;  // [B, T_q, H_q, d]
   const int32_t* seq_lens; // [B]
   int B, S_max, H_q, H_kv, G, d;
+  // Query rows per sequence: the last T_q positions L - T_q .. L - 1, query
+  // t seeing keys 0 .. L - T_q + t (1 for plain decode).  Row (b, t, h) is
+  // (b * T_q + t) * H_q + h of out [B, T_q, H_q, d], lse and the workspace;
+  // T_q * G <= 16 (the rows of one mma M tile).
+  int T_q;
   int n_split, chunk;
   float scale_log2;        // tau * log2(e)
   float2* ws_ml;           // [B, H_q, n_split]  (m in natural-log units, l)

@@ -271,6 +271,29 @@ gqa_status gqa_attn_prefill_chunk_split(const void* q, const void* k_cache, cons
                                         gqa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Multi-token decode
+ * ------------------------------------------------------------------------ */
+
+/* Decode of the last T_q positions of each sequence at once (speculative
+ * verification, multi-token prediction): query t (0 <= t < T_q) of sequence b
+ * sits at position L - T_q + t, L = seq_lens[b], and attends keys
+ * 0 .. L - T_q + t of the cache (causal, aligned to the end of the sequence:
+ * "Attention Kernel 계보" p.13 §1 with the chunk offset of ADR-0060 §5.4).
+ * The T_q * G query rows of one KV head are folded into the M dimension of
+ * the split-KV decode (so T_q * G <= 16; GQA_ERR_UNSUPPORTED otherwise; larger
+ * chunks go to gqa_attn_prefill_chunk).  q and out are bf16 [B, T_q, H_q, d],
+ * lse fp32 [B, T_q, H_q] (natural log); the cache layout, splits and errors
+ * are those of gqa_attn_decode, with the device check 1 <= T_q <= L <= S_max.
+ * With n_split > 1 the partials go to `workspace`
+ * (gqa_attn_decode_workspace_bytes(B * T_q, H_q, d, n_split) bytes) and
+ * gqa_attn_decode_combine(workspace, B * T_q, H_q, d, n_split, out, lse)
+ * merges them.  T_q = 1 is gqa_attn_decode. */
+gqa_status gqa_attn_decode_multi(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* seq_lens, int B, int T_q, int S_max, int H_q,
+                                 int H_kv, int d, float scale, int n_split, void* workspace,
+                                 void* out, float* lse, gqa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Decode with the merge inside thread-block clusters
  * ------------------------------------------------------------------------ */
 

@@ -1,0 +1,111 @@
+"""GPU parity of the multi-token decode (the last T_q positions of each sequence,
+causal among themselves) against the fp64 oracle's chunk rows, and against the
+chunked prefill path.  Cache rows past each sequence length hold NaN."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_attention_gb300 as g
+from gqa_attention_gb300 import inputs
+
+from parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gqa_attention_gb300 import build
+
+    build.build()
+    g.load()
+    yield
+    assert g.gqa_last_device_error() == g.GQA_OK
+
+
+def _inputs(B, T_q, S_max, H_q, H_kv, d, lens, seed):
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, T_q, H_q, d, generator=gen).to(torch.bfloat16)
+    k = torch.randn(B, S_max, H_kv, d, generator=gen).to(torch.bfloat16)
+    v = torch.randn(B, S_max, H_kv, d, generator=gen).to(torch.bfloat16)
+    for b, L in enumerate(lens):  # rows past each sequence must never be read
+        k[b, L:] = float("nan")
+        v[b, L:] = float("nan")
+    return q, k, v, torch.tensor(lens, dtype=torch.int32)
+
+
+def _multi(q, k, v, sl, n_split):
+    out, lse = g.decode_multi(q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV), n_split=n_split)
+    torch.cuda.synchronize()
+    return out.cpu(), lse.cpu()
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("T_q,G", [(1, 8), (2, 8), (4, 4), (3, 5), (16, 1), (2, 1)])
+@pytest.mark.parametrize("n_split", [1, 3, None])
+def test_matches_oracle_chunk_rows(oracle_mod, d, T_q, G, n_split):
+    H_kv = 2
+    lens = [T_q, 700, 64 + T_q]  # the shortest legal sequence, a long one, a tile edge
+    q, k, v, sl = _inputs(3, T_q, 700, G * H_kv, H_kv, d, lens, seed=7 * T_q + G + d)
+    ref_o, ref_l = oracle_mod.prefill_chunk_rows(q, k, v, 1 / math.sqrt(d), seq_lens=sl)
+    out, lse = _multi(q, k, v, sl, n_split)
+    # the oracle's chunk LSE is [B, H_q, T_q]; multi-token decode writes [B, T_q, H_q]
+    assert_parity(out, lse.transpose(1, 2), ref_o, ref_l,
+                  f"multi d={d} T_q={T_q} G={G} n_split={n_split}")
+
+
+def test_matches_chunked_prefill():
+    q, k, v, sl = _inputs(2, 2, 3000, 64, 8, 128, [3000, 1234], seed=5)
+    m_o, m_l = _multi(q, k, v, sl, None)
+    c_o, c_l = g.prefill_chunk(q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV))
+    torch.cuda.synchronize()
+    assert (m_o.float() - c_o.cpu().float()).abs().max().item() <= 2 ** -7
+    assert (m_l.transpose(1, 2) - c_l.cpu()).abs().max().item() <= 2e-5
+
+
+def test_t_q_1_is_plain_decode_bit_for_bit():
+    q, k, v, sl = inputs.decode_inputs(2, 16, 2, 128, 900, seed=3, seq_lens=[900, 77])
+    for n_split in (1, 4):
+        a_o, a_l = g.decode(q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV), n_split=n_split)
+        b_o, b_l = g.decode_multi(q[:, None].to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV),
+                                  n_split=n_split)
+        torch.cuda.synchronize()
+        assert torch.equal(a_o.view(torch.int16), b_o[:, 0].view(torch.int16))
+        assert torch.equal(a_l, b_l[:, 0])
+
+
+def test_length_shorter_than_t_q_gives_nan_and_error_word():
+    q, k, v, sl = _inputs(2, 4, 256, 8, 2, 64, [256, 3], seed=2)  # 3 < T_q
+    out, lse = _multi(q, k, v, sl, 2)
+    assert g.gqa_last_device_error() == g.GQA_ERR_INVALID_ARG
+    assert torch.isnan(out[1].float()).all() and torch.isnan(lse[1]).all()
+    assert torch.isfinite(out[0].float()).all() and torch.isfinite(lse[0]).all()
+
+
+def test_rejects_bad_host_arguments():
+    x = torch.empty(4096, dtype=torch.bfloat16, device=DEV)
+    t = torch.ones(2, dtype=torch.int32, device=DEV)
+    f = torch.empty(64, dtype=torch.float32, device=DEV)
+    # T_q * G = 3 * 8 = 24 rows: more than one mma tile
+    assert g.gqa_attn_decode_multi(x, x, x, t, 1, 3, 64, 16, 2, 128, 0.1, 1, None, x, f) == \
+        g.GQA_ERR_UNSUPPORTED
+    assert g.gqa_attn_decode_multi(x, x, x, t, 1, 0, 64, 8, 2, 128, 0.1, 1, None, x, f) == \
+        g.GQA_ERR_INVALID_ARG
+    assert g.gqa_attn_decode_multi(x, x, x, t, 1, 65, 64, 1, 1, 128, 0.1, 1, None, x, f) == \
+        g.GQA_ERR_INVALID_ARG  # T_q > S_max (and > 16)
+    assert g.gqa_attn_decode_multi(x, x, x, t, 1, 2, 64, 8, 2, 128, 0.1, 3, None, x, f) == \
+        g.GQA_ERR_INVALID_ARG  # n_split > 1 without a workspace
+
+
+def test_llama70b_two_token_verification_full_size(oracle_mod):
+    """Two query tokens ending a 32768-token Llama3-70B cache (G = 8: 16 rows)."""
+    q, k, v, sl = _inputs(1, 2, 32768, 64, 8, 128, [32768], seed=11)
+    ref_o, ref_l = oracle_mod.prefill_chunk_rows(q, k, v, 1 / math.sqrt(128), seq_lens=sl)
+    out, lse = _multi(q, k, v, sl, None)
+    assert_parity(out, lse.transpose(1, 2), ref_o, ref_l, "multi T_q=2 llama70b 32K")
+    assert np.isfinite(lse.numpy()).all()
