@@ -29,6 +29,7 @@ from ._binding import (  # noqa: E402,F401
     gqa_attn_decode_noalloc,
     gqa_attn_decode_paged,
     gqa_attn_decode_paged_fp8,
+    gqa_attn_decode_paged_multi,
     gqa_attn_decode_split_chunk,
     gqa_attn_decode_workspace_bytes,
     gqa_attn_prefill_causal,

@@ -36,6 +36,8 @@ SIGNATURES = {
     "gqa_attn_decode_paged_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                        _I, _P, _P, _P, _P]),
     "gqa_attn_decode_multi": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
+    "gqa_attn_decode_paged_multi": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                                         _P, _P, _P, _P]),
     "gqa_attn_decode_fused_splits": (_I, [_I, _I, _I, _I]),
     "gqa_attn_decode_fused": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "gqa_attn_prefill_causal": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
@@ -129,6 +131,15 @@ def gqa_attn_decode_multi(q, k_cache, v_cache, seq_lens, B, T_q, S_max, H_q, H_k
     return load().gqa_attn_decode_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B,
                                         T_q, S_max, H_q, H_kv, d, scale, n_split, _ptr(workspace),
                                         _ptr(out), _ptr(lse), _stream(stream))
+
+
+def gqa_attn_decode_paged_multi(q, k_pool, v_pool, block_table, seq_lens, B, T_q, num_pages,
+                                page_size, max_blocks, H_q, H_kv, d, scale, n_split, workspace,
+                                out, lse, stream=None) -> int:
+    return load().gqa_attn_decode_paged_multi(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), _ptr(seq_lens), B, T_q, num_pages,
+        page_size, max_blocks, H_q, H_kv, d, scale, n_split, _ptr(workspace), _ptr(out), _ptr(lse),
+        _stream(stream))
 
 
 def gqa_attn_decode_fused_splits(B, H_q, H_kv, d) -> int:
@@ -308,27 +319,41 @@ def paged_default_splits(B, H_kv, S_max, d, page_size):
 
 def decode_paged(q, k_pool, v_pool, block_table, seq_lens, scale=None, n_split=None,
                  workspace=None, out=None, lse=None, stream=None):
-    """Paged split-KV decode + combine on CUDA tensors; returns (out, lse)."""
+    """Paged split-KV decode + combine on CUDA tensors; returns (out, lse).
+
+    q [B, H_q, d] (out [B, H_q, d], lse [B, H_q]) or, for the last T_q positions of each
+    sequence, q [B, T_q, H_q, d] (out [B, T_q, H_q, d], lse [B, T_q, H_q])."""
     import torch
 
-    B, H_q, d = q.shape
+    multi = q.dim() == 4
+    if multi:
+        B, T_q, H_q, d = q.shape
+    else:
+        (B, H_q, d), T_q = q.shape, 1
     P, B_p, H_kv, _ = k_pool.shape
     max_blocks = block_table.shape[1]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if n_split is None:
         n_split = paged_default_splits(B, H_kv, max_blocks * B_p, d, B_p)
+    rows = (B, T_q, H_q) if multi else (B, H_q)
     if out is None:
-        out = torch.empty((B, H_q, d), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty(rows + (d,), dtype=torch.bfloat16, device=q.device)
     if lse is None:
-        lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
+        lse = torch.empty(rows, dtype=torch.float32, device=q.device)
     if n_split > 1 and workspace is None:
-        workspace = decode_workspace(B, H_q, d, n_split, q.device)
-    _check(gqa_attn_decode_paged(q, k_pool, v_pool, block_table, seq_lens, B, P, B_p, max_blocks,
-                                 H_q, H_kv, d, scale, n_split, workspace, out, lse, stream),
-           "gqa_attn_decode_paged")
+        workspace = decode_workspace(B * T_q, H_q, d, n_split, q.device)
+    if multi:
+        _check(gqa_attn_decode_paged_multi(q, k_pool, v_pool, block_table, seq_lens, B, T_q, P,
+                                           B_p, max_blocks, H_q, H_kv, d, scale, n_split,
+                                           workspace, out, lse, stream),
+               "gqa_attn_decode_paged_multi")
+    else:
+        _check(gqa_attn_decode_paged(q, k_pool, v_pool, block_table, seq_lens, B, P, B_p,
+                                     max_blocks, H_q, H_kv, d, scale, n_split, workspace, out, lse,
+                                     stream), "gqa_attn_decode_paged")
     if n_split > 1:
-        _check(gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream),
+        _check(gqa_attn_decode_combine(workspace, B * T_q, H_q, d, n_split, out, lse, stream),
                "gqa_attn_decode_combine")
     return out, lse
 

@@ -296,11 +296,16 @@ gqa_status gqa_attn_decode_fused(const void* q, const void* k_cache, const void*
       gqa::launch_decode_fused(p, tm_k, tm_v, false, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-gqa_status gqa_attn_decode_paged(const void* q, const void* k_pool, const void* v_pool,
-                                 const int32_t* block_table, const int32_t* seq_lens, int B,
-                                 int num_pages, int page_size, int max_blocks, int H_q, int H_kv,
-                                 int d, float scale, int n_split, void* workspace, void* out,
-                                 float* lse, gqa_stream_t stream) {
+gqa_status gqa_attn_decode_paged_multi(const void* q, const void* k_pool, const void* v_pool,
+                                       const int32_t* block_table, const int32_t* seq_lens, int B,
+                                       int T_q, int num_pages, int page_size, int max_blocks,
+                                       int H_q, int H_kv, int d, float scale, int n_split,
+                                       void* workspace, void* out, float* lse,
+                                       gqa_stream_t stream) {
+  if (T_q < 1 || T_q > 16) return GQA_ERR_INVALID_ARG;
+  if (H_kv < 1 || H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
+  if (T_q * (H_q / H_kv) > 16) return GQA_ERR_UNSUPPORTED;  // one mma M tile of rows
+  if ((long long)B * T_q > 65535) return GQA_ERR_INVALID_ARG;
   if (!block_table || !aligned(block_table, 4)) return GQA_ERR_INVALID_ARG;
   if (num_pages < 1 || max_blocks < 1 || page_size < 1) return GQA_ERR_INVALID_ARG;
   if (page_size < 16 || (page_size & (page_size - 1)) != 0) return GQA_ERR_UNSUPPORTED;
@@ -321,7 +326,21 @@ gqa_status gqa_attn_decode_paged(const void* q, const void* k_pool, const void* 
   p.max_blocks = max_blocks;
   p.page_size = page_size;
   p.num_pages = num_pages;
+  p.T_q = T_q;
+  p.ws_O = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                gqa::decode_ws_O_offset(B * T_q, H_q, n_split))
+                     : nullptr;
   return cuda_status(gqa::launch_decode_paged(p, tm_k, tm_v, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_attn_decode_paged(const void* q, const void* k_pool, const void* v_pool,
+                                 const int32_t* block_table, const int32_t* seq_lens, int B,
+                                 int num_pages, int page_size, int max_blocks, int H_q, int H_kv,
+                                 int d, float scale, int n_split, void* workspace, void* out,
+                                 float* lse, gqa_stream_t stream) {
+  return gqa_attn_decode_paged_multi(q, k_pool, v_pool, block_table, seq_lens, B, 1, num_pages,
+                                     page_size, max_blocks, H_q, H_kv, d, scale, n_split,
+                                     workspace, out, lse, stream);
 }
 
 }  // extern "C"

@@ -293,6 +293,16 @@ gqa_status gqa_attn_decode_multi(const void* q, const void* k_cache, const void*
                                  int H_kv, int d, float scale, int n_split, void* workspace,
                                  void* out, float* lse, gqa_stream_t stream);
 
+/* gqa_attn_decode_multi over a paged cache: the cache, block table and page
+ * rules of gqa_attn_decode_paged, the query rows, outputs, workspace and merge
+ * of gqa_attn_decode_multi.  T_q = 1 is gqa_attn_decode_paged. */
+gqa_status gqa_attn_decode_paged_multi(const void* q, const void* k_pool, const void* v_pool,
+                                       const int32_t* block_table, const int32_t* seq_lens, int B,
+                                       int T_q, int num_pages, int page_size, int max_blocks,
+                                       int H_q, int H_kv, int d, float scale, int n_split,
+                                       void* workspace, void* out, float* lse,
+                                       gqa_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Decode with the merge inside thread-block clusters
  * ------------------------------------------------------------------------ */

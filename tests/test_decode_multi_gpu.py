@@ -109,3 +109,41 @@ def test_llama70b_two_token_verification_full_size(oracle_mod):
     out, lse = _multi(q, k, v, sl, None)
     assert_parity(out, lse.transpose(1, 2), ref_o, ref_l, "multi T_q=2 llama70b 32K")
     assert np.isfinite(lse.numpy()).all()
+
+
+def _paginate(k, v, page_size, seed, spare=3):
+    """Scatter a contiguous cache [B, S, H, d] into shuffled pages; unused pages hold NaN."""
+    B, S, H, d = k.shape
+    nb = -(-S // page_size)
+    n_pages = B * nb + spare
+    perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(seed))
+    kp = torch.full((n_pages, page_size, H, d), float("nan"), dtype=k.dtype)
+    vp = torch.full_like(kp, float("nan"))
+    table = torch.zeros(B, nb, dtype=torch.int32)
+    for b in range(B):
+        for j in range(nb):
+            pg = int(perm[b * nb + j])
+            lo, hi = j * page_size, min(S, (j + 1) * page_size)
+            kp[pg, : hi - lo] = k[b, lo:hi]
+            vp[pg, : hi - lo] = v[b, lo:hi]
+            table[b, j] = pg
+    return kp, vp, table
+
+
+@pytest.mark.parametrize("page_size", [16, 64, 256])
+@pytest.mark.parametrize("T_q,G", [(2, 8), (4, 4), (3, 2)])
+def test_paged_multi_matches_oracle_and_contiguous(oracle_mod, page_size, T_q, G):
+    H_kv = 2
+    q, k, v, sl = _inputs(2, T_q, 1000, G * H_kv, H_kv, 128, [1000, 3 * T_q + 37],
+                          seed=page_size + T_q)
+    kp, vp, table = _paginate(k, v, page_size, seed=T_q)
+    ref_o, ref_l = oracle_mod.prefill_chunk_rows(q, k, v, 1 / math.sqrt(128), seq_lens=sl)
+    n = g.paged_default_splits(2, H_kv, table.shape[1] * page_size, 128, page_size)
+    out, lse = g.decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), sl.to(DEV),
+                              n_split=n)
+    torch.cuda.synchronize()
+    assert_parity(out.cpu(), lse.cpu().transpose(1, 2), ref_o, ref_l,
+                  f"paged multi page={page_size} T_q={T_q} G={G}")
+    c_o, c_l = _multi(q, k, v, sl, n)
+    assert torch.equal(out.cpu().view(torch.int16), c_o.view(torch.int16))  # same arithmetic
+    assert torch.equal(lse.cpu(), c_l)
