@@ -364,7 +364,8 @@ def run_ours(args, rank, world, dist):
 
 # ---------------------------------------------------- further workloads ---
 WORKLOADS = ("decode_tiny", "decode_ragged", "decode_paged16", "decode_paged128", "decode_fp8",
-             "decode_fp8_ragged", "decode_multi2", "prefill_64k", "prefill_window", "prefill_chunk")
+             "decode_fp8_ragged", "decode_multi2", "decode_multi4", "decode_multi8", "prefill_64k",
+             "prefill_window", "prefill_chunk")
 
 
 def _shuffled_pages(k, v, page_size, seed):
@@ -442,11 +443,11 @@ def run_workload(name, args):
                 "l2": f"{copies} rotating cache copies" if copies > 1 else "inputs exceed L2",
                 "dtype": "e4m3 cache, bf16 q/out", "data": "synthetic"}
 
-    if name == "decode_multi2":
-        # two query tokens ending a Llama3-70B 32K cache (speculative verification):
+    if name.startswith("decode_multi"):
+        # T_q query tokens ending a Llama3-70B 32K cache (speculative verification):
         # the multi-token decode, and the chunked prefill on the same problem
         cfg = inputs.LLAMA70B_DECODE
-        T_q = 2
+        T_q = int(name[len("decode_multi"):])
         gen = torch.Generator().manual_seed(0)
         q = torch.randn(cfg.B, T_q, cfg.H_q, cfg.d, generator=gen).to(torch.bfloat16)
         k = torch.randn(cfg.B, cfg.S_max, cfg.H_kv, cfg.d, generator=gen).to(torch.bfloat16)
@@ -456,7 +457,8 @@ def run_workload(name, args):
         qd, ld = q.to(dev), lens.to(dev)
         kds = [k.to(dev) for _ in range(3)]
         vds = [v.to(dev) for _ in range(3)]
-        n = g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, cfg.d)
+        n = g.gqa_attn_decode_multi_default_splits(cfg.B, T_q, cfg.H_q, cfg.H_kv, cfg.S_max,
+                                                   cfg.d)
         ws = g.decode_workspace(cfg.B * T_q, cfg.H_q, cfg.d, n, dev)
         out = torch.empty(cfg.B, T_q, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
         lse = torch.empty(cfg.B, T_q, cfg.H_q, dtype=torch.float32, device=dev)
@@ -477,7 +479,8 @@ def run_workload(name, args):
         ms = timed(mstep)
         ms_chunk = timed(cstep)
         gbs = kv_bytes / (ms * 1e-3) / 1e9
-        return {"metric": f"multi-token decode KV GB/s ({cfg.name}, T_q=2)", "value": round(gbs, 2),
+        return {"metric": f"multi-token decode KV GB/s ({cfg.name}, T_q={T_q})",
+                "value": round(gbs, 2),
                 "unit": "GB/s", "ms_per_step": round(ms, 5), "steps": steps, "n_split": n,
                 "kv_bytes": kv_bytes, "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
                 "chunked_prefill_ms_same_problem": round(ms_chunk, 5),

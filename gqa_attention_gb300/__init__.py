@@ -26,6 +26,7 @@ from ._binding import (  # noqa: E402,F401
     gqa_attn_decode_fused,
     gqa_attn_decode_fused_splits,
     gqa_attn_decode_multi,
+    gqa_attn_decode_multi_default_splits,
     gqa_attn_decode_noalloc,
     gqa_attn_decode_paged,
     gqa_attn_decode_paged_fp8,

@@ -36,6 +36,7 @@ SIGNATURES = {
     "gqa_attn_decode_paged_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                        _I, _P, _P, _P, _P]),
     "gqa_attn_decode_multi": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
+    "gqa_attn_decode_multi_default_splits": (_I, [_I, _I, _I, _I, _I, _I]),
     "gqa_attn_decode_paged_multi": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                          _P, _P, _P, _P]),
     "gqa_attn_decode_fused_splits": (_I, [_I, _I, _I, _I]),
@@ -131,6 +132,10 @@ def gqa_attn_decode_multi(q, k_cache, v_cache, seq_lens, B, T_q, S_max, H_q, H_k
     return load().gqa_attn_decode_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B,
                                         T_q, S_max, H_q, H_kv, d, scale, n_split, _ptr(workspace),
                                         _ptr(out), _ptr(lse), _stream(stream))
+
+
+def gqa_attn_decode_multi_default_splits(B, T_q, H_q, H_kv, S_max, d) -> int:
+    return load().gqa_attn_decode_multi_default_splits(B, T_q, H_q, H_kv, S_max, d)
 
 
 def gqa_attn_decode_paged_multi(q, k_pool, v_pool, block_table, seq_lens, B, T_q, num_pages,
@@ -278,7 +283,7 @@ def decode_multi(q, k_cache, v_cache, seq_lens, scale=None, n_split=None, worksp
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if n_split is None:
-        n_split = gqa_attn_decode_default_splits(B, H_kv, S_max, d)
+        n_split = gqa_attn_decode_multi_default_splits(B, T_q, H_q, H_kv, S_max, d)
     if out is None:
         out = torch.empty((B, T_q, H_q, d), dtype=torch.bfloat16, device=q.device)
     if lse is None:

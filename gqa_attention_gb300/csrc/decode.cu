@@ -157,15 +157,20 @@ __global__ void __launch_bounds__(kThreads, 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t smem_base = smem_u32(smem);
 
-  const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
+  // (row groups of one split are neighbours in launch order, so their reads
+  // of the same K/V tiles meet in L2)
+  const int split = CLUSTER ? blockIdx.x : blockIdx.x / p.n_rg;
+  const int rg = CLUSTER ? 0 : blockIdx.x % p.n_rg;
+  const int kv = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
   const int h0 = kv * G;
-  // mma row r (0..15) is query t = r / G of head h0 + r % G; rows past
-  // T_q * G are padding.
-  const int R = p.T_q * G;
+  // mma row r (0..15) of row group rg is row x = 16 rg + r of the KV head:
+  // query t = x / G of head h0 + x % G; rows past T_q * G are padding.
+  const int R = min(16, p.T_q * G - 16 * rg);
   auto out_row = [&](int r) -> size_t {
-    return ((size_t)b * p.T_q + r / G) * p.H_q + h0 + r % G;
+    const int x = 16 * rg + r;
+    return ((size_t)b * p.T_q + x / G) * p.H_q + h0 + x % G;
   };
   // Launched as a programmatic dependent of the previous kernel in the stream:
   // nothing is read or written before that kernel has completed.
@@ -174,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // ---- device-side argument check and empty splits (no pipeline needed) ----
   if (L < p.T_q || L > p.S_max || L < 1) {
-    if (threadIdx.x == 0 && split == 0 && kv == 0) atomicOr(p.err, kErrBadSeqLen);
+    if (threadIdx.x == 0 && split == 0 && kv == 0 && rg == 0) atomicOr(p.err, kErrBadSeqLen);
     for (int e = threadIdx.x; e < R * D; e += kThreads) {
       const int r = e / D, c = e % D;
       const size_t row = out_row(r);
@@ -366,8 +371,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // Key limits of rows g and g + 8 in this split: query t sees keys below
   // L - T_q + 1 + t (the split end t_end for plain decode).
-  const int lim0 = min(t_end, L - p.T_q + 1 + g / G);
-  const int lim1 = min(t_end, L - p.T_q + 1 + (g + 8) / G);
+  const int lim0 = min(t_end, L - p.T_q + 1 + (16 * rg + g) / G);
+  const int lim1 = min(t_end, L - p.T_q + 1 + (16 * rg + g + 8) / G);
   const int lim_lo = min(lim0, lim1);
 
   bool aborted = false;
@@ -768,7 +773,7 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tm_k, const C
   cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem, done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_split, p.H_kv, p.B);
+  cfg.gridDim = dim3(p.n_split * p.n_rg, p.H_kv, p.B);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -787,7 +792,7 @@ cudaError_t launch_split_rows(const DecodeParams& p, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
                               const CUtensorMap& tm_vs, cudaStream_t stream) {
   constexpr int NSTAGE = FP8 ? GQA_DECODE_STAGES_FP8 : (D >= 128 ? GQA_DECODE_STAGES_D128 : 6);
-  if (p.T_q * p.G > 8)  // rows g + 8 are live
+  if (p.T_q * p.G > 8)  // rows g + 8 are live (in the first row group at least)
     return launch_split<D, true, NSTAGE, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
   return launch_split<D, false, NSTAGE, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
 }

@@ -20,9 +20,10 @@ struct DecodeParams {
   int B, S_max, H_q, H_kv, G, d;
   // Query rows per sequence: the last T_q positions L - T_q .. L - 1, query
   // t seeing keys 0 .. L - T_q + t (1 for plain decode).  Row (b, t, h) is
-  // (b * T_q + t) * H_q + h of out [B, T_q, H_q, d], lse and the workspace;
-  // T_q * G <= 16 (the rows of one mma M tile).
-  int T_q;
+  // (b * T_q + t) * H_q + h of out [B, T_q, H_q, d], lse and the workspace.
+  // The T_q * G rows of a KV head come in n_rg groups of 16 (one mma M tile),
+  // each its own CTA: grid x = split * n_rg + group.
+  int T_q, n_rg;
   int n_split, chunk;
   float scale_log2;        // tau * log2(e)
   float2* ws_ml;           // [B, H_q, n_split]  (m in natural-log units, l)

@@ -46,7 +46,8 @@ def _multi(q, k, v, sl, n_split):
 
 
 @pytest.mark.parametrize("d", [32, 64, 128])
-@pytest.mark.parametrize("T_q,G", [(1, 8), (2, 8), (4, 4), (3, 5), (16, 1), (2, 1)])
+@pytest.mark.parametrize("T_q,G", [(1, 8), (2, 8), (4, 4), (3, 5), (16, 1), (2, 1), (4, 8),
+                                   (3, 7), (8, 8), (5, 12), (64, 1)])
 @pytest.mark.parametrize("n_split", [1, 3, None])
 def test_matches_oracle_chunk_rows(oracle_mod, d, T_q, G, n_split):
     H_kv = 2
@@ -91,8 +92,8 @@ def test_rejects_bad_host_arguments():
     x = torch.empty(4096, dtype=torch.bfloat16, device=DEV)
     t = torch.ones(2, dtype=torch.int32, device=DEV)
     f = torch.empty(64, dtype=torch.float32, device=DEV)
-    # T_q * G = 3 * 8 = 24 rows: more than one mma tile
-    assert g.gqa_attn_decode_multi(x, x, x, t, 1, 3, 64, 16, 2, 128, 0.1, 1, None, x, f) == \
+    # T_q * G = 9 * 8 = 72 rows: more than four row groups of 16
+    assert g.gqa_attn_decode_multi(x, x, x, t, 1, 9, 64, 16, 2, 128, 0.1, 1, None, x, f) == \
         g.GQA_ERR_UNSUPPORTED
     assert g.gqa_attn_decode_multi(x, x, x, t, 1, 0, 64, 8, 2, 128, 0.1, 1, None, x, f) == \
         g.GQA_ERR_INVALID_ARG
@@ -102,12 +103,13 @@ def test_rejects_bad_host_arguments():
         g.GQA_ERR_INVALID_ARG  # n_split > 1 without a workspace
 
 
-def test_llama70b_two_token_verification_full_size(oracle_mod):
-    """Two query tokens ending a 32768-token Llama3-70B cache (G = 8: 16 rows)."""
-    q, k, v, sl = _inputs(1, 2, 32768, 64, 8, 128, [32768], seed=11)
+@pytest.mark.parametrize("T_q", [2, 4, 8])
+def test_llama70b_verification_full_size(oracle_mod, T_q):
+    """T_q query tokens ending a 32768-token Llama3-70B cache (G = 8: 8 T_q rows)."""
+    q, k, v, sl = _inputs(1, T_q, 32768, 64, 8, 128, [32768], seed=11 + T_q)
     ref_o, ref_l = oracle_mod.prefill_chunk_rows(q, k, v, 1 / math.sqrt(128), seq_lens=sl)
     out, lse = _multi(q, k, v, sl, None)
-    assert_parity(out, lse.transpose(1, 2), ref_o, ref_l, "multi T_q=2 llama70b 32K")
+    assert_parity(out, lse.transpose(1, 2), ref_o, ref_l, f"multi T_q={T_q} llama70b 32K")
     assert np.isfinite(lse.numpy()).all()
 
 
@@ -131,7 +133,7 @@ def _paginate(k, v, page_size, seed, spare=3):
 
 
 @pytest.mark.parametrize("page_size", [16, 64, 256])
-@pytest.mark.parametrize("T_q,G", [(2, 8), (4, 4), (3, 2)])
+@pytest.mark.parametrize("T_q,G", [(2, 8), (4, 4), (3, 2), (4, 8)])
 def test_paged_multi_matches_oracle_and_contiguous(oracle_mod, page_size, T_q, G):
     H_kv = 2
     q, k, v, sl = _inputs(2, T_q, 1000, G * H_kv, H_kv, 128, [1000, 3 * T_q + 37],
