@@ -27,8 +27,10 @@
  *   affected outputs are written as NaN and the call still returns GQA_OK.
  *   gqa_last_device_error() reports and clears them.
  * - Device pointers must be 16-byte aligned (tensor-memory-access copies).
- * - Thread safety: calls on different streams may run concurrently; the only
- *   shared state is the error word.
+ * - Thread safety: calls on different streams may run concurrently.  Shared
+ *   state: the per-device error word, per-device values computed once and
+ *   then only read (SM count, kernel attributes, cluster support), and the
+ *   scratch array of gqa_attn_decode_noalloc (see there).
  */
 #ifndef GQA_ATTN_H
 #define GQA_ATTN_H
