@@ -420,7 +420,7 @@ def run_workload(name, args):
         copies = 1 if kv_bytes > 512 << 20 else 3
         qd, ld = q.to(dev), lens.to(dev)
         caches = [tuple(x.to(dev) for x in (k8, v8, ks, vs)) for _ in range(copies)]
-        n = 2 * g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, cfg.d)
+        n = 3 * g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, cfg.d)
         ws = g.decode_workspace(cfg.B, cfg.H_q, cfg.d, n, dev)
         out = torch.empty(cfg.B, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
         lse = torch.empty(cfg.B, cfg.H_q, dtype=torch.float32, device=dev)

@@ -376,8 +376,8 @@ def decode_fp8(q, k8, v8, k_scale, v_scale, seq_lens, scale=None, n_split=None, 
         S_max = block_table.shape[1] * B_p
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    if n_split is None:  # the on-chip conversion wants two CTAs per SM
-        n_split = 2 * gqa_attn_decode_default_splits(B, H_kv, S_max, d)
+    if n_split is None:  # the on-chip conversion wants three CTAs per SM
+        n_split = 3 * gqa_attn_decode_default_splits(B, H_kv, S_max, d)
     if out is None:
         out = torch.empty((B, H_q, d), dtype=torch.bfloat16, device=q.device)
     if lse is None:

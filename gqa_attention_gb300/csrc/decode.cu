@@ -11,6 +11,8 @@
 // merged once at the end through shared memory (FA2 K-split, p.9 §5).  A fifth
 // warp only issues TMA copies into a ring of NSTAGE shared-memory stages with
 // full/empty mbarriers (p.10 §3); every wait has a time limit.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -84,6 +86,44 @@ struct Fp8Layout {
   }
 };
 
+// FP8 key placement inside a warp's 16-key slice.  Logical key kappa (the
+// order of the score and P fragments) sits in token row fp8_row(kappa) of the
+// slice: the bit permutation (b3 b2 b1 b0) -> (b1 b3 b2 b0).  With 128-byte
+// rows it puts the 8 rows of one K fragment load (kappa = 2g - (g & 1) + 2nt,
+// g = 0..7) on 8 different swizzle phases, so those loads do not conflict in
+// shared memory.  Any permutation is correct: scores, masks, scales and the
+// V rows all go through the same map.
+__device__ __forceinline__ int fp8_row(int kappa) {
+  return ((kappa & 2) << 2) | ((kappa >> 2) << 1) | (kappa & 1);
+}
+
+// NW consecutive 32-bit words of row `row` of an E4M3 tile (rows of D bytes
+// as TMA writes them, 16-byte chunks swizzled over min(D, 128) bytes) from
+// byte b0 on; b0 is a multiple of 4 * min(NW, 4), so no load straddles a
+// 16-byte chunk.
+template <int D, int NW>
+__device__ __forceinline__ void lds_fp8_words(const uint8_t* tile, int row, int b0,
+                                              uint32_t (&w)[NW]) {
+  constexpr int kSpan = Fp8Layout<D>::kSpan;
+  if constexpr (NW >= 4) {
+#pragma unroll
+    for (int h = 0; h < NW / 4; ++h) {
+      const uint4 v =
+          *reinterpret_cast<const uint4*>(tile + swizzle<kSpan>(row * D + b0 + 16 * h));
+      w[4 * h] = v.x;
+      w[4 * h + 1] = v.y;
+      w[4 * h + 2] = v.z;
+      w[4 * h + 3] = v.w;
+    }
+  } else if constexpr (NW == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(tile + swizzle<kSpan>(row * D + b0));
+    w[0] = v.x;
+    w[1] = v.y;
+  } else {
+    w[0] = *reinterpret_cast<const uint32_t*>(tile + swizzle<kSpan>(row * D + b0));
+  }
+}
+
 // Shared-memory offset of a CTA's partial in the cluster merge: after the
 // four warps' partials (mO, mML) of the final in-CTA merge.
 template <int D>
@@ -135,8 +175,11 @@ __device__ __forceinline__ float online_update(float (&x)[4], float& m, float& l
 // through distributed shared memory (the same associative merge as the
 // combine kernel, p.4 of "Attention Kernel 계보").  No workspace, no second
 // launch.
+// Two CTAs per SM; three for the FP8 cache with G <= 8, whose sweep is bound
+// by its per-tile integer work (E4M3 conversion, byte transposes) rather than
+// by HBM, so it gains from more warps at 128 registers.
 template <int D, bool ROWS16, int NSTAGE, bool PAGED, bool FP8, bool CLUSTER>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
     gqa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v,
                             const __grid_constant__ CUtensorMap tm_ks,
@@ -338,9 +381,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int kk = 0; kk < D / 16; ++kk) {
       // bf16: 32-bit word c holds columns (kk*16 + 2t, +1), word c + 4 holds
       // (kk*16 + 2t + 8, +1).  FP8: the k index of the fragment runs over d in
-      // the order its K fragment is loaded (4 consecutive bytes per lane):
-      // words kk*8 + 2t and kk*8 + 2t + 1 (columns kk*16 + 4t .. + 3).
-      const int c = FP8 ? kk * 8 + 2 * t : kk * 8 + t;
+      // the order its K fragment is loaded: lane t holds bytes (D/4) t ..
+      // (D/4) t + D/4 - 1 of a key row, 4 per k-step, so step kk takes words
+      // (D/8) t + 2 kk and + 1 (columns (D/4) t + 4 kk .. + 3).
+      const int c = FP8 ? (D / 8) * t + 2 * kk : kk * 8 + t;
       const int c2 = FP8 ? c + 1 : c + 4;
       qa[kk][0] = v0 ? q32[rb0 + c] : 0u;
       qa[kk][1] = v1 ? q32[rb1 + c] : 0u;
@@ -357,6 +401,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
 
+  // FP8 with G <= 8 computes P V transposed, O^T = V^T P^T (M = d, N = the
+  // 8 query rows, no padded rows): o[mt] is d-tile mt, only D/16 of them.
+  // Otherwise o[n] is n-tile n of O (M = query rows, N = d).
+  constexpr bool TPV = FP8 && !ROWS16;
   float o[D / 8][4];
 #pragma unroll
   for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -368,6 +416,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int k_chk = (lane >> 3) & 1;
   const int v_row = warp * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
   const int v_chk = lane >> 4;
+  // FP8 (see fp8_row): tile rows of this lane's K fragments (n-tiles 0, 1)
+  // and of its V gathers (logical keys 4t .. 4t + 3).
+  const int k8_row0 = warp * 16 + fp8_row(2 * g - (g & 1));
+  const int k8_row1 = warp * 16 + fp8_row(2 * g - (g & 1) + 2);
+  int v8_row[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) v8_row[e] = warp * 16 + fp8_row(4 * t + e);
 
   // Key limits of rows g and g + 8 in this split: query t sees keys below
   // L - T_q + 1 + t (the split end t_end for plain decode).
@@ -392,14 +447,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     float ksv[4], vsv[4];  // FP8: scales of this thread's 4 score columns
     if constexpr (FP8) {
       // Key order inside a warp's 16-key slice (FP8 only): the lane with
-      // fragment column g of score tile nt holds key 2g - (g & 1) + 2 nt, so
-      // lane (g, t) ends up with the scores of keys 4t .. 4t + 3, which are the
-      // A-fragment k indices 2t, 2t + 1, 2t + 8, 2t + 9 of P V.
+      // fragment column g of score tile nt holds logical key 2g - (g & 1) + 2 nt,
+      // so lane (g, t) ends up with the scores of logical keys 4t .. 4t + 3,
+      // which are the A-fragment k indices 2t, 2t + 1, 2t + 8, 2t + 9 of P V.
+      // Logical key kappa is token row fp8_row(kappa) of the slice.
       const uint8_t* sc_sm = smem + st * kStageBytes;
       const int h = PAGED ? min(p.page_size, kTile) : kTile;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int col = warp * 16 + 4 * t + e;  // key of score column e of this lane
+        const int col = v8_row[e];  // token of score column e of this lane
         const int off = F8::scale_offset(col, h);
         ksv[e] = *reinterpret_cast<const float*>(sc_sm + F8::kOffKs + off);
         vsv[e] = *reinterpret_cast<const float*>(sc_sm + F8::kOffVs + off);
@@ -408,19 +464,22 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // S = Q K^T over this warp's 16 tokens (two n8 tiles).
     float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if constexpr (FP8) {
+      // K fragments straight from the E4M3 rows: lane (g, t) loads bytes
+      // (D/4) t .. + D/4 - 1 of its two key rows; word kk of a row becomes the
+      // two f16 pairs of that row's k-step kk fragment.
+      uint32_t kw[2][D / 16];
+      lds_fp8_words<D, D / 16>(smem + st * kStageBytes, k8_row0, (D / 4) * t, kw[0]);
+      lds_fp8_words<D, D / 16>(smem + st * kStageBytes, k8_row1, (D / 4) * t, kw[1]);
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      if constexpr (FP8) {
-        // K fragment straight from the E4M3 rows: 4 bytes (d = kk*16 + 4t ..)
-        // of key 2g - (g & 1) + 2 nt become the two f16 pairs of the fragment.
+      for (int kk = 0; kk < D / 16; ++kk)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int row = warp * 16 + 2 * g - (g & 1) + 2 * nt;
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(
-              smem + st * kStageBytes + swizzle<F8::kSpan>(row * D + kk * 16 + 4 * t));
-          mma_f16_16816(sacc[nt], qa[kk], e4m3x2_to_f16x2(w), e4m3x2_to_f16x2(w >> 16));
-        }
-      } else {
+        for (int nt = 0; nt < 2; ++nt)
+          mma_f16_16816(sacc[nt], qa[kk], e4m3x2_to_f16x2(kw[nt][kk]),
+                        e4m3x2_to_f16x2(kw[nt][kk] >> 16));
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
         uint32_t b00, b01, b10, b11;
         ldsm_x4(kbase + Lay::offset(k_row, kk * 2 + k_chk), b00, b01, b10, b11);
         mma_bf16_16816(sacc[0], qa[kk], b00, b01);
@@ -435,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        const int tk = FP8 ? tok0 + 4 * t + 2 * nt + c : tok0 + nt * 8 + 2 * t + c;
+        const int tk = FP8 ? tok0 - warp * 16 + v8_row[2 * nt + c] : tok0 + nt * 8 + 2 * t + c;
         const bool ok0 = !partial || tk < lim0, ok1 = !partial || tk < lim1;
         const float sc = FP8 ? ksv[nt * 2 + c] * p.scale_log2 : p.scale_log2;
         x0[nt * 2 + c] = ok0 ? sacc[nt][c] * sc : -INFINITY;
@@ -448,13 +507,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float a0 = online_update(x0, m0, l0, p0);
     float a1 = 1.f;
     if (ROWS16) a1 = online_update(x1, m1, l1, p1);
+    if constexpr (TPV) {
+      // columns 2t, 2t + 1 of O^T are query rows 2t, 2t + 1, whose factors
+      // live in lanes 8t and 8t + 4
+      const float r0 = __shfl_sync(0xffffffffu, a0, 8 * t);
+      const float r1 = __shfl_sync(0xffffffffu, a0, 8 * t + 4);
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      o[n][0] *= a0;
-      o[n][1] *= a0;
-      if (ROWS16) {
-        o[n][2] *= a1;
-        o[n][3] *= a1;
+      for (int mt = 0; mt < D / 16; ++mt) {
+        o[mt][0] *= r0;
+        o[mt][1] *= r1;
+        o[mt][2] *= r0;
+        o[mt][3] *= r1;
+      }
+    } else {
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        o[n][0] *= a0;
+        o[n][1] *= a0;
+        if (ROWS16) {
+          o[n][2] *= a1;
+          o[n][3] *= a1;
+        }
       }
     }
     // P as the A operand of P V (k = this warp's 16 tokens).
@@ -476,33 +549,65 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
     if (partial) {
       // k indices 2t, 2t + 1 (vm0) and 2t + 8, 2t + 9 (vm1): keys tok0 + 2t ..
-      // (FP8 order: keys tok0 + 4t .. 4t + 3)
-      const int tk = FP8 ? tok0 + 4 * t : tok0 + 2 * t;
-      const int tk8 = FP8 ? tk + 2 : tk + 8;
-      vm0 = (tk < t_end ? 0x0000ffffu : 0u) | (tk + 1 < t_end ? 0xffff0000u : 0u);
-      vm1 = (tk8 < t_end ? 0x0000ffffu : 0u) | (tk8 + 1 < t_end ? 0xffff0000u : 0u);
+      // (FP8: logical keys 4t .. 4t + 3, in token rows v8_row[0..3])
+      const int base = tok0 - warp * 16;
+      const int ta = FP8 ? base + v8_row[0] : tok0 + 2 * t, tb = FP8 ? base + v8_row[1] : ta + 1;
+      const int tc = FP8 ? base + v8_row[2] : tok0 + 2 * t + 8, td = FP8 ? base + v8_row[3] : tc + 1;
+      vm0 = (ta < t_end ? 0x0000ffffu : 0u) | (tb < t_end ? 0xffff0000u : 0u);
+      vm1 = (tc < t_end ? 0x0000ffffu : 0u) | (td < t_end ? 0xffff0000u : 0u);
     }
     if constexpr (FP8) {
-      // n-tile 4J + jj, fragment column g is d = 32J + 4g + jj: lane (g, t)
-      // reads d = 32J + 4g .. + 3 of keys 4t .. 4t + 3 (four 4-byte pieces)
-      // and transposes them so that byte e of word jj is key 4t + e at d + jj.
+      // n-tile n = 4J + jj, fragment column g is d = (D/8) g + n: lane (g, t)
+      // loads bytes (D/8) g .. + D/8 - 1 of the rows of logical keys
+      // 4t .. 4t + 3 (word J of each: d = (D/8) g + 4J ..) and transposes the
+      // words J so that byte e of word jj is key 4t + e at d = (D/8) g + 4J + jj.
       const uint8_t* vraw = smem + st * kStageBytes + F8::kOffV8;
+      uint32_t vw[4][D / 32];
 #pragma unroll
-      for (int J = 0; J < D / 32; ++J) {
-        uint32_t w[4];
+      for (int e = 0; e < 4; ++e) lds_fp8_words<D, D / 32>(vraw, v8_row[e], (D / 8) * g, vw[e]);
+      // Masking costs two ANDs per mma, so only the tile holding the split end
+      // pays for it.
+      auto pv = [&](auto masked) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          w[e] = *reinterpret_cast<const uint32_t*>(
-              vraw + swizzle<F8::kSpan>((warp * 16 + 4 * t + e) * D + 32 * J + 4 * g));
-        const uint32_t lo01 = __byte_perm(w[0], w[1], 0x5140), hi01 = __byte_perm(w[0], w[1], 0x7362);
-        const uint32_t lo23 = __byte_perm(w[2], w[3], 0x5140), hi23 = __byte_perm(w[2], w[3], 0x7362);
-        const uint32_t x[4] = {__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo01, lo23, 0x7632),
-                               __byte_perm(hi01, hi23, 0x5410), __byte_perm(hi01, hi23, 0x7632)};
+        for (int J = 0; J < D / 32; ++J) {
+          const uint32_t lo01 = __byte_perm(vw[0][J], vw[1][J], 0x5140),
+                         hi01 = __byte_perm(vw[0][J], vw[1][J], 0x7362);
+          const uint32_t lo23 = __byte_perm(vw[2][J], vw[3][J], 0x5140),
+                         hi23 = __byte_perm(vw[2][J], vw[3][J], 0x7362);
+          const uint32_t x[4] = {__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo01, lo23, 0x7632),
+                                 __byte_perm(hi01, hi23, 0x5410), __byte_perm(hi01, hi23, 0x7632)};
+          if constexpr (TPV) {
+            // d-tile mt = 2J + u: its rows g, g + 8 are d = (D/8) g + 4J + 2u
+            // and + 1, i.e. words x[2u], x[2u + 1]; P^T is pa[0], pa[2]
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-          mma_f16_16816(o[4 * J + jj], pa, e4m3x2_to_f16x2(x[jj]) & vm0,
-                        e4m3x2_to_f16x2(x[jj] >> 16) & vm1);
-      }
+            for (int u = 0; u < 2; ++u) {
+              uint32_t a[4] = {e4m3x2_to_f16x2(x[2 * u]), e4m3x2_to_f16x2(x[2 * u + 1]),
+                               e4m3x2_to_f16x2(x[2 * u] >> 16), e4m3x2_to_f16x2(x[2 * u + 1] >> 16)};
+              if constexpr (decltype(masked)::value) {
+                a[0] &= vm0;
+                a[1] &= vm0;
+                a[2] &= vm1;
+                a[3] &= vm1;
+              }
+              mma_f16_16816(o[2 * J + u], a, pa[0], pa[2]);
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              uint32_t b0 = e4m3x2_to_f16x2(x[jj]), b1 = e4m3x2_to_f16x2(x[jj] >> 16);
+              if constexpr (decltype(masked)::value) {
+                b0 &= vm0;
+                b1 &= vm1;
+              }
+              mma_f16_16816(o[4 * J + jj], pa, b0, b1);
+            }
+          }
+        }
+      };
+      if (partial)
+        pv(std::true_type{});
+      else
+        pv(std::false_type{});
     } else {
 #pragma unroll
       for (int jj = 0; jj < D / 16; ++jj) {
@@ -527,15 +632,24 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* mO = reinterpret_cast<float*>(smem);  // [warps][16][D]
   float2* mML = reinterpret_cast<float2*>(smem + kConsumerWarps * 16 * D * 4);  // [warps][16]
   if (!failed) {
+    if constexpr (TPV) {  // O^T d-tile mt = 2J + u: rows g, g + 8 are d = (D/8) g + 4J + 2u, + 1
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      if constexpr (FP8) {  // fragment column c of n-tile 4J + jj is d = 32J + 4c + jj
-        const int col = (n >> 2) * 32 + 8 * t + (n & 3);
+      for (int mt = 0; mt < D / 16; ++mt) {
+        const int d0 = (D / 8) * g + 4 * (mt >> 1) + 2 * (mt & 1);
+        *reinterpret_cast<float2*>(&mO[(warp * 16 + 2 * t) * D + d0]) = make_float2(o[mt][0], o[mt][2]);
+        *reinterpret_cast<float2*>(&mO[(warp * 16 + 2 * t + 1) * D + d0]) =
+            make_float2(o[mt][1], o[mt][3]);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < (TPV ? 0 : D / 8); ++n) {
+      if constexpr (FP8) {  // fragment column c of n-tile n is d = (D/8) c + n
+        const int col = (D / 4) * t + n;
         mO[(warp * 16 + g) * D + col] = o[n][0];
-        mO[(warp * 16 + g) * D + col + 4] = o[n][1];
+        mO[(warp * 16 + g) * D + col + D / 8] = o[n][1];
         if (ROWS16) {
           mO[(warp * 16 + g + 8) * D + col] = o[n][2];
-          mO[(warp * 16 + g + 8) * D + col + 4] = o[n][3];
+          mO[(warp * 16 + g + 8) * D + col + D / 8] = o[n][3];
         }
       } else {
         const int col = n * 8 + 2 * t;
