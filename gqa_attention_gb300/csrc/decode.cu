@@ -41,6 +41,7 @@ namespace {
 constexpr int kTile = kDecodeTile;  // tokens per stage
 constexpr int kMaxClusterSplits = 16;
 constexpr int kConsumerWarps = 4;   // 16 tokens each
+constexpr int kPrefetchTiles = 6;   // tiles a split CTA may warm in L2 before its dependency wait
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
 template <int D>
@@ -216,7 +217,38 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
     return ((size_t)b * p.T_q + x / G) * p.H_q + h0 + x % G;
   };
   // Launched as a programmatic dependent of the previous kernel in the stream:
-  // nothing is read or written before that kernel has completed.
+  // nothing is read or written before that kernel has completed.  While it
+  // finishes, the producer lane of each split's first row group prefetches the
+  // split's first K/V tiles into L2 (contiguous cache only: the page table is
+  // an input).  The prefetch extent comes from a relaxed load of seq_lens[b],
+  // which may see the value from before the previous kernel's writes; it sizes
+  // the prefetch only.  A prefetch hands no data to the kernel and L2 is where
+  // writes become coherent, so it cannot expose stale values; at worst it
+  // fetches rows the split will not use.
+  if constexpr (!PAGED) {
+    if (p.prefetch_tiles > 0 && threadIdx.x == kConsumerWarps * 32 && rg == 0) {
+      int L_hint;
+      asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(L_hint) : "l"(p.seq_lens + b));
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      const int tp0 = split * p.chunk;
+      const int tp_end = min(min(p.S_max, L_hint), tp0 + p.chunk);
+      for (int i = 0; i < p.prefetch_tiles && tp0 + i * kTile < tp_end; ++i) {
+        const int tok = tp0 + i * kTile, row = b * p.S_max + tok;
+        if constexpr (FP8) {
+          tma_prefetch_l2_3d(&tm_k, 0, kv, row);
+          tma_prefetch_l2_3d(&tm_v, 0, kv, row);
+          tma_prefetch_l2_2d(&tm_ks, tok, b);
+          tma_prefetch_l2_2d(&tm_vs, tok, b);
+        } else {
+          for (int blk = 0; blk < Lay::kBlocks; ++blk) {
+            tma_prefetch_l2_3d(&tm_k, blk * Lay::kBox, kv, row);
+            tma_prefetch_l2_3d(&tm_v, blk * Lay::kBox, kv, row);
+          }
+        }
+      }
+    }
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int L = p.seq_lens[b];
 
@@ -247,8 +279,6 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
   const int t_end = min(t0 + p.chunk, L);
   const int n_tiles = t_end > t0 ? (t_end - t0 + kTile - 1) / kTile : 0;
 
-  // Let a dependent combine launch get scheduled now; it waits for this grid.
-  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
@@ -356,6 +386,11 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
         }
         issued = i + 1;
       }
+      // Let the next kernel in the stream be scheduled once this CTA has
+      // issued its last copy.  A following combine waits for this grid anyway;
+      // a following split prefetches its first tiles into L2, which pays only
+      // this late (earlier, this grid's own stream evicts them before use).
+      asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
       // No copy may still target this CTA's shared memory when it exits.
       for (int i = max(0, issued - NSTAGE); i < issued; ++i)
         mbar_wait(smem_u32(&full_bar[i % NSTAGE]), (i / NSTAGE) & 1, p.wait_ns, p.err);
@@ -878,14 +913,44 @@ inline cudaError_t set_smem_attr_once(const void* kern, int smem, unsigned char*
   return e;
 }
 
+// CTAs of `kern` (160 threads, `smem` bytes) the current device holds at once,
+// looked up once per device.
+inline cudaError_t resident_ctas(const void* kern, int smem, int* cache, int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+    *out = cache[dev];
+    return cudaSuccess;
+  }
+  int per_sm = 0, sms = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  *out = per_sm * sms;
+  if (dev >= 0 && dev < 64) cache[dev] = *out;  // benign race: idempotent
+  return cudaSuccess;
+}
+
 template <int D, bool ROWS16, int NSTAGE, bool PAGED, bool FP8>
-cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                         const CUtensorMap& tm_ks, const CUtensorMap& tm_vs, cudaStream_t stream) {
+cudaError_t launch_split(const DecodeParams& p_in, const CUtensorMap& tm_k,
+                         const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
+                         const CUtensorMap& tm_vs, cudaStream_t stream) {
   constexpr int smem = decode_smem_bytes<D, NSTAGE, FP8>();
   auto kern = gqa_decode_split_kernel<D, ROWS16, NSTAGE, PAGED, FP8, false>;
   static unsigned char done[64];
+  static int resident[64];
   cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem, done);
   if (e != cudaSuccess) return e;
+  int fit = 0;
+  e = resident_ctas(reinterpret_cast<const void*>(kern), smem, resident, &fit);
+  if (e != cudaSuccess) return e;
+  DecodeParams p = p_in;
+  // The L2 prefetch pays only when every CTA is resident while the previous
+  // kernel drains; a CTA of a later wave would prefetch what it loads next.
+  const long long ctas = (long long)p.n_split * p.n_rg * p.H_kv * p.B;
+  p.prefetch_tiles = (!PAGED && ctas <= fit) ? kPrefetchTiles : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_split * p.n_rg, p.H_kv, p.B);
   cfg.blockDim = dim3(kThreads);

@@ -36,6 +36,10 @@ struct DecodeParams {
   // of the pools, page = block_table[b * max_blocks + t / page_size]
   const int32_t* block_table;
   int max_blocks, page_size, num_pages;
+  // Set by the launcher: K/V tiles each split CTA prefetches into L2 before
+  // its dependency wait (0 = none; used only when the whole grid is resident
+  // at once, so that the prefetch overlaps the previous kernel).
+  int prefetch_tiles;
 };
 
 constexpr int kMaxPagesPerCta = 512;  // page indices a paged decode CTA stages in shared memory

@@ -106,8 +106,9 @@ int gqa_attn_decode_default_splits(int B, int H_kv, int S_max, int d);
  *   lse       device fp32 [B, H_q]        LSE = m + ln l
  * Keys past seq_lens[b] are never used: their cache rows may hold anything.
  * The kernel is launched as a programmatic dependent of the preceding kernel in
- * the stream: it may be scheduled early but reads and writes nothing before
- * that kernel has completed. */
+ * the stream: it may be scheduled early and then only prefetches the first K/V
+ * tiles of each split into L2 (no data reaches the kernel); it reads and
+ * writes nothing before that kernel has completed. */
 gqa_status gqa_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                            const int32_t* seq_lens, int B, int S_max, int H_q, int H_kv, int d,
                            float scale, int n_split, void* workspace, void* out, float* lse,
