@@ -218,29 +218,47 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
   };
   // Launched as a programmatic dependent of the previous kernel in the stream:
   // nothing is read or written before that kernel has completed.  While it
-  // finishes, the producer lane of each split's first row group prefetches the
-  // split's first K/V tiles into L2 (contiguous cache only: the page table is
-  // an input).  The prefetch extent comes from a relaxed load of seq_lens[b],
-  // which may see the value from before the previous kernel's writes; it sizes
-  // the prefetch only.  A prefetch hands no data to the kernel and L2 is where
-  // writes become coherent, so it cannot expose stale values; at worst it
-  // fetches rows the split will not use.
-  if constexpr (!PAGED) {
-    if (p.prefetch_tiles > 0 && threadIdx.x == kConsumerWarps * 32 && rg == 0) {
-      int L_hint;
-      asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(L_hint) : "l"(p.seq_lens + b));
+  // finishes, the producer warp of each split's first row group prefetches the
+  // split's first K/V tiles into L2, one (tile, page segment) per lane.  The
+  // extent comes from relaxed loads of seq_lens[b] and, for a paged cache, of
+  // the page indices; they may see values from before the previous kernel's
+  // writes and only aim the prefetch (an index outside the pool is skipped).
+  // A prefetch hands no data to the kernel and L2 is where writes become
+  // coherent, so it cannot expose stale values; at worst it fetches rows the
+  // split will not use.
+  if (p.prefetch_tiles > 0 && warp == kConsumerWarps && rg == 0) {
+    int L_hint;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(L_hint) : "l"(p.seq_lens + b));
+    if (lane == 0) {
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
-      const int tp0 = split * p.chunk;
-      const int tp_end = min(min(p.S_max, L_hint), tp0 + p.chunk);
-      for (int i = 0; i < p.prefetch_tiles && tp0 + i * kTile < tp_end; ++i) {
-        const int tok = tp0 + i * kTile, row = b * p.S_max + tok;
+    }
+    const int h = PAGED ? min(p.page_size, kTile) : kTile;  // rows per box
+    const int subs = kTile / h;
+    const int i = lane / subs, sub = lane % subs;
+    const int tk = split * p.chunk + i * kTile + sub * h;
+    const int tp_end = min(min(p.S_max, L_hint), split * p.chunk + p.chunk);
+    if (i < p.prefetch_tiles && tk < tp_end) {
+      int row = b * p.S_max + tk, sc_x = tk, sc_y = b;
+      bool ok = true;
+      if constexpr (PAGED) {
+        int pg;
+        asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];"
+                     : "=r"(pg)
+                     : "l"(p.block_table + (size_t)b * p.max_blocks + tk / p.page_size));
+        ok = pg >= 0 && pg < p.num_pages;
+        row = pg * p.page_size + tk % p.page_size;
+        sc_x = tk % p.page_size;
+        sc_y = pg;
+      }
+      if (ok) {
         if constexpr (FP8) {
           tma_prefetch_l2_3d(&tm_k, 0, kv, row);
           tma_prefetch_l2_3d(&tm_v, 0, kv, row);
-          tma_prefetch_l2_2d(&tm_ks, tok, b);
-          tma_prefetch_l2_2d(&tm_vs, tok, b);
+          tma_prefetch_l2_2d(&tm_ks, sc_x, sc_y);
+          tma_prefetch_l2_2d(&tm_vs, sc_x, sc_y);
         } else {
+#pragma unroll
           for (int blk = 0; blk < Lay::kBlocks; ++blk) {
             tma_prefetch_l2_3d(&tm_k, blk * Lay::kBox, kv, row);
             tma_prefetch_l2_3d(&tm_v, blk * Lay::kBox, kv, row);
@@ -950,7 +968,7 @@ cudaError_t launch_split(const DecodeParams& p_in, const CUtensorMap& tm_k,
   // The L2 prefetch pays only when every CTA is resident while the previous
   // kernel drains; a CTA of a later wave would prefetch what it loads next.
   const long long ctas = (long long)p.n_split * p.n_rg * p.H_kv * p.B;
-  p.prefetch_tiles = (!PAGED && ctas <= fit) ? kPrefetchTiles : 0;
+  p.prefetch_tiles = ctas <= fit ? kPrefetchTiles : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_split * p.n_rg, p.H_kv, p.B);
   cfg.blockDim = dim3(kThreads);
