@@ -364,8 +364,8 @@ def run_ours(args, rank, world, dist):
 
 # ---------------------------------------------------- further workloads ---
 WORKLOADS = ("decode_tiny", "decode_ragged", "decode_paged16", "decode_paged128", "decode_fp8",
-             "decode_fp8_ragged", "decode_multi2", "decode_multi4", "decode_multi8", "prefill_64k",
-             "prefill_window", "prefill_chunk")
+             "decode_fp8_ragged", "decode_multi2", "decode_multi4", "decode_multi8", "decode_multi16",
+             "prefill_64k", "prefill_window", "prefill_chunk")
 
 
 def _shuffled_pages(k, v, page_size, seed):

@@ -102,8 +102,11 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 bool head_dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
 
 // Query rows (T_q x G) a multi-token decode folds per KV head: four row groups
-// of 16, each its own CTA.
+// of 16, each its own CTA; with d = 128, up to 128 rows in one tensor-core
+// tile (used above 16 rows).
 constexpr int kMaxMultiRows = 64;
+constexpr int kMaxMultiRowsTc = 128;
+bool multi_uses_tc(int T_q, int G, int d) { return d == 128 && T_q * G > 16; }
 
 }  // namespace
 
@@ -238,6 +241,8 @@ int gqa_attn_decode_multi_default_splits(int B, int T_q, int H_q, int H_kv, int 
   const int n = gqa_attn_decode_default_splits(B, H_kv, S_max, d);
   const long long groups = (T_q * (long long)(H_q / H_kv) + 15) / 16;
   if (groups <= 1) return n;
+  // The tensor-core kernel: one CTA per SM, K/V read once per split.
+  if (multi_uses_tc(T_q, H_q / H_kv, d)) return n;
   // Several row groups: keep every CTA of a split resident at once (two per
   // SM), so the groups' reads of the same K/V tiles meet in L2 (measured for
   // Llama3-70B at 32K: 19 / 12 / 9 splits best for 2 / 3 / 4 groups).
@@ -251,14 +256,35 @@ gqa_status gqa_attn_decode_multi(const void* q, const void* k_cache, const void*
                                  void* out, float* lse, gqa_stream_t stream) {
   if (T_q < 1 || T_q > 64 || T_q > S_max) return GQA_ERR_INVALID_ARG;
   if (H_kv < 1 || H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
-  if (T_q * (H_q / H_kv) > kMaxMultiRows) return GQA_ERR_UNSUPPORTED;
+  const bool tc = multi_uses_tc(T_q, H_q / H_kv, d);
+  if (T_q * (H_q / H_kv) > (tc ? kMaxMultiRowsTc : kMaxMultiRows)) return GQA_ERR_UNSUPPORTED;
   if ((long long)B * T_q > 65535) return GQA_ERR_INVALID_ARG;
   CUtensorMap tm_k, tm_v;
   gqa::DecodeParams p;
   gqa_status st = prepare_decode(q, k_cache, v_cache, seq_lens, B, S_max, (long long)B * S_max,
-                                 gqa::kDecodeTile, H_q, H_kv, d, scale, n_split, workspace, out,
-                                 lse, &tm_k, &tm_v, &p);
+                                 tc ? 128 : gqa::kDecodeTile, H_q, H_kv, d, scale, n_split,
+                                 workspace, out, lse, &tm_k, &tm_v, &p);
   if (st != GQA_OK) return st;
+  if (tc) {
+    // All T_q * G rows of a KV head in one tile: Q as [B * T_q][H_q][d], one
+    // box of G heads x T_q queries per d half; 128-key splits.
+    CUtensorMap tm_q;
+    const uint64_t qdims[3] = {(uint64_t)d, (uint64_t)H_q, (uint64_t)B * T_q};
+    const uint64_t qstrides[2] = {(uint64_t)d * 2, (uint64_t)H_q * d * 2};
+    const uint32_t qbox[3] = {64u, (uint32_t)(H_q / H_kv), (uint32_t)T_q};
+    if ((st = encode_bf16(&tm_q, q, 3, qdims, qstrides, qbox, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+        GQA_OK)
+      return st;
+    p.T_q = T_q;
+    p.n_rg = 1;
+    const long long per = ((long long)S_max + n_split - 1) / n_split;
+    p.chunk = (int)((per + 127) / 128 * 128);
+    p.ws_O = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                  gqa::decode_ws_O_offset(B * T_q, H_q, n_split))
+                       : nullptr;
+    return cuda_status(
+        gqa::launch_decode_tc(p, tm_q, tm_k, tm_v, reinterpret_cast<cudaStream_t>(stream)));
+  }
   p.T_q = T_q;
   p.n_rg = (T_q * p.G + 15) / 16;
   if ((long long)n_split * p.n_rg > 0x7fffffffLL) return GQA_ERR_INVALID_ARG;

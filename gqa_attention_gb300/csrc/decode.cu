@@ -816,13 +816,16 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
 // not change the result beyond rounding.  The kernel may start before the
 // decode kernel ends (programmatic dependent launch); it reads nothing before
 // griddepcontrol.wait.
+// CHUNK = splits per warp per round of loads: 16, or 8 when every warp folds
+// at most 8 splits, which halves the registers so that twice as many CTAs
+// (rows) are resident at once.
 constexpr int kCombineThreads = 128;
 constexpr int kCombineWarps = kCombineThreads / 32;
-constexpr int kCombineChunk = 16;  // splits per warp per round of loads
 
-template <int D>
-__global__ void __launch_bounds__(kCombineThreads)
+template <int D, int CHUNK>
+__global__ void __launch_bounds__(kCombineThreads, CHUNK == 8 ? 7 : 4)
     gqa_decode_combine_kernel(const CombineParams p) {
+  constexpr int kCombineChunk = CHUNK;
   constexpr int VEC = D / 32;  // columns per lane
   __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
   __shared__ int s_bad[kCombineWarps];
@@ -1049,7 +1052,7 @@ cudaError_t launch_fused(const DecodeParams& p, const CUtensorMap& tm_k, const C
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, int CHUNK>
 cudaError_t launch_comb(const CombineParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.H_q, p.B);
@@ -1061,7 +1064,7 @@ cudaError_t launch_comb(const CombineParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = GQA_COMBINE_PDL ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gqa_decode_combine_kernel<D>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gqa_decode_combine_kernel<D, CHUNK>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1104,10 +1107,11 @@ cudaError_t launch_decode_fused(const DecodeParams& p, const CUtensorMap& tm_k,
 }
 
 cudaError_t launch_decode_combine(const CombineParams& p, cudaStream_t stream) {
+  const bool small = p.n_split <= kCombineWarps * 8;  // one round of 8 per warp
   switch (p.d) {
-    case 32: return launch_comb<32>(p, stream);
-    case 64: return launch_comb<64>(p, stream);
-    case 128: return launch_comb<128>(p, stream);
+    case 32: return small ? launch_comb<32, 8>(p, stream) : launch_comb<32, 16>(p, stream);
+    case 64: return small ? launch_comb<64, 8>(p, stream) : launch_comb<64, 16>(p, stream);
+    case 128: return small ? launch_comb<128, 8>(p, stream) : launch_comb<128, 16>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

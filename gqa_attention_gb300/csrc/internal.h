@@ -85,6 +85,13 @@ cudaError_t launch_decode_combine(const CombineParams& p, cudaStream_t stream);
 // can be resident on the current device.
 cudaError_t launch_decode_fused(const DecodeParams& p, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, bool probe, cudaStream_t stream);
+// Multi-token decode with all T_q * G (<= 128) rows of a KV head in one
+// tcgen05.mma tile: d = 128, 128-key tiles (p.chunk a multiple of 128), Q
+// through `tm_q` (q viewed as [B * T_q][H_q][d], box {64, G, T_q}), K/V boxes
+// of 128 rows.  Same partial layout as launch_decode_split.
+cudaError_t launch_decode_tc(const DecodeParams& p, const CUtensorMap& tm_q,
+                             const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                             cudaStream_t stream);
 cudaError_t launch_decode_paged(const DecodeParams& p, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, cudaStream_t stream);
 // E4M3 cache with per-token scales; paged when p.block_table is set.

@@ -283,10 +283,13 @@ gqa_status gqa_attn_prefill_chunk_split(const void* q, const void* k_cache, cons
  * 0 .. L - T_q + t of the cache (causal, aligned to the end of the sequence:
  * "Attention Kernel 계보" p.13 §1 with the chunk offset of ADR-0060 §5.4).
  * The T_q * G query rows of one KV head are folded into the M dimension of
- * the split-KV decode, in groups of 16 rows (one mma tile), one CTA per group
- * and split (so T_q * G <= 64 and T_q <= 64; GQA_ERR_UNSUPPORTED for more rows,
- * GQA_ERR_INVALID_ARG for T_q outside 1..64; larger chunks go to
- * gqa_attn_prefill_chunk).  q and out are bf16 [B, T_q, H_q, d],
+ * the split-KV decode.  Up to 16 rows, and for d = 32 or 64 up to 64 rows in
+ * groups of 16 (one mma.sync tile each, one CTA per group and split).  With
+ * d = 128 and more than 16 rows, all rows (up to 128) form one tensor-core
+ * tile, with one CTA per split reading each K/V tile once; its splits cover
+ * 128-key multiples (ceil(S_max / n_split) rounded up to 128).
+ * GQA_ERR_UNSUPPORTED for more rows, GQA_ERR_INVALID_ARG for T_q outside 1..64;
+ * larger chunks go to gqa_attn_prefill_chunk.  q and out are bf16 [B, T_q, H_q, d],
  * lse fp32 [B, T_q, H_q] (natural log); the cache layout, splits and errors
  * are those of gqa_attn_decode, with the device check 1 <= T_q <= L <= S_max.
  * With n_split > 1 the partials go to `workspace`
@@ -299,9 +302,10 @@ gqa_status gqa_attn_decode_multi(const void* q, const void* k_cache, const void*
                                  void* out, float* lse, gqa_stream_t stream);
 
 /* Split count for gqa_attn_decode_multi on the current device: that of
- * gqa_attn_decode_default_splits when the T_q * G rows fit one group of 16;
- * with more groups, at most the count that keeps all groups of all splits
- * resident at once (two CTAs per SM).  Returns >= 1. */
+ * gqa_attn_decode_default_splits when the T_q * G rows fit one group of 16 or
+ * go to the tensor-core tile (d = 128); with more mma.sync groups, at most the
+ * count that keeps all groups of all splits resident at once (two CTAs per
+ * SM).  Returns >= 1. */
 int gqa_attn_decode_multi_default_splits(int B, int T_q, int H_q, int H_kv, int S_max, int d);
 
 /* gqa_attn_decode_multi over a paged cache: the cache, block table and page

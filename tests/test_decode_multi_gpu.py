@@ -1,6 +1,8 @@
 """GPU parity of the multi-token decode (the last T_q positions of each sequence,
 causal among themselves) against the fp64 oracle's chunk rows, and against the
-chunked prefill path.  Cache rows past each sequence length hold NaN."""
+chunked prefill path.  Cache rows past each sequence length hold NaN.  With
+d = 128 and more than 16 query rows per KV head the tensor-core kernel runs;
+otherwise the mma.sync row groups do."""
 import math
 
 import numpy as np
@@ -89,11 +91,15 @@ def test_length_shorter_than_t_q_gives_nan_and_error_word():
 
 
 def test_rejects_bad_host_arguments():
+    # every call below fails a host check before any launch
     x = torch.empty(4096, dtype=torch.bfloat16, device=DEV)
     t = torch.ones(2, dtype=torch.int32, device=DEV)
     f = torch.empty(64, dtype=torch.float32, device=DEV)
-    # T_q * G = 9 * 8 = 72 rows: more than four row groups of 16
-    assert g.gqa_attn_decode_multi(x, x, x, t, 1, 9, 64, 16, 2, 128, 0.1, 1, None, x, f) == \
+    # d = 64, T_q * G = 9 * 8 = 72 rows: more than four row groups of 16
+    assert g.gqa_attn_decode_multi(x, x, x, t, 1, 9, 64, 16, 2, 64, 0.1, 1, None, x, f) == \
+        g.GQA_ERR_UNSUPPORTED
+    # d = 128, T_q * G = 17 * 8 = 136 rows: more than one tensor-core tile
+    assert g.gqa_attn_decode_multi(x, x, x, t, 1, 17, 64, 16, 2, 128, 0.1, 1, None, x, f) == \
         g.GQA_ERR_UNSUPPORTED
     assert g.gqa_attn_decode_multi(x, x, x, t, 1, 0, 64, 8, 2, 128, 0.1, 1, None, x, f) == \
         g.GQA_ERR_INVALID_ARG
@@ -103,7 +109,54 @@ def test_rejects_bad_host_arguments():
         g.GQA_ERR_INVALID_ARG  # n_split > 1 without a workspace
 
 
-@pytest.mark.parametrize("T_q", [2, 4, 8])
+@pytest.mark.parametrize("T_q,G,H_kv", [(9, 8, 2), (16, 8, 2), (32, 4, 2), (64, 2, 1), (2, 16, 2),
+                                        (6, 3, 3), (40, 3, 1)])
+@pytest.mark.parametrize("n_split", [1, 4, None])
+def test_tensor_core_rows_match_oracle(oracle_mod, T_q, G, H_kv, n_split):
+    """d = 128 with 17..128 query rows per KV head (one tensor-core tile): a
+    sequence of exactly T_q tokens, a long one and one ending just past a
+    128-key tile; cache rows past each length hold NaN."""
+    lens = [T_q, 1000, 128 + T_q]
+    q, k, v, sl = _inputs(3, T_q, 1000, G * H_kv, H_kv, 128, lens, seed=T_q * 31 + G)
+    ref_o, ref_l = oracle_mod.prefill_chunk_rows(q, k, v, 1 / math.sqrt(128), seq_lens=sl)
+    out, lse = _multi(q, k, v, sl, n_split)
+    assert_parity(out, lse.transpose(1, 2), ref_o, ref_l, f"tc T_q={T_q} G={G} n_split={n_split}")
+
+
+def test_tensor_core_rows_match_chunked_prefill():
+    q, k, v, sl = _inputs(2, 8, 3000, 64, 8, 128, [3000, 1234], seed=9)
+    m_o, m_l = _multi(q, k, v, sl, None)
+    c_o, c_l = g.prefill_chunk(q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV))
+    torch.cuda.synchronize()
+    assert (m_o.float() - c_o.cpu().float()).abs().max().item() <= 2 ** -7
+    assert (m_l.transpose(1, 2) - c_l.cpu()).abs().max().item() <= 2e-5
+
+
+def test_tensor_core_length_shorter_than_t_q_gives_nan_and_error_word():
+    q, k, v, sl = _inputs(2, 4, 512, 16, 2, 128, [512, 3], seed=4)  # 32 rows; 3 < T_q
+    for n_split in (1, 3):
+        out, lse = _multi(q, k, v, sl, n_split)
+        assert g.gqa_last_device_error() == g.GQA_ERR_INVALID_ARG
+        assert torch.isnan(out[1].float()).all() and torch.isnan(lse[1]).all()
+        assert torch.isfinite(out[0].float()).all() and torch.isfinite(lse[0]).all()
+
+
+def test_tensor_core_outputs_stay_inside_their_buffers():
+    B, T_q, H_q, H_kv, d = 2, 8, 16, 2, 128
+    q, k, v, sl = _inputs(B, T_q, 700, H_q, H_kv, d, [700, 9], seed=5)
+    pad = 4096
+    n = B * T_q * H_q
+    out_buf = torch.full((n * d + 2 * pad,), 7.0, dtype=torch.bfloat16, device=DEV)
+    lse_buf = torch.full((n + 2 * pad,), 7.0, dtype=torch.float32, device=DEV)
+    out = out_buf[pad: pad + n * d].view(B, T_q, H_q, d)
+    lse = lse_buf[pad: pad + n].view(B, T_q, H_q)
+    g.decode_multi(q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV), n_split=3, out=out, lse=lse)
+    torch.cuda.synchronize()
+    for buf, m in ((out_buf, n * d), (lse_buf, n)):
+        assert (buf[:pad].float() == 7.0).all() and (buf[pad + m:].float() == 7.0).all()
+
+
+@pytest.mark.parametrize("T_q", [2, 4, 8, 16])
 def test_llama70b_verification_full_size(oracle_mod, T_q):
     """T_q query tokens ending a 32768-token Llama3-70B cache (G = 8: 8 T_q rows)."""
     q, k, v, sl = _inputs(1, T_q, 32768, 64, 8, 128, [32768], seed=11 + T_q)
@@ -147,5 +200,9 @@ def test_paged_multi_matches_oracle_and_contiguous(oracle_mod, page_size, T_q, G
     assert_parity(out.cpu(), lse.cpu().transpose(1, 2), ref_o, ref_l,
                   f"paged multi page={page_size} T_q={T_q} G={G}")
     c_o, c_l = _multi(q, k, v, sl, n)
-    assert torch.equal(out.cpu().view(torch.int16), c_o.view(torch.int16))  # same arithmetic
-    assert torch.equal(lse.cpu(), c_l)
+    if T_q * G <= 16:  # both run the same mma.sync arithmetic
+        assert torch.equal(out.cpu().view(torch.int16), c_o.view(torch.int16))
+        assert torch.equal(lse.cpu(), c_l)
+    else:  # the contiguous cache runs the tensor-core kernel: rounding only
+        assert (out.cpu().float() - c_o.float()).abs().max().item() <= 2 ** -7
+        assert (lse.cpu() - c_l).abs().max().item() <= 2e-5
