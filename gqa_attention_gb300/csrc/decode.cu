@@ -851,8 +851,23 @@ __global__ void __launch_bounds__(kCombineThreads, CHUNK == 8 ? 7 : 4)
       const int s = base + kCombineWarps * c;
       const bool in = s < p.n_split;
       mlv[c] = in ? ml[s] : make_float2(-INFINITY, 0.f);
-#pragma unroll
-      for (int v = 0; v < VEC; ++v) ov[c][v] = in ? O[(size_t)s * D + v] : 0.f;
+      // this lane's VEC columns in one load: the workspace is 256-byte
+      // aligned and a row of D floats is a multiple of 16 bytes
+      if constexpr (VEC == 4) {
+        const float4 w = in ? *reinterpret_cast<const float4*>(O + (size_t)s * D)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        ov[c][0] = w.x;
+        ov[c][1] = w.y;
+        ov[c][2] = w.z;
+        ov[c][3] = w.w;
+      } else if constexpr (VEC == 2) {
+        const float2 w = in ? *reinterpret_cast<const float2*>(O + (size_t)s * D)
+                            : make_float2(0.f, 0.f);
+        ov[c][0] = w.x;
+        ov[c][1] = w.y;
+      } else {
+        ov[c][0] = in ? O[(size_t)s * D] : 0.f;
+      }
     }
     float cm = -INFINITY;
 #pragma unroll
