@@ -92,6 +92,21 @@ def test_decode_rejects_bad_arguments(lib, kw, status):
     assert st == status
 
 
+def test_multi_token_row_limits_and_splits(lib):
+    # d = 128 takes up to 128 rows per KV head (one tensor-core tile), d = 32/64
+    # up to 64 (four mma.sync row groups); both fail before any launch
+    assert g.gqa_attn_decode_multi(FAKE, FAKE, FAKE, FAKE, 1, 17, 64, 16, 2, 128, 0.1, 1, None,
+                                   FAKE, FAKE, stream=0) == g.GQA_ERR_UNSUPPORTED  # 136 rows
+    assert g.gqa_attn_decode_multi(FAKE, FAKE, FAKE, FAKE, 1, 9, 64, 16, 2, 64, 0.1, 1, None,
+                                   FAKE, FAKE, stream=0) == g.GQA_ERR_UNSUPPORTED  # 72 rows, d = 64
+    assert g.gqa_attn_decode_multi(FAKE, FAKE, FAKE, FAKE, 1, 65, 128, 2, 2, 128, 0.1, 1, None,
+                                   FAKE, FAKE, stream=0) == g.GQA_ERR_INVALID_ARG  # T_q > 64
+    # the tensor-core tile runs one CTA per SM: the plain decode's split count
+    for B, T_q, H_q, H_kv, S in [(1, 8, 64, 8, 32768), (1, 16, 64, 8, 32768), (2, 3, 64, 8, 5000)]:
+        assert g.gqa_attn_decode_multi_default_splits(B, T_q, H_q, H_kv, S, 128) == \
+            g.gqa_attn_decode_default_splits(B, H_kv, S, 128)
+
+
 def test_combine_and_prefill_reject_bad_arguments(lib):
     assert g.gqa_attn_decode_combine(None, 1, 8, 128, 2, FAKE, FAKE, stream=0) == g.GQA_ERR_INVALID_ARG
     assert g.gqa_attn_decode_combine(FAKE, 1, 8, 96, 2, FAKE, FAKE, stream=0) == g.GQA_ERR_UNSUPPORTED
