@@ -365,7 +365,8 @@ def run_ours(args, rank, world, dist):
 # ---------------------------------------------------- further workloads ---
 WORKLOADS = ("decode_tiny", "decode_ragged", "decode_paged16", "decode_paged128", "decode_fp8",
              "decode_fp8_ragged", "decode_multi2", "decode_multi4", "decode_multi8", "decode_multi16",
-             "prefill_64k", "prefill_window", "prefill_chunk")
+             "decode_paged16_multi8", "decode_paged128_multi8", "prefill_64k", "prefill_window",
+             "prefill_chunk")
 
 
 def _shuffled_pages(k, v, page_size, seed):
@@ -485,6 +486,43 @@ def run_workload(name, args):
                 "kv_bytes": kv_bytes, "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
                 "chunked_prefill_ms_same_problem": round(ms_chunk, 5),
                 "l2": "3 rotating K/V copies", "dtype": "bf16", "data": "synthetic"}
+
+    if name.startswith("decode_paged") and "_multi" in name:
+        # T_q query tokens ending a Llama3-70B 32K cache held in shuffled pages
+        cfg = inputs.LLAMA70B_DECODE
+        page = int(name[len("decode_paged"):name.index("_multi")])
+        T_q = int(name[name.index("_multi") + len("_multi"):])
+        gen = torch.Generator().manual_seed(0)
+        q = torch.randn(cfg.B, T_q, cfg.H_q, cfg.d, generator=gen).to(torch.bfloat16)
+        k = torch.randn(cfg.B, cfg.S_max, cfg.H_kv, cfg.d, generator=gen).to(torch.bfloat16)
+        v = torch.randn(cfg.B, cfg.S_max, cfg.H_kv, cfg.d, generator=gen).to(torch.bfloat16)
+        lens = torch.full((cfg.B,), cfg.S_max, dtype=torch.int32)
+        kv_bytes = 2 * int(lens.sum()) * cfg.H_kv * cfg.d * 2
+        kp, vp, table = _shuffled_pages(k, v, page, seed=0)
+        qd, ld, td = q.to(dev), lens.to(dev), table.to(dev)
+        kps = [kp.to(dev) for _ in range(3)]
+        vps = [vp.to(dev) for _ in range(3)]
+        n = g.gqa_attn_decode_multi_default_splits(cfg.B, T_q, cfg.H_q, cfg.H_kv, cfg.S_max,
+                                                   cfg.d)
+        ws = g.decode_workspace(cfg.B * T_q, cfg.H_q, cfg.d, n, dev)
+        out = torch.empty(cfg.B, T_q, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(cfg.B, T_q, cfg.H_q, dtype=torch.float32, device=dev)
+
+        def pmstep(i):
+            assert g.gqa_attn_decode_paged_multi(qd, kps[i % 3], vps[i % 3], td, ld, cfg.B, T_q,
+                                                 kp.shape[0], page, table.shape[1], cfg.H_q,
+                                                 cfg.H_kv, cfg.d, cfg.scale, n, ws, out, lse,
+                                                 stream) == g.GQA_OK
+            assert g.gqa_attn_decode_combine(ws, cfg.B * T_q, cfg.H_q, cfg.d, n, out, lse,
+                                             stream) == g.GQA_OK
+
+        ms = timed(pmstep)
+        gbs = kv_bytes / (ms * 1e-3) / 1e9
+        return {"metric": f"paged multi-token decode KV GB/s ({cfg.name}, page {page}, T_q={T_q})",
+                "value": round(gbs, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
+                "steps": steps, "n_split": n, "kv_bytes": kv_bytes,
+                "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
+                "l2": "3 rotating page pools", "dtype": "bf16", "data": "synthetic"}
 
     if name.startswith("decode_paged"):
         cfg = inputs.LLAMA70B_DECODE

@@ -349,7 +349,8 @@ gqa_status gqa_attn_decode_paged_multi(const void* q, const void* k_pool, const 
                                        gqa_stream_t stream) {
   if (T_q < 1 || T_q > 64) return GQA_ERR_INVALID_ARG;
   if (H_kv < 1 || H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
-  if (T_q * (H_q / H_kv) > kMaxMultiRows) return GQA_ERR_UNSUPPORTED;
+  const bool tc = multi_uses_tc(T_q, H_q / H_kv, d);
+  if (T_q * (H_q / H_kv) > (tc ? kMaxMultiRowsTc : kMaxMultiRows)) return GQA_ERR_UNSUPPORTED;
   if ((long long)B * T_q > 65535) return GQA_ERR_INVALID_ARG;
   if (!block_table || !aligned(block_table, 4)) return GQA_ERR_INVALID_ARG;
   if (num_pages < 1 || max_blocks < 1 || page_size < 1) return GQA_ERR_INVALID_ARG;
@@ -357,6 +358,35 @@ gqa_status gqa_attn_decode_paged_multi(const void* q, const void* k_pool, const 
   const long long S_max = (long long)max_blocks * page_size;
   const long long rows = (long long)num_pages * page_size;
   if (S_max > 0x7fffffffLL || rows > 0x7ffffffeLL) return GQA_ERR_INVALID_ARG;
+  if (tc) {
+    // All T_q * G rows of a KV head in one tensor-core tile; each 128-key tile
+    // arrives as boxes of min(page_size, 128) rows, one page each.
+    CUtensorMap tm_k, tm_v, tm_q;
+    gqa::DecodeParams p;
+    gqa_status st = prepare_decode(q, k_pool, v_pool, seq_lens, B, (int)S_max, rows,
+                                   page_size < 128 ? page_size : 128, H_q, H_kv, d, scale,
+                                   n_split, workspace, out, lse, &tm_k, &tm_v, &p);
+    if (st != GQA_OK) return st;
+    const uint64_t qdims[3] = {(uint64_t)d, (uint64_t)H_q, (uint64_t)B * T_q};
+    const uint64_t qstrides[2] = {(uint64_t)d * 2, (uint64_t)H_q * d * 2};
+    const uint32_t qbox[3] = {64u, (uint32_t)(H_q / H_kv), (uint32_t)T_q};
+    if ((st = encode_bf16(&tm_q, q, 3, qdims, qstrides, qbox, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+        GQA_OK)
+      return st;
+    p.block_table = block_table;
+    p.max_blocks = max_blocks;
+    p.page_size = page_size;
+    p.num_pages = num_pages;
+    p.T_q = T_q;
+    p.n_rg = 1;
+    const long long per = (S_max + n_split - 1) / n_split;
+    p.chunk = (int)((per + 127) / 128 * 128);
+    p.ws_O = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                  gqa::decode_ws_O_offset(B * T_q, H_q, n_split))
+                       : nullptr;
+    return cuda_status(
+        gqa::launch_decode_tc(p, tm_q, tm_k, tm_v, reinterpret_cast<cudaStream_t>(stream)));
+  }
   if (n_split >= 1) {
     const int chunk = gqa_attn_decode_split_chunk((int)S_max, n_split);
     if (chunk / page_size + 2 > gqa::kMaxPagesPerCta) return GQA_ERR_UNSUPPORTED;

@@ -35,6 +35,11 @@
 //
 // O is rescaled only when a row's running maximum grows by more than 2^8
 // (base 2), as in prefill.cu: l and O share one reference, so O / l holds.
+//
+// PAGED = true: the cache is a pool of fixed-size pages reached through a
+// block table (p.17 §2-§4, p.18 §5); each 128-key tile arrives as boxes of
+// min(page_size, 128) rows, one page each.  A page index outside the pool is
+// reported and replaced by page 0, and the CTA's outputs become NaN.
 #include "tcgen05.cuh"
 
 namespace gqa {
@@ -52,6 +57,7 @@ constexpr uint32_t kTcSmem = kOffV + kTcSlots * kTileB + 1024;
 constexpr uint32_t kColO = 256;                 // O after S_0, S_1
 constexpr float kRescaleLog2 = 8.f;
 
+template <bool PAGED>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gqa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -63,6 +69,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ __align__(8) uint64_t s_full[2], p_ready[2], pv_done;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  __shared__ int bad_page;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -91,6 +98,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(smem_u32(&pv_done), 1);
     abort_flag = 0;
+    bad_page = 0;
     fence_barrier_init();
   }
   // Q rows past T_q * G are zero (their S, P and O rows are never stored, but
@@ -111,7 +119,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // relaxed load of seq_lens[b], which may see the value from before the
   // previous kernel's writes and only sizes the prefetch; a prefetch hands no
   // data to the kernel and L2 is where writes become coherent.
-  if (warp == 0 && lane < p.prefetch_tiles) {
+  if (!PAGED && warp == 0 && lane < p.prefetch_tiles) {
     int L_hint;
     asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(L_hint) : "l"(p.seq_lens + b));
     const int tk = split * p.chunk + lane * kTcKeys;
@@ -173,40 +181,87 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0) {
     // ----------------------------------------------------------- TMA producer --
+    // The whole warp runs the loop (so that the page indices of a tile are
+    // read in parallel, one per lane); lane 0 arms each barrier before any
+    // copy of its tile is issued.
+    const uint32_t qb = smem_u32(&q_full);
     if (lane == 0) {
       tma_prefetch_map(&tm_q);
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
-      const uint32_t qb = smem_u32(&q_full);
       mbar_arrive_expect_tx(qb, static_cast<uint32_t>(rows) * 256u);
       for (int dh = 0; dh < 2; ++dh)
         tma_load_3d(sb + kOffQ + dh * kHalfB, &tm_q, qb, dh * 64, kv * G, b * p.T_q);
-      // K_0, then K_{j+1} and V_j: the order in which the tensor core reads
-      // them.  A tile's slot is refilled once the MMA that read it completed.
-      int k_issued = 0, v_issued = 0;
-      auto load = [&](bool is_k, int j) -> bool {
-        const int slot = j % kTcSlots;
-        uint64_t* empty = is_k ? &k_empty[slot] : &v_empty[slot];
-        if (j >= kTcSlots && !wait(empty, ((j / kTcSlots) - 1) & 1)) return false;
-        const uint32_t fb = smem_u32(is_k ? &k_full[slot] : &v_full[slot]);
-        mbar_arrive_expect_tx(fb, kTileB);
-        const uint32_t dst = sb + (is_k ? kOffK : kOffV) + slot * kTileB;
-        const int row = b * p.S_max + t0 + j * kTcKeys;
-        for (int dh = 0; dh < 2; ++dh)
-          tma_load_3d(dst + dh * kHalfB, is_k ? &tm_k : &tm_v, fb, dh * 64, kv, row);
-        return true;
-      };
-      bool ok = load(true, 0);
-      if (ok) k_issued = 1;
-      for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n) {
-          ok = load(true, j + 1);
-          if (!ok) break;
-          k_issued = j + 2;
+    }
+    // K_0, then K_{j+1} and V_j: the order in which the tensor core reads
+    // them.  A tile's slot is refilled once the MMA that read it completed.
+    int k_issued = 0, v_issued = 0;
+    // Paged: boxes of h rows, one page each (h = page_size up to 128), box i
+    // of a tile issued by lane i.  Each tile's page indices are read once,
+    // two tiles ahead, so the reads are in flight while the producer waits for
+    // a slot; K_j and V_j use the same boxes.  A box wholly past the split end
+    // reads rows past the pool, which TMA fills with zeros, so that every tile
+    // still receives its full bytes.
+    const int h = PAGED ? min(p.page_size, kTcKeys) : kTcKeys;
+    const int nb = kTcKeys / h;  // <= 8 (page_size >= 16)
+    struct Box {
+      int pg;
+      bool has;
+    };
+    auto fetch = [&](int j) -> Box {  // this lane's page of tile j
+      Box x;
+      const int tok = t0 + j * kTcKeys + lane * h;
+      x.has = PAGED && lane < nb && j < n && tok < t_end;
+      x.pg = x.has ? p.block_table[(size_t)b * p.max_blocks + tok / p.page_size] : 0;
+      return x;
+    };
+    auto issue = [&](bool is_k, int j, Box x) -> bool {
+      const int slot = j % kTcSlots;
+      uint64_t* empty = is_k ? &k_empty[slot] : &v_empty[slot];
+      if (j >= kTcSlots && !wait_all(empty, ((j / kTcSlots) - 1) & 1)) return false;
+      const uint32_t fb = smem_u32(is_k ? &k_full[slot] : &v_full[slot]);
+      const uint32_t dst = sb + (is_k ? kOffK : kOffV) + slot * kTileB;
+      const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+      const int tok0 = t0 + j * kTcKeys;
+      if constexpr (!PAGED) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, kTileB);
+          for (int dh = 0; dh < 2; ++dh)
+            tma_load_3d(dst + dh * kHalfB, map, fb, dh * 64, kv, b * p.S_max + tok0);
         }
-        ok = load(false, j);
-        if (ok) v_issued = j + 1;
+      } else {
+        const bool bad = x.has && (x.pg < 0 || x.pg >= p.num_pages);
+        const int row = x.has ? (bad ? 0 : x.pg) * p.page_size + (tok0 + lane * h) % p.page_size
+                              : p.num_pages * p.page_size;
+        // a bad index is recorded before lane 0's arrive releases it
+        if (__any_sync(0xffffffffu, bad) && lane == 0) {
+          if (!*reinterpret_cast<volatile int*>(&bad_page)) atomicOr(p.err, kErrBadPage);
+          *reinterpret_cast<volatile int*>(&bad_page) = 1;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(fb, kTileB);
+        __syncwarp();
+        if (lane < nb)
+          for (int dh = 0; dh < 2; ++dh)
+            tma_load_3d(dst + dh * kHalfB + lane * h * 128, map, fb, dh * 64, kv, row);
       }
+      return true;
+    };
+    Box box_j = fetch(0), box_j1 = fetch(1);  // tiles j and j + 1
+    bool ok = issue(true, 0, box_j);
+    if (ok) k_issued = 1;
+    for (int j = 0; ok && j < n; ++j) {
+      const Box box_j2 = fetch(j + 2);
+      if (j + 1 < n) {
+        ok = issue(true, j + 1, box_j1);
+        if (!ok) break;
+        k_issued = j + 2;
+      }
+      ok = issue(false, j, box_j);
+      if (ok) v_issued = j + 1;
+      box_j = box_j1;
+      box_j1 = box_j2;
+    }
+    if (lane == 0) {
       // The next kernel in the stream may be scheduled now; it waits for this
       // grid before it reads anything.
       asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -217,6 +272,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_wait(smem_u32(&v_full[j % kTcSlots]), (j / kTcSlots) & 1, p.wait_ns, p.err);
       mbar_wait(qb, 0, p.wait_ns, p.err);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer --
     constexpr uint32_t idS = instr_desc_bf16_f32(128, 128, false);
@@ -403,7 +459,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 
     // Epilogue: the last P V, then O / l and LSE, or this split's partial.
-    if (alive && wait_all(&pv_done, (n - 1) & 1)) {
+    // Paged: a bad page index (recorded before the producer's arrive on the
+    // last V tile, which this wait acquires) makes the outputs NaN.
+    bool page_ok = true;
+    if (PAGED && alive) {
+      if (wait_all(&v_full[(n - 1) % kTcSlots], ((n - 1) / kTcSlots) & 1))
+        page_ok = *reinterpret_cast<volatile int*>(&bad_page) == 0;
+      else
+        alive = false;
+    }
+    if (alive && page_ok && wait_all(&pv_done, (n - 1) & 1)) {
       tc_fence_after();
       const bool store = r < rows;
       const size_t row = store ? out_row(r) : 0;
@@ -442,7 +507,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         else  // m in natural-log units; a row with no visible key: (-inf, 0)
           p.ws_ml[row * p.n_split + split] = make_float2(m_ref * kLn2, l);
       }
-    } else if (r < rows) {  // a wait gave up: this row's outputs are NaN
+    } else if (r < rows) {  // a wait gave up, or a bad page: this row's outputs are NaN
       const size_t row = out_row(r);
       if (p.n_split == 1) {
         for (int c = 0; c < 128; ++c) p.out[row * 128 + c] = __float2bfloat16(NAN);
@@ -474,8 +539,11 @@ cudaError_t launch_decode_tc(const DecodeParams& p_in, const CUtensorMap& tm_q,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    e = cudaFuncSetAttribute(gqa_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kTcSmem);
+    e = cudaFuncSetAttribute(gqa_decode_tc_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gqa_decode_tc_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     if (e != cudaSuccess) return e;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -490,7 +558,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p_in, const CUtensorMap& tm_q,
   // while the previous kernel drains.
   const long long ctas = (long long)p.n_split * p.H_kv * p.B;
   const int sms = (dev >= 0 && dev < 64) ? sm_count[dev] : 0;
-  p.prefetch_tiles = ctas <= sms ? kTcSlots : 0;
+  p.prefetch_tiles = (!p.block_table && ctas <= sms) ? kTcSlots : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_split, p.H_kv, p.B);
   cfg.blockDim = dim3(kTcThreads);
@@ -501,7 +569,8 @@ cudaError_t launch_decode_tc(const DecodeParams& p_in, const CUtensorMap& tm_q,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gqa_decode_tc_kernel, tm_q, tm_k, tm_v, p);
+  e = p.block_table ? cudaLaunchKernelEx(&cfg, gqa_decode_tc_kernel<true>, tm_q, tm_k, tm_v, p)
+                    : cudaLaunchKernelEx(&cfg, gqa_decode_tc_kernel<false>, tm_q, tm_k, tm_v, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -310,7 +310,9 @@ int gqa_attn_decode_multi_default_splits(int B, int T_q, int H_q, int H_kv, int 
 
 /* gqa_attn_decode_multi over a paged cache: the cache, block table and page
  * rules of gqa_attn_decode_paged, the query rows, outputs, workspace and merge
- * of gqa_attn_decode_multi.  T_q = 1 is gqa_attn_decode_paged. */
+ * of gqa_attn_decode_multi (including the tensor-core tile for more than 16
+ * rows at d = 128, whose splits cover 128-key multiples and which needs no
+ * page-count limit per split).  T_q = 1 is gqa_attn_decode_paged. */
 gqa_status gqa_attn_decode_paged_multi(const void* q, const void* k_pool, const void* v_pool,
                                        const int32_t* block_table, const int32_t* seq_lens, int B,
                                        int T_q, int num_pages, int page_size, int max_blocks,

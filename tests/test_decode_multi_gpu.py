@@ -206,3 +206,37 @@ def test_paged_multi_matches_oracle_and_contiguous(oracle_mod, page_size, T_q, G
     else:  # the contiguous cache runs the tensor-core kernel: rounding only
         assert (out.cpu().float() - c_o.float()).abs().max().item() <= 2 ** -7
         assert (lse.cpu() - c_l).abs().max().item() <= 2e-5
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 128, 256])
+@pytest.mark.parametrize("T_q,G", [(8, 8), (16, 8), (5, 4)])
+def test_paged_tensor_core_rows_match_oracle_and_contiguous(oracle_mod, page_size, T_q, G):
+    """d = 128 with more than 16 rows per KV head over a paged cache: each
+    128-key tile arrives as one box per page; unused pages hold NaN."""
+    H_kv = 2
+    q, k, v, sl = _inputs(2, T_q, 1500, G * H_kv, H_kv, 128, [1500, 2 * T_q + 129],
+                          seed=page_size + 3 * T_q)
+    kp, vp, table = _paginate(k, v, page_size, seed=T_q + 1)
+    ref_o, ref_l = oracle_mod.prefill_chunk_rows(q, k, v, 1 / math.sqrt(128), seq_lens=sl)
+    for n_split in (1, 5):
+        out, lse = g.decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), sl.to(DEV),
+                                  n_split=n_split)
+        torch.cuda.synchronize()
+        assert_parity(out.cpu(), lse.cpu().transpose(1, 2), ref_o, ref_l,
+                      f"paged tc page={page_size} T_q={T_q} G={G} n_split={n_split}")
+        c_o, c_l = _multi(q, k, v, sl, n_split)  # the same tiles, contiguous
+        assert torch.equal(out.cpu().view(torch.int16), c_o.view(torch.int16))
+        assert torch.equal(lse.cpu(), c_l)
+
+
+def test_paged_tensor_core_bad_table_entry_gives_nan_and_error_word():
+    q, k, v, sl = _inputs(2, 8, 512, 16, 2, 128, [512, 512], seed=8)  # 64 rows per KV head
+    kp, vp, table = _paginate(k, v, 64, seed=2)
+    table[1, 3] = kp.shape[0] + 5  # outside the pool
+    out, lse = g.decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), sl.to(DEV),
+                              n_split=2)
+    torch.cuda.synchronize()
+    assert g.gqa_last_device_error() == g.GQA_ERR_INVALID_ARG
+    assert torch.isnan(out[1].float()).all() and torch.isnan(lse[1]).all()
+    assert torch.isfinite(out[0].float()).all() and torch.isfinite(lse[0]).all()
+
