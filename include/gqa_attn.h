@@ -35,8 +35,8 @@
  * Which call for which workload (measured on GB300, Llama3-70B heads, 32K cache)
  * -------------------------------------------------------------------------
  * - One new token per sequence, contiguous cache: gqa_attn_decode with
- *   gqa_attn_decode_default_splits, then gqa_attn_decode_combine (25.5 us per
- *   step; the split kernel streams K/V at 88% of the measured HBM rate).
+ *   gqa_attn_decode_default_splits, then gqa_attn_decode_combine (25.1 us per
+ *   step; the split kernel streams K/V at 92% of the measured HBM rate).
  * - The same over a paged cache: gqa_attn_decode_paged (+ combine).
  * - An E4M3 cache with per-token scales: gqa_attn_decode_fp8 /
  *   gqa_attn_decode_paged_fp8 (+ combine) with 3x the default split count.
