@@ -341,72 +341,86 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
         tma_prefetch_map(&tm_ks);
         tma_prefetch_map(&tm_vs);
       }
-      int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int st = i % NSTAGE;
+    }
+    // The whole warp runs the tile loop: lane 0 takes the slot and arms its
+    // barrier, then the copies are issued, by lane 0 for a contiguous cache
+    // and by lane `sub` for page segment `sub` of a paged one (so that the
+    // boxes of small pages are issued in parallel).
+    int issued = 0;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int st = i % NSTAGE;
+      bool go = true;
+      if (lane == 0) {
         if (i >= NSTAGE &&
             !mbar_wait(smem_u32(&empty_bar[st]), ((i / NSTAGE) - 1) & 1, p.wait_ns, p.err)) {
           *reinterpret_cast<volatile int*>(&abort_flag) = 1;
-          break;
+          go = false;
         }
-        if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
-        const uint32_t fb = smem_u32(&full_bar[st]);
-        mbar_arrive_expect_tx(fb, kTxBytes);
-        const uint32_t dst_k = smem_base + st * kStageBytes;
-        const uint32_t dst_v = dst_k + Lay::kTileBytes;
-        if constexpr (FP8) {
-          // E4M3 rows (D bytes) and the per-token scales; page segments of
-          // h rows when paged.  Rows past the end read as zeros (TMA fill).
-          const int h = PAGED ? min(p.page_size, kTile) : kTile;
-          for (int sub = 0; sub < kTile / h; ++sub) {
-            const int tok = t0 + i * kTile + sub * h;
-            int row, sc_x, sc_y;
-            if (!PAGED) {
-              row = b * p.S_max + tok;
-              sc_x = tok;
-              sc_y = b;
-            } else if (tok < t_end) {
-              const int pg = pages_sm[tok / p.page_size - page0];
-              row = pg * p.page_size + tok % p.page_size;
-              sc_x = tok % p.page_size;
-              sc_y = pg;
-            } else {
-              row = p.num_pages * p.page_size;
-              sc_x = 0;
-              sc_y = p.num_pages;
-            }
-            tma_load_3d(dst_k + sub * h * D, &tm_k, fb, 0, kv, row);
-            tma_load_3d(dst_k + F8::kOffV8 + sub * h * D, &tm_v, fb, 0, kv, row);
-            tma_load_2d(dst_k + F8::kOffKs + sub * F8::slot_bytes(h), &tm_ks, fb, sc_x, sc_y);
-            tma_load_2d(dst_k + F8::kOffVs + sub * F8::slot_bytes(h), &tm_vs, fb, sc_x, sc_y);
+        if (go && *reinterpret_cast<volatile int*>(&abort_flag)) go = false;
+        if (go) mbar_arrive_expect_tx(smem_u32(&full_bar[st]), kTxBytes);
+      }
+      if (!__shfl_sync(0xffffffffu, go, 0)) break;  // (the barrier is armed before any copy)
+      const uint32_t fb = smem_u32(&full_bar[st]);
+      const uint32_t dst_k = smem_base + st * kStageBytes;
+      const uint32_t dst_v = dst_k + Lay::kTileBytes;
+      if constexpr (FP8) {
+        // E4M3 rows (D bytes) and the per-token scales; page segments of
+        // h rows when paged.  Rows past the end read as zeros (TMA fill).
+        const int h = PAGED ? min(p.page_size, kTile) : kTile;
+        const int sub = lane;
+        if (sub < kTile / h) {
+          const int tok = t0 + i * kTile + sub * h;
+          int row, sc_x, sc_y;
+          if (!PAGED) {
+            row = b * p.S_max + tok;
+            sc_x = tok;
+            sc_y = b;
+          } else if (tok < t_end) {
+            const int pg = pages_sm[tok / p.page_size - page0];
+            row = pg * p.page_size + tok % p.page_size;
+            sc_x = tok % p.page_size;
+            sc_y = pg;
+          } else {
+            row = p.num_pages * p.page_size;
+            sc_x = 0;
+            sc_y = p.num_pages;
           }
-        } else if (!PAGED) {
+          tma_load_3d(dst_k + sub * h * D, &tm_k, fb, 0, kv, row);
+          tma_load_3d(dst_k + F8::kOffV8 + sub * h * D, &tm_v, fb, 0, kv, row);
+          tma_load_2d(dst_k + F8::kOffKs + sub * F8::slot_bytes(h), &tm_ks, fb, sc_x, sc_y);
+          tma_load_2d(dst_k + F8::kOffVs + sub * F8::slot_bytes(h), &tm_vs, fb, sc_x, sc_y);
+        }
+      } else if (!PAGED) {
+        if (lane == 0) {
           const int row = b * p.S_max + t0 + i * kTile;
 #pragma unroll
           for (int blk = 0; blk < Lay::kBlocks; ++blk) {
             tma_load_3d(dst_k + blk * Lay::kBlockBytes, &tm_k, fb, blk * Lay::kBox, kv, row);
             tma_load_3d(dst_v + blk * Lay::kBlockBytes, &tm_v, fb, blk * Lay::kBox, kv, row);
           }
-        } else {
-          // Boxes of h = min(page_size, 64) rows; a box wholly past the split
-          // end reads rows past the pool (TMA fills them with zeros) so that
-          // every stage still receives its full byte count.
-          const int h = min(p.page_size, kTile);
-          for (int sub = 0; sub < kTile / h; ++sub) {
-            const int tok = t0 + i * kTile + sub * h;
-            const int row = tok < t_end ? pages_sm[tok / p.page_size - page0] * p.page_size +
-                                              tok % p.page_size
-                                        : p.num_pages * p.page_size;
-            const uint32_t off = sub * h * Lay::kSpan;
+        }
+      } else {
+        // Boxes of h = min(page_size, 64) rows; a box wholly past the split
+        // end reads rows past the pool (TMA fills them with zeros) so that
+        // every stage still receives its full byte count.
+        const int h = min(p.page_size, kTile);
+        const int sub = lane;
+        if (sub < kTile / h) {
+          const int tok = t0 + i * kTile + sub * h;
+          const int row = tok < t_end ? pages_sm[tok / p.page_size - page0] * p.page_size +
+                                            tok % p.page_size
+                                      : p.num_pages * p.page_size;
+          const uint32_t off = sub * h * Lay::kSpan;
 #pragma unroll
-            for (int blk = 0; blk < Lay::kBlocks; ++blk) {
-              tma_load_3d(dst_k + blk * Lay::kBlockBytes + off, &tm_k, fb, blk * Lay::kBox, kv, row);
-              tma_load_3d(dst_v + blk * Lay::kBlockBytes + off, &tm_v, fb, blk * Lay::kBox, kv, row);
-            }
+          for (int blk = 0; blk < Lay::kBlocks; ++blk) {
+            tma_load_3d(dst_k + blk * Lay::kBlockBytes + off, &tm_k, fb, blk * Lay::kBox, kv, row);
+            tma_load_3d(dst_v + blk * Lay::kBlockBytes + off, &tm_v, fb, blk * Lay::kBox, kv, row);
           }
         }
-        issued = i + 1;
       }
+      issued = i + 1;
+    }
+    if (lane == 0) {
       // Let the next kernel in the stream be scheduled once this CTA has
       // issued its last copy.  A following combine waits for this grid anyway;
       // a following split prefetches its first tiles into L2, which pays only
@@ -416,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
       for (int i = max(0, issued - NSTAGE); i < issued; ++i)
         mbar_wait(smem_u32(&full_bar[i % NSTAGE]), (i / NSTAGE) & 1, p.wait_ns, p.err);
     }
+    __syncwarp();
     if constexpr (CLUSTER) {  // the consumers' two cluster barriers
       __syncwarp();
       cluster_sync();
