@@ -96,3 +96,16 @@ def test_fp8_llama70b_decode_full_size(oracle_mod):
     torch.cuda.synchronize()
     assert_parity(out, lse, ref_o, ref_l, "fp8 llama70b")
     assert np.isfinite(lse.cpu().numpy()).all()
+
+
+def test_fp8_deterministic_across_runs():
+    """Same input, same split count: bit-identical O and LSE (fixed merge order)."""
+    q, k8, v8, ks, vs, lens = inputs.decode_inputs_fp8(2, 64, 8, 128, 5000, seed=21,
+                                                       seq_lens=[5000, 1234])
+    runs = []
+    for _ in range(2):
+        out, lse = g.decode_fp8(*_dev(q, k8, v8, ks, vs, lens))
+        torch.cuda.synchronize()
+        runs.append((out.cpu(), lse.cpu()))
+    assert torch.equal(runs[0][0].view(torch.int16), runs[1][0].view(torch.int16))
+    assert torch.equal(runs[0][1], runs[1][1])

@@ -240,3 +240,11 @@ def test_paged_tensor_core_bad_table_entry_gives_nan_and_error_word():
     assert torch.isnan(out[1].float()).all() and torch.isnan(lse[1]).all()
     assert torch.isfinite(out[0].float()).all() and torch.isfinite(lse[0]).all()
 
+
+@pytest.mark.parametrize("T_q", [2, 8])  # mma.sync row group, tensor-core tile
+def test_deterministic_across_runs(T_q):
+    q, k, v, sl = _inputs(2, T_q, 3000, 64, 8, 128, [3000, 1500], seed=23 + T_q)
+    a = _multi(q, k, v, sl, None)
+    b = _multi(q, k, v, sl, None)
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    assert torch.equal(a[1], b[1])

@@ -122,3 +122,15 @@ def test_paged_llama70b_decode_full_size(oracle_mod, page_size):
     ref_o, ref_l = oracle_mod.decode(q, k, v, lens, cfg.scale)
     assert_parity(out, lse, ref_o, ref_l, f"paged {page_size} llama70b")
     assert np.isfinite(lse.cpu().numpy()).all()
+
+
+def test_paged_deterministic_across_runs():
+    q, k, v, lens = inputs.decode_inputs(2, 64, 8, 128, 3000, seed=22, seq_lens=[3000, 777])
+    kp, vp, table = _paginate(k, v, 16, seed=3)
+    runs = []
+    for _ in range(2):
+        out, lse = g.decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), lens.to(DEV))
+        torch.cuda.synchronize()
+        runs.append((out.cpu(), lse.cpu()))
+    assert torch.equal(runs[0][0].view(torch.int16), runs[1][0].view(torch.int16))
+    assert torch.equal(runs[0][1], runs[1][1])

@@ -196,3 +196,16 @@ def test_split_chunk_2048_at_the_end_of_a_32k_cache_sampled_rows(oracle_mod):
     torch.cuda.synchronize()
     r = rows.numpy()
     assert_parity(out.cpu()[:, r], lse.cpu()[:, :, r], ref_o, ref_l, f"split chunk n_part={n_part}")
+
+
+@pytest.mark.parametrize("n_part", [1, 3])
+def test_chunk_deterministic_across_runs(n_part):
+    q, k, v, sl = _chunk_inputs(2, 300, 3000, 8, 2, [3000, 2000], seed=24)
+    runs = []
+    for _ in range(2):
+        out, lse = g.prefill_chunk(q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV), window=500,
+                                   n_part=n_part)
+        torch.cuda.synchronize()
+        runs.append((out.cpu(), lse.cpu()))
+    assert torch.equal(runs[0][0].view(torch.int16), runs[1][0].view(torch.int16))
+    assert torch.equal(runs[0][1], runs[1][1])
