@@ -521,6 +521,9 @@ gqa_status gqa_attn_decode_combine(const void* workspace, int B, int H_q, int d,
   if (B < 1 || H_q < 1 || n_split < 1 || B > 65535 || H_q > 65535) return GQA_ERR_INVALID_ARG;
   if (!head_dim_ok(d)) return GQA_ERR_UNSUPPORTED;
   if (!aligned(workspace, 256) || !aligned(out, 16) || !aligned(lse, 4)) return GQA_ERR_INVALID_ARG;
+  unsigned* err = nullptr;
+  const gqa_status st = error_word(&err);
+  if (st != GQA_OK) return st;
   gqa::CombineParams p;
   p.ws_ml = static_cast<const float2*>(workspace);
   p.ws_O = reinterpret_cast<const float*>(static_cast<const char*>(workspace) +
@@ -531,6 +534,7 @@ gqa_status gqa_attn_decode_combine(const void* workspace, int B, int H_q, int d,
   p.n_split = n_split;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
+  p.err = err;
   return cuda_status(gqa::launch_decode_combine(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -668,6 +672,7 @@ gqa_status gqa_last_device_error(gqa_stream_t stream) {
     if (cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
       return GQA_ERR_CUDA;
   }
+  if (word & gqa::kErrBounds) return GQA_ERR_CUDA;  // bounds-checking builds: an internal fault
   if (word & gqa::kErrTimeout) return GQA_ERR_TIMEOUT;
   if (word & (gqa::kErrBadSeqLen | gqa::kErrBadPage)) return GQA_ERR_INVALID_ARG;
   return GQA_OK;

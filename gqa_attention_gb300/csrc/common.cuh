@@ -71,6 +71,29 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
+// ----------------------------------------------------------- bounds checks --
+// A build with GQA_DEBUG_BOUNDS=1 checks every computed global store: the
+// `width` elements from `idx` must lie inside a buffer of `extent` elements,
+// else the store is skipped and kErrBounds is set.  In other builds this is
+// `true` and costs nothing.  (TMA copies are bounds-checked by the hardware.)
+#ifndef GQA_DEBUG_BOUNDS
+#define GQA_DEBUG_BOUNDS 0
+#endif
+__device__ __forceinline__ bool in_bounds(size_t idx, size_t width, size_t extent, unsigned* err) {
+#if GQA_DEBUG_BOUNDS
+  if (idx + width > extent) {
+    atomicOr(err, kErrBounds);
+    return false;
+  }
+#else
+  (void)idx;
+  (void)width;
+  (void)extent;
+  (void)err;
+#endif
+  return true;
+}
+
 // --------------------------------------------------------------------- TMA --
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -219,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
     const int x = 16 * rg + r;
     return ((size_t)b * p.T_q + x / G) * p.H_q + h0 + x % G;
   };
+  const size_t n_rows = (size_t)p.B * p.T_q * p.H_q;  // rows of out, lse and the workspace
   // Launched as a programmatic dependent of the previous kernel in the stream:
   // nothing is read or written before that kernel has completed.  While it
   // finishes, the producer warp of each split's first row group prefetches the
@@ -282,9 +283,9 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
       if (p.n_split == 1 || CLUSTER) {
         // (a cluster's CTAs all see the same length and all return here)
         if (CLUSTER && split != 0) continue;
-        p.out[row * D + c] = __float2bfloat16(NAN);
-        if (c == 0) p.lse[row] = NAN;
-      } else if (c == 0) {
+        if (in_bounds(row * D + c, 1, n_rows * D, p.err)) p.out[row * D + c] = __float2bfloat16(NAN);
+        if (c == 0 && in_bounds(row, 1, n_rows, p.err)) p.lse[row] = NAN;
+      } else if (c == 0 && in_bounds(row * p.n_split + split, 1, n_rows * p.n_split, p.err)) {
         p.ws_ml[row * p.n_split + split] = make_float2(NAN, NAN);
       }
     }
@@ -293,7 +294,8 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
   const int t0 = split * p.chunk;
   if (!CLUSTER && t0 >= L) {  // empty split: the merge identity (-inf, 0); O is not written
     for (int r = threadIdx.x; r < R; r += kThreads)
-      p.ws_ml[out_row(r) * p.n_split + split] = make_float2(-INFINITY, 0.f);
+      if (in_bounds(out_row(r) * p.n_split + split, 1, n_rows * p.n_split, p.err))
+        p.ws_ml[out_row(r) * p.n_split + split] = make_float2(-INFINITY, 0.f);
     return;
   }
   // (in a cluster an empty split still takes part: no tiles, partial (-inf, 0, 0))
@@ -774,12 +776,15 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
       uint2 packed;
       packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
       packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-      *reinterpret_cast<uint2*>(&p.out[row * D + c4 * 4]) = packed;
-      if (c4 == 0) p.lse[row] = (M + log2f(Lsum)) * kLn2;
+      if (in_bounds(row * D + c4 * 4, 4, n_rows * D, p.err))
+        *reinterpret_cast<uint2*>(&p.out[row * D + c4 * 4]) = packed;
+      if (c4 == 0 && in_bounds(row, 1, n_rows, p.err)) p.lse[row] = (M + log2f(Lsum)) * kLn2;
     } else {
       const size_t idx = row * p.n_split + split;
-      *reinterpret_cast<float4*>(&p.ws_O[idx * D + c4 * 4]) = acc;
-      if (c4 == 0) p.ws_ml[idx] = make_float2(M * kLn2, Lsum);
+      if (in_bounds(idx * D + c4 * 4, 4, n_rows * p.n_split * D, p.err))
+        *reinterpret_cast<float4*>(&p.ws_O[idx * D + c4 * 4]) = acc;
+      if (c4 == 0 && in_bounds(idx, 1, n_rows * p.n_split, p.err))
+        p.ws_ml[idx] = make_float2(M * kLn2, Lsum);
     }
   }
 
@@ -817,8 +822,10 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
       }
       const bool poisoned = bad || !(Lt > 0.f);
       const size_t row = out_row(r);
-      p.out[row * D + c] = __float2bfloat16(poisoned ? NAN : acc / Lt);
-      if (c == 0) p.lse[row] = poisoned ? NAN : (Mx + log2f(Lt)) * kLn2;
+      if (in_bounds(row * D + c, 1, n_rows * D, p.err))
+        p.out[row * D + c] = __float2bfloat16(poisoned ? NAN : acc / Lt);
+      if (c == 0 && in_bounds(row, 1, n_rows, p.err))
+        p.lse[row] = poisoned ? NAN : (Mx + log2f(Lt)) * kLn2;
     }
     __syncwarp();
     cluster_sync();  // no CTA leaves while another may still read its partial
@@ -940,9 +947,12 @@ __global__ void __launch_bounds__(kCombineThreads, CHUNK == 8 ? 7 : 4)
   poisoned |= !(Lt > 0.f);  // every split empty, or NaN
   const float inv = poisoned ? NAN : 1.f / Lt;
   __nv_bfloat16* dst = p.out + row * D + lane * VEC;
+  const size_t rows = (size_t)p.B * p.H_q;
+  if (in_bounds(row * D + lane * VEC, VEC, rows * D, p.err)) {
 #pragma unroll
-  for (int v = 0; v < VEC; ++v) dst[v] = __float2bfloat16(tot[v] * inv);
-  if (lane == 0) p.lse[row] = poisoned ? NAN : Mt + logf(Lt);
+    for (int v = 0; v < VEC; ++v) dst[v] = __float2bfloat16(tot[v] * inv);
+  }
+  if (lane == 0 && in_bounds(row, 1, rows, p.err)) p.lse[row] = poisoned ? NAN : Mt + logf(Lt);
 }
 
 __global__ void gqa_wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {

@@ -80,6 +80,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto out_row = [&](int r) -> size_t {
     return ((size_t)b * p.T_q + r / G) * p.H_q + kv * G + r % G;
   };
+  const size_t n_rows = (size_t)p.B * p.T_q * p.H_q;  // rows of out, lse and the workspace
+  // NaN outputs of a row (one split), or its partial (m, l) alone (O is not read)
+  auto write_nan_or_ml = [&](size_t row, float2 ml) {
+    if (p.n_split == 1) {
+      if (in_bounds(row * 128, 128, n_rows * 128, p.err))
+        for (int c = 0; c < 128; ++c) p.out[row * 128 + c] = __float2bfloat16(NAN);
+      if (in_bounds(row, 1, n_rows, p.err)) p.lse[row] = NAN;
+    } else if (in_bounds(row * p.n_split + split, 1, n_rows * p.n_split, p.err)) {
+      p.ws_ml[row * p.n_split + split] = ml;
+    }
+  };
 
   // Set-up that touches no global memory runs before the dependency wait.
   volatile int* abort_v = &abort_flag;
@@ -147,16 +158,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // A bad length: NaN outputs and the error bit.  An empty split: the merge
     // identity (-inf, 0); its O is not written.  (One split is never empty.)
     if (bad && threadIdx.x == 0 && split == 0 && kv == 0) atomicOr(p.err, kErrBadSeqLen);
-    for (int r = threadIdx.x; r < rows; r += kTcThreads) {
-      const size_t row = out_row(r);
-      if (p.n_split == 1) {
-        for (int c = 0; c < 128; ++c) p.out[row * 128 + c] = __float2bfloat16(NAN);
-        p.lse[row] = NAN;
-      } else {
-        p.ws_ml[row * p.n_split + split] =
-            bad ? make_float2(NAN, NAN) : make_float2(-INFINITY, 0.f);
-      }
-    }
+    for (int r = threadIdx.x; r < rows; r += kTcThreads)
+      write_nan_or_ml(out_row(r), bad ? make_float2(NAN, NAN) : make_float2(-INFINITY, 0.f));
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -481,6 +484,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_wait_ld();
         reg_fence32(o);
         if (!store) continue;
+        const size_t at = (one ? row : row * p.n_split + split) * 128 + 32 * c;
+        if (!in_bounds(at, 32, n_rows * (one ? 1 : p.n_split) * 128, p.err)) continue;
         if (one) {
           uint4* d4 = reinterpret_cast<uint4*>(p.out + row * 128 + 32 * c);
 #pragma unroll
@@ -502,19 +507,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       if (store) {
-        if (one)
+        if (one && in_bounds(row, 1, n_rows, p.err))
           p.lse[row] = (m_ref + log2f(l)) * kLn2;
-        else  // m in natural-log units; a row with no visible key: (-inf, 0)
+        else if (!one && in_bounds(row * p.n_split + split, 1, n_rows * p.n_split, p.err))
+          // m in natural-log units; a row with no visible key: (-inf, 0)
           p.ws_ml[row * p.n_split + split] = make_float2(m_ref * kLn2, l);
       }
     } else if (r < rows) {  // a wait gave up, or a bad page: this row's outputs are NaN
-      const size_t row = out_row(r);
-      if (p.n_split == 1) {
-        for (int c = 0; c < 128; ++c) p.out[row * 128 + c] = __float2bfloat16(NAN);
-        p.lse[row] = NAN;
-      } else {
-        p.ws_ml[row * p.n_split + split] = make_float2(NAN, NAN);
-      }
+      write_nan_or_ml(out_row(r), make_float2(NAN, NAN));
     }
   }
 

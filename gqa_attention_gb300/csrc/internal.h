@@ -9,8 +9,9 @@
 
 namespace gqa {
 
-// Bits of the per-device error word.
-enum : unsigned { kErrTimeout = 1u, kErrBadSeqLen = 2u, kErrBadPage = 4u };
+// Bits of the per-device error word.  kErrBounds is set only by a build with
+// GQA_DEBUG_BOUNDS=1: a computed global store index outside its buffer.
+enum : unsigned { kErrTimeout = 1u, kErrBadSeqLen = 2u, kErrBadPage = 4u, kErrBounds = 8u };
 
 constexpr int kDecodeTile = 64;  // tokens per decode pipeline stage; split chunks are multiples
 
@@ -50,6 +51,7 @@ struct CombineParams {
   int B, H_q, d, n_split;
   __nv_bfloat16* out;
   float* lse;
+  unsigned* err;  // device error word (bounds bit of a checking build)
 };
 
 struct PrefillParams {

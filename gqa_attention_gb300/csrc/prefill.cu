@@ -361,8 +361,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const int n = gm.n;
       const int q_row = it.qt * 128 + r;
       const size_t ws_row = (static_cast<size_t>(it.b) * p.S + q_row) * p.H_q + h;
+      const size_t n_rows = static_cast<size_t>(p.B) * p.S * p.H_q;  // rows of out, lse, workspace
       if (GENERAL && n == 0) {  // an empty part: the merge identity (-inf, 0)
-        if (q_row < p.S) p.ws_ml[ws_row * p.n_part + it.part] = make_float2(-INFINITY, 0.f);
+        if (q_row < p.S && in_bounds(ws_row * p.n_part + it.part, 1, n_rows * p.n_part, p.err))
+          p.ws_ml[ws_row * p.n_part + it.part] = make_float2(-INFINITY, 0.f);
         continue;
       }
       float m_ref = -INFINITY, l = 0.f;
@@ -512,6 +514,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tmem_ld32(tO + 32 * c, o);
         tmem_wait_ld();
         reg_fence32(o);
+        if (store && !in_bounds((split ? ws_row * p.n_part + it.part : ws_row) * 128 + 32 * c, 32,
+                                n_rows * (split ? p.n_part : 1) * 128, p.err))
+          continue;
         if (split && store) {  // this part's unnormalised O, fp32
           float4* d4 = reinterpret_cast<float4*>(p.ws_O + (ws_row * p.n_part + it.part) * 128 + 32 * c);
 #pragma unroll
@@ -531,12 +536,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
           }
         }
       }
-      if (split && store)
+      const size_t lse_at = (static_cast<size_t>(it.b) * p.H_q + h) * p.S + q_row;
+      if (split && store && in_bounds(ws_row * p.n_part + it.part, 1, n_rows * p.n_part, p.err))
         p.ws_ml[ws_row * p.n_part + it.part] =
             gm.bad ? make_float2(NAN, NAN) : make_float2(m_ref, l);
-      else if (store)
-        p.lse[(static_cast<size_t>(it.b) * p.H_q + h) * p.S + q_row] =
-            (GENERAL && gm.bad) ? NAN : (m_ref + log2f(l)) * kLn2;
+      else if (!split && store && in_bounds(lse_at, 1, n_rows, p.err))
+        p.lse[lse_at] = (GENERAL && gm.bad) ? NAN : (m_ref + log2f(l)) * kLn2;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&o_empty[x]));
@@ -608,13 +613,15 @@ __global__ void __launch_bounds__(256) gqa_prefill_merge_kernel(const PrefillPar
   uint2 packed;
   packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
   packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  reinterpret_cast<uint2*>(p.out + row * 128)[lane] = packed;
+  if (in_bounds(row * 128 + lane * 4, 4, rows * 128, p.err))
+    reinterpret_cast<uint2*>(p.out + row * 128)[lane] = packed;
   if (lane == 0) {
     const int h = static_cast<int>(row % p.H_q);
     const size_t bi = row / p.H_q;
     const int i = static_cast<int>(bi % p.S);
     const size_t b = bi / p.S;
-    p.lse[(b * p.H_q + h) * p.S + i] = poisoned ? NAN : (M + log2f(L)) * kLn2;
+    if (in_bounds((b * p.H_q + h) * p.S + i, 1, rows, p.err))
+      p.lse[(b * p.H_q + h) * p.S + i] = poisoned ? NAN : (M + log2f(L)) * kLn2;
   }
 }
 

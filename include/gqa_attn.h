@@ -373,7 +373,10 @@ gqa_status gqa_attn_decode_fused(const void* q, const void* k_cache, const void*
 /* Synchronises `stream`, reads and clears the current device's error word and
  * maps it to a status: GQA_ERR_TIMEOUT if a wait timed out, else
  * GQA_ERR_INVALID_ARG if a device-side argument check failed, else GQA_OK.
- * GQA_ERR_CUDA if the synchronisation itself failed. */
+ * GQA_ERR_CUDA if the synchronisation itself failed, or, in a library built
+ * with -DGQA_DEBUG_BOUNDS=1, if a kernel computed a global store index outside
+ * the buffer its parameters describe (that store is skipped; this check
+ * comes first).  The default build compiles those checks out. */
 gqa_status gqa_last_device_error(gqa_stream_t stream);
 
 /* Sets the time limit, in nanoseconds, of every device pipeline wait launched
