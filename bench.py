@@ -7,8 +7,8 @@ One step = one pass of the whole path on seeded synthetic inputs:
   * prefill : Llama3-70B-shaped causal GQA prefill, B=1, S=8192, H_q=64,
               H_kv=8, d=128.
 ``value`` is the decode leg's KV-cache throughput (GB/s of K and V bytes read,
-inputs resident in HBM; three rotating K/V copies so that no step finds its
-inputs in L2); the prefill leg's TFLOP/s (causal FLOPs only) is reported beside
+inputs resident in HBM; rotating K/V copies, at least 1.5 GiB of them, so
+that no step finds its inputs in L2); the prefill leg's TFLOP/s (causal FLOPs only) is reported beside
 it under ``prefill``.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -161,7 +161,17 @@ def _time_region(torch, fn, steps, stream):
     return e0.elapsed_time(e1) / steps
 
 
-N_KV_COPIES = 3  # 3 x 256 MiB of K/V: consecutive steps never find their inputs in L2
+# Decode inputs rotate through copies of the cache so that a copy is read again
+# only after at least ROTATION_BYTES of other cache reads (12 x the 126 MB L2).
+# The decode sweep loads K/V evict-first in L2, which leaves the lines that a
+# step prefetched at normal priority; with 3 copies (384 MiB) some of them were
+# still in L2 when their copy came round again (measured 1.1 us faster per
+# step than with 12 copies), so a shorter rotation would overstate the rate.
+ROTATION_BYTES = 3 << 29
+
+
+def n_copies(bytes_per_copy):
+    return max(2, -(-ROTATION_BYTES // bytes_per_copy))
 
 
 def run_ours(args, rank, world, dist):
@@ -181,6 +191,7 @@ def run_ours(args, rank, world, dist):
     q, k, v, lens = inputs.decode_inputs_for(dc, seed=0)
     kv_bytes = 2 * int(lens.sum()) * dc.H_kv * dc.d * 2
     qd, ld = q.to(dev), lens.to(dev)
+    N_KV_COPIES = n_copies(kv_bytes)
     kds = [k.to(dev) for _ in range(N_KV_COPIES)]
     vds = [v.to(dev) for _ in range(N_KV_COPIES)]
     n_split = g.gqa_attn_decode_default_splits(dc.B, dc.H_kv, dc.S_max, dc.d)
@@ -317,8 +328,8 @@ def run_ours(args, rank, world, dist):
                        "hbm_frac_of_nominal_8TBs": round(value / world / 8000.0, 4)},
             "prefill": {"B": pc.B, "S": pc.S, "H_q": pc.H_q, "H_kv": pc.H_kv, "d": pc.d},
             "l2": (f"decode: {N_KV_COPIES} rotating K/V copies ({N_KV_COPIES * kv_bytes >> 20} MiB), "
-                   "each step reads a copy the previous step did not touch; prefill inputs "
-                   "(160 MiB) exceed L2"),
+                   "a copy is read again only after >= 1.5 GiB (12 x L2) of other cache reads; "
+                   "prefill inputs (160 MiB) exceed L2"),
             "timing": "CUDA events around K back-to-back steps on the launching stream",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
@@ -418,7 +429,7 @@ def run_workload(name, args):
                                                            cfg.S_max, seed=0, ragged=cfg.ragged)
         # bytes the sweep must read: E4M3 codes + one fp32 scale per token, for K and V
         kv_bytes = 2 * int(lens.sum()) * (cfg.H_kv * cfg.d + 4)
-        copies = 1 if kv_bytes > 512 << 20 else 3
+        copies = n_copies(kv_bytes)
         qd, ld = q.to(dev), lens.to(dev)
         caches = [tuple(x.to(dev) for x in (k8, v8, ks, vs)) for _ in range(copies)]
         n = 3 * g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, cfg.d)
@@ -441,7 +452,7 @@ def run_workload(name, args):
                 "unit": "GB/s", "ms_per_step": round(ms, 5), "steps": steps, "n_split": n,
                 "fp8_bytes": kv_bytes, "bf16_equivalent_GBs": round(bf16_equiv / (ms * 1e-3) / 1e9, 2),
                 "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
-                "l2": f"{copies} rotating cache copies" if copies > 1 else "inputs exceed L2",
+                "l2": f"{copies} rotating cache copies",
                 "dtype": "e4m3 cache, bf16 q/out", "data": "synthetic"}
 
     if name.startswith("decode_multi"):
@@ -456,8 +467,9 @@ def run_workload(name, args):
         lens = torch.full((cfg.B,), cfg.S_max, dtype=torch.int32)
         kv_bytes = 2 * int(lens.sum()) * cfg.H_kv * cfg.d * 2
         qd, ld = q.to(dev), lens.to(dev)
-        kds = [k.to(dev) for _ in range(3)]
-        vds = [v.to(dev) for _ in range(3)]
+        nc = n_copies(kv_bytes)
+        kds = [k.to(dev) for _ in range(nc)]
+        vds = [v.to(dev) for _ in range(nc)]
         n = g.gqa_attn_decode_multi_default_splits(cfg.B, T_q, cfg.H_q, cfg.H_kv, cfg.S_max,
                                                    cfg.d)
         ws = g.decode_workspace(cfg.B * T_q, cfg.H_q, cfg.d, n, dev)
@@ -466,14 +478,14 @@ def run_workload(name, args):
         lse_c = torch.empty(cfg.B, cfg.H_q, T_q, dtype=torch.float32, device=dev)
 
         def mstep(i):
-            assert g.gqa_attn_decode_multi(qd, kds[i % 3], vds[i % 3], ld, cfg.B, T_q, cfg.S_max,
+            assert g.gqa_attn_decode_multi(qd, kds[i % nc], vds[i % nc], ld, cfg.B, T_q, cfg.S_max,
                                            cfg.H_q, cfg.H_kv, cfg.d, cfg.scale, n, ws, out, lse,
                                            stream) == g.GQA_OK
             assert g.gqa_attn_decode_combine(ws, cfg.B * T_q, cfg.H_q, cfg.d, n, out, lse,
                                              stream) == g.GQA_OK
 
         def cstep(i):
-            assert g.gqa_attn_prefill_chunk(qd, kds[i % 3], vds[i % 3], ld, cfg.B, T_q, cfg.S_max,
+            assert g.gqa_attn_prefill_chunk(qd, kds[i % nc], vds[i % nc], ld, cfg.B, T_q, cfg.S_max,
                                             cfg.H_q, cfg.H_kv, cfg.d, cfg.scale, -1, out, lse_c,
                                             stream) == g.GQA_OK
 
@@ -485,7 +497,7 @@ def run_workload(name, args):
                 "unit": "GB/s", "ms_per_step": round(ms, 5), "steps": steps, "n_split": n,
                 "kv_bytes": kv_bytes, "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
                 "chunked_prefill_ms_same_problem": round(ms_chunk, 5),
-                "l2": "3 rotating K/V copies", "dtype": "bf16", "data": "synthetic"}
+                "l2": f"{nc} rotating K/V copies", "dtype": "bf16", "data": "synthetic"}
 
     if name.startswith("decode_paged") and "_multi" in name:
         # T_q query tokens ending a Llama3-70B 32K cache held in shuffled pages
@@ -500,8 +512,9 @@ def run_workload(name, args):
         kv_bytes = 2 * int(lens.sum()) * cfg.H_kv * cfg.d * 2
         kp, vp, table = _shuffled_pages(k, v, page, seed=0)
         qd, ld, td = q.to(dev), lens.to(dev), table.to(dev)
-        kps = [kp.to(dev) for _ in range(3)]
-        vps = [vp.to(dev) for _ in range(3)]
+        nc = n_copies(kv_bytes)
+        kps = [kp.to(dev) for _ in range(nc)]
+        vps = [vp.to(dev) for _ in range(nc)]
         n = g.gqa_attn_decode_multi_default_splits(cfg.B, T_q, cfg.H_q, cfg.H_kv, cfg.S_max,
                                                    cfg.d)
         ws = g.decode_workspace(cfg.B * T_q, cfg.H_q, cfg.d, n, dev)
@@ -509,7 +522,7 @@ def run_workload(name, args):
         lse = torch.empty(cfg.B, T_q, cfg.H_q, dtype=torch.float32, device=dev)
 
         def pmstep(i):
-            assert g.gqa_attn_decode_paged_multi(qd, kps[i % 3], vps[i % 3], td, ld, cfg.B, T_q,
+            assert g.gqa_attn_decode_paged_multi(qd, kps[i % nc], vps[i % nc], td, ld, cfg.B, T_q,
                                                  kp.shape[0], page, table.shape[1], cfg.H_q,
                                                  cfg.H_kv, cfg.d, cfg.scale, n, ws, out, lse,
                                                  stream) == g.GQA_OK
@@ -522,7 +535,7 @@ def run_workload(name, args):
                 "value": round(gbs, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
                 "steps": steps, "n_split": n, "kv_bytes": kv_bytes,
                 "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
-                "l2": "3 rotating page pools", "dtype": "bf16", "data": "synthetic"}
+                "l2": f"{nc} rotating page pools", "dtype": "bf16", "data": "synthetic"}
 
     if name.startswith("decode_paged"):
         cfg = inputs.LLAMA70B_DECODE
@@ -531,15 +544,16 @@ def run_workload(name, args):
         kv_bytes = 2 * int(lens.sum()) * cfg.H_kv * cfg.d * 2
         kp, vp, table = _shuffled_pages(k, v, page, seed=0)
         qd, ld, td = q.to(dev), lens.to(dev), table.to(dev)
-        kps = [kp.to(dev) for _ in range(3)]
-        vps = [vp.to(dev) for _ in range(3)]
+        nc = n_copies(kv_bytes)
+        kps = [kp.to(dev) for _ in range(nc)]
+        vps = [vp.to(dev) for _ in range(nc)]
         n = g.paged_default_splits(cfg.B, cfg.H_kv, cfg.S_max, cfg.d, page)
         ws = g.decode_workspace(cfg.B, cfg.H_q, cfg.d, n, dev)
         out = torch.empty(cfg.B, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
         lse = torch.empty(cfg.B, cfg.H_q, dtype=torch.float32, device=dev)
 
         def pstep(i):
-            assert g.gqa_attn_decode_paged(qd, kps[i % 3], vps[i % 3], td, ld, cfg.B, kp.shape[0],
+            assert g.gqa_attn_decode_paged(qd, kps[i % nc], vps[i % nc], td, ld, cfg.B, kp.shape[0],
                                            page, table.shape[1], cfg.H_q, cfg.H_kv, cfg.d,
                                            cfg.scale, n, ws, out, lse, stream) == g.GQA_OK
             assert g.gqa_attn_decode_combine(ws, cfg.B, cfg.H_q, cfg.d, n, out, lse,
@@ -551,13 +565,13 @@ def run_workload(name, args):
                 "value": round(gbs, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
                 "steps": steps, "n_split": n, "kv_bytes": kv_bytes,
                 "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
-                "l2": "3 rotating page pools", "dtype": "bf16", "data": "synthetic"}
+                "l2": f"{nc} rotating page pools", "dtype": "bf16", "data": "synthetic"}
 
     if name.startswith("decode"):
         cfg = inputs.TINY_DECODE if name == "decode_tiny" else inputs.LLAMA70B_DECODE_RAGGED
         q, k, v, lens = inputs.decode_inputs_for(cfg, seed=0)
         kv_bytes = 2 * int(lens.sum()) * cfg.H_kv * cfg.d * 2
-        copies = 1 if kv_bytes > 512 << 20 else 3
+        copies = n_copies(kv_bytes)
         qd, ld = q.to(dev), lens.to(dev)
         kds = [k.to(dev) for _ in range(copies)]
         vds = [v.to(dev) for _ in range(copies)]
@@ -579,7 +593,7 @@ def run_workload(name, args):
         return {"metric": f"decode KV GB/s ({cfg.name})", "value": round(gbs, 2), "unit": "GB/s",
                 "ms_per_step": round(ms, 5), "steps": steps, "n_split": n, "kv_bytes": kv_bytes,
                 "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
-                "l2": f"{copies} rotating K/V copies" if copies > 1 else "inputs exceed L2",
+                "l2": f"{copies} rotating K/V copies",
                 "dtype": "bf16", "data": "synthetic"}
 
     # prefill workloads

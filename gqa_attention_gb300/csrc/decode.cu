@@ -347,7 +347,10 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
     // The whole warp runs the tile loop: lane 0 takes the slot and arms its
     // barrier, then the copies are issued, by lane 0 for a contiguous cache
     // and by lane `sub` for page segment `sub` of a paged one (so that the
-    // boxes of small pages are issued in parallel).
+    // boxes of small pages are issued in parallel).  With one row group per
+    // split each K/V byte is read once, so the copies are evict-first in L2;
+    // several row groups read each tile through L2 and keep the default.
+    const uint64_t kv_pol = p.n_rg == 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
     int issued = 0;
     for (int i = 0; i < n_tiles; ++i) {
       const int st = i % NSTAGE;
@@ -387,18 +390,22 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
             sc_x = 0;
             sc_y = p.num_pages;
           }
-          tma_load_3d(dst_k + sub * h * D, &tm_k, fb, 0, kv, row);
-          tma_load_3d(dst_k + F8::kOffV8 + sub * h * D, &tm_v, fb, 0, kv, row);
-          tma_load_2d(dst_k + F8::kOffKs + sub * F8::slot_bytes(h), &tm_ks, fb, sc_x, sc_y);
-          tma_load_2d(dst_k + F8::kOffVs + sub * F8::slot_bytes(h), &tm_vs, fb, sc_x, sc_y);
+          tma_load_3d(dst_k + sub * h * D, &tm_k, fb, 0, kv, row, kv_pol);
+          tma_load_3d(dst_k + F8::kOffV8 + sub * h * D, &tm_v, fb, 0, kv, row, kv_pol);
+          tma_load_2d(dst_k + F8::kOffKs + sub * F8::slot_bytes(h), &tm_ks, fb, sc_x, sc_y,
+                      kv_pol);
+          tma_load_2d(dst_k + F8::kOffVs + sub * F8::slot_bytes(h), &tm_vs, fb, sc_x, sc_y,
+                      kv_pol);
         }
       } else if (!PAGED) {
         if (lane == 0) {
           const int row = b * p.S_max + t0 + i * kTile;
 #pragma unroll
           for (int blk = 0; blk < Lay::kBlocks; ++blk) {
-            tma_load_3d(dst_k + blk * Lay::kBlockBytes, &tm_k, fb, blk * Lay::kBox, kv, row);
-            tma_load_3d(dst_v + blk * Lay::kBlockBytes, &tm_v, fb, blk * Lay::kBox, kv, row);
+            tma_load_3d(dst_k + blk * Lay::kBlockBytes, &tm_k, fb, blk * Lay::kBox, kv, row,
+                        kv_pol);
+            tma_load_3d(dst_v + blk * Lay::kBlockBytes, &tm_v, fb, blk * Lay::kBox, kv, row,
+                        kv_pol);
           }
         }
       } else {
@@ -415,8 +422,10 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
           const uint32_t off = sub * h * Lay::kSpan;
 #pragma unroll
           for (int blk = 0; blk < Lay::kBlocks; ++blk) {
-            tma_load_3d(dst_k + blk * Lay::kBlockBytes + off, &tm_k, fb, blk * Lay::kBox, kv, row);
-            tma_load_3d(dst_v + blk * Lay::kBlockBytes + off, &tm_v, fb, blk * Lay::kBox, kv, row);
+            tma_load_3d(dst_k + blk * Lay::kBlockBytes + off, &tm_k, fb, blk * Lay::kBox, kv, row,
+                        kv_pol);
+            tma_load_3d(dst_v + blk * Lay::kBlockBytes + off, &tm_v, fb, blk * Lay::kBox, kv, row,
+                        kv_pol);
           }
         }
       }

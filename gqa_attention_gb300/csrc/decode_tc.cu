@@ -218,6 +218,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       x.pg = x.has ? p.block_table[(size_t)b * p.max_blocks + tok / p.page_size] : 0;
       return x;
     };
+    // every K/V tile is read by this CTA alone, once: evict-first in L2
+    const uint64_t kv_pol = l2_policy_evict_first();
     auto issue = [&](bool is_k, int j, Box x) -> bool {
       const int slot = j % kTcSlots;
       uint64_t* empty = is_k ? &k_empty[slot] : &v_empty[slot];
@@ -230,7 +232,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
           mbar_arrive_expect_tx(fb, kTileB);
           for (int dh = 0; dh < 2; ++dh)
-            tma_load_3d(dst + dh * kHalfB, map, fb, dh * 64, kv, b * p.S_max + tok0);
+            tma_load_3d(dst + dh * kHalfB, map, fb, dh * 64, kv, b * p.S_max + tok0, kv_pol);
         }
       } else {
         const bool bad = x.has && (x.pg < 0 || x.pg >= p.num_pages);
@@ -245,7 +247,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         if (lane < nb)
           for (int dh = 0; dh < 2; ++dh)
-            tma_load_3d(dst + dh * kHalfB + lane * h * 128, map, fb, dh * 64, kv, row);
+            tma_load_3d(dst + dh * kHalfB + lane * h * 128, map, fb, dh * 64, kv, row, kv_pol);
       }
       return true;
     };
