@@ -159,3 +159,21 @@ def test_full_size_workloads(oracle_mod, cfg):
     ref_o, ref_l = oracle_mod.decode(q, k, v, lens, cfg.scale)
     out, lse = _run(q, k, v, lens, None)
     assert_parity(out, lse, ref_o, ref_l, cfg.name)
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,d,n_split", [
+    (1, 64, 8, 128, 19),    # 64 rows, <= 32 splits: column-per-warp combine
+    (2, 16, 2, 128, 32),    # the largest split count it takes
+    (2, 16, 2, 128, 33),    # one more: four warps of split groups (16 per round)
+    (16, 64, 8, 128, 19),   # 1024 rows: more than four per SM, split groups of 8
+    (16, 64, 8, 64, 40),    # many rows and splits
+    (3, 8, 2, 32, 9),       # d = 32 on the column kernel
+])
+def test_combine_routes(oracle_mod, B, H_q, H_kv, d, n_split):
+    """Every combine variant the launcher can pick, including empty splits."""
+    S_max = 700
+    lens = [S_max] + [1 + (97 * b) % S_max for b in range(1, B)]
+    q, k, v, sl = inputs.decode_inputs(B, H_q, H_kv, d, S_max, seed=B + n_split, seq_lens=lens)
+    ref_o, ref_l = oracle_mod.decode(q, k, v, sl, 1 / math.sqrt(d))
+    out, lse = _run(q, k, v, sl, n_split)
+    assert_parity(out, lse, ref_o, ref_l, f"B={B} d={d} n_split={n_split}")
