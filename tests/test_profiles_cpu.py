@@ -6,7 +6,8 @@ do.
   lower-triangle tile count (no tile past the diagonal is computed, none twice).
 - Decode: DRAM bytes read equal the K/V bytes once, whether the 8 query heads of
   a KV head (plain decode) or 64 query rows (multi-token decode on the tensor
-  cores) share them: the reads do not grow with G or with the rows.
+  cores) share them, and whether the cache is contiguous or in shuffled pages:
+  the reads do not grow with G, with the rows or with the page gather.
 """
 import os
 import re
@@ -48,6 +49,7 @@ def test_prefill_tensor_work_is_the_causal_tile_count():
     ("decode_split_llama70b_ctx32768.md", KV_BYTES_32K),        # 8 query heads per KV head
     ("decode_tc_multi8_llama70b_ctx32768.md", KV_BYTES_32K),    # 64 query rows per KV head
     ("decode_fp8_llama70b_ctx32768.md", FP8_BYTES_32K),
+    ("decode_paged16_llama70b_ctx32768.md", KV_BYTES_32K),     # 2048 shuffled 16-token pages
 ])
 def test_decode_reads_the_cache_once(name, algo):
     read = _dram_read(_read(name))
