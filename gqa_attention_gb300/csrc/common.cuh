@@ -94,6 +94,18 @@ __device__ __forceinline__ bool in_bounds(size_t idx, size_t width, size_t exten
   return true;
 }
 
+// One 256-bit store of eight 32-bit words to a 32-byte-aligned global address.
+// A thread that writes a whole row of a partial (its own tensor-memory lane)
+// touches half as many lines per warp instruction as with 128-bit stores; the
+// epilogues that write one row per thread are bound by those lines.
+__device__ __forceinline__ void st_global_v8(void* dst, uint32_t w0, uint32_t w1, uint32_t w2,
+                                             uint32_t w3, uint32_t w4, uint32_t w5, uint32_t w6,
+                                             uint32_t w7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w0),
+               "r"(w1), "r"(w2), "r"(w3), "r"(w4), "r"(w5), "r"(w6), "r"(w7)
+               : "memory");
+}
+
 // --------------------------------------------------------------------- TMA --
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -518,11 +518,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                 n_rows * (split ? p.n_part : 1) * 128, p.err))
           continue;
         if (split && store) {  // this part's unnormalised O, fp32
-          float4* d4 = reinterpret_cast<float4*>(p.ws_O + (ws_row * p.n_part + it.part) * 128 + 32 * c);
+          // (the workspace is 256-byte aligned, a partial row 512 bytes)
+          float* d = p.ws_O + (ws_row * p.n_part + it.part) * 128 + 32 * c;
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            d4[v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
-                                __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+          for (int v = 0; v < 4; ++v)
+            st_global_v8(d + 8 * v, o[8 * v], o[8 * v + 1], o[8 * v + 2], o[8 * v + 3], o[8 * v + 4],
+                         o[8 * v + 5], o[8 * v + 6], o[8 * v + 7]);
         } else if (store) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
