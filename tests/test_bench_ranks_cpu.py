@@ -55,3 +55,14 @@ def test_two_rank_max_and_aggregate_rate():
 def test_single_process_is_identity():
     assert bench.max_over_ranks([1.5, 2.5], None, "cpu") == [1.5, 2.5]
     assert bench.whole_job_rate(1, 10.0, 2.0) == 5.0
+
+
+@pytest.mark.parametrize("per_copy", [262144, 64 << 20, 128 << 20, 67371008, 1 << 30, 2200000000])
+def test_rotation_reads_a_copy_again_only_after_1_5_gib(per_copy):
+    """Decode inputs rotate through enough cache copies that at least 1.5 GiB of
+    other cache reads (12 x the 126 MB L2) separate two reads of the same copy."""
+    n = bench.n_copies(per_copy)
+    assert n >= 2
+    assert n * per_copy >= bench.ROTATION_BYTES
+    assert (n - 1) * per_copy < bench.ROTATION_BYTES or n == 2
+    assert bench.ROTATION_BYTES >= 12 * 126 * 10 ** 6
