@@ -506,7 +506,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const float inv = (GENERAL && gm.bad) ? NAN : 1.f / l;
       const bool store = q_row < p.S;
       if (GENERAL && gm.bad && x == 0 && warp == 4 && lane == 0) atomicOr(p.err, kErrBadSeqLen);
-      __nv_bfloat16* dst = p.out + ((static_cast<size_t>(it.b) * p.S + q_row) * p.H_q + h) * 128;
       const bool split = GENERAL && p.n_part > 1;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
@@ -514,8 +513,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tmem_ld32(tO + 32 * c, o);
         tmem_wait_ld();
         reg_fence32(o);
-        if (store && !in_bounds((split ? ws_row * p.n_part + it.part : ws_row) * 128 + 32 * c, 32,
-                                n_rows * (split ? p.n_part : 1) * 128, p.err))
+        if (split && store && !in_bounds((ws_row * p.n_part + it.part) * 128 + 32 * c, 32,
+                                         n_rows * p.n_part * 128, p.err))
           continue;
         if (split && store) {  // this part's unnormalised O, fp32
           // (the workspace is 256-byte aligned, a partial row 512 bytes)
@@ -524,16 +523,42 @@ __global__ void __launch_bounds__(kPThreads, 1)
           for (int v = 0; v < 4; ++v)
             st_global_v8(d + 8 * v, o[8 * v], o[8 * v + 1], o[8 * v + 2], o[8 * v + 3], o[8 * v + 4],
                          o[8 * v + 5], o[8 * v + 6], o[8 * v + 7]);
-        } else if (store) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+        } else if (!split) {
+          // Row r's 32 columns as four 16-byte units u[k] (columns 8k .. 8k+7).
+          // A 4 x 4 transpose of units across each quad of lanes leaves lane
+          // 4q + t with unit t of the quad's rows 4q .. 4q+3, so that every
+          // store instruction writes 64 contiguous bytes of each of 8 rows.
+          uint32_t u[4][4];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-            d4[v] = w;
+          for (int k4 = 0; k4 < 4; ++k4)
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+              u[k4][w] = pack_bf16x2(__uint_as_float(o[8 * k4 + 2 * w]) * inv,
+                                     __uint_as_float(o[8 * k4 + 2 * w + 1]) * inv);
+          const int t = lane & 3;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {  // swap the off-diagonal 2 x 2 blocks (lanes t, t ^ 2)
+            const uint32_t s0 = (t & 2) ? u[0][w] : u[2][w];
+            const uint32_t s1 = (t & 2) ? u[1][w] : u[3][w];
+            const uint32_t r0 = __shfl_xor_sync(0xffffffffu, s0, 2);
+            const uint32_t r1 = __shfl_xor_sync(0xffffffffu, s1, 2);
+            if (t & 2) { u[0][w] = r0; u[1][w] = r1; } else { u[2][w] = r0; u[3][w] = r1; }
+          }
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {  // transpose each 2 x 2 block (lanes t, t ^ 1)
+            const uint32_t s0 = (t & 1) ? u[0][w] : u[1][w];
+            const uint32_t s1 = (t & 1) ? u[2][w] : u[3][w];
+            const uint32_t r0 = __shfl_xor_sync(0xffffffffu, s0, 1);
+            const uint32_t r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+            if (t & 1) { u[0][w] = r0; u[2][w] = r1; } else { u[1][w] = r0; u[3][w] = r1; }
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {  // u[v]: unit t of the quad's row v
+            const int qrow = it.qt * 128 + quarter * 32 + (lane & ~3) + v;
+            const size_t orow = (static_cast<size_t>(it.b) * p.S + qrow) * p.H_q + h;
+            if (qrow < p.S && in_bounds(orow * 128 + 32 * c + 8 * t, 8, n_rows * 128, p.err))
+              *reinterpret_cast<uint4*>(p.out + orow * 128 + 32 * c + 8 * t) =
+                  make_uint4(u[v][0], u[v][1], u[v][2], u[v][3]);
           }
         }
       }
