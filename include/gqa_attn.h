@@ -44,7 +44,7 @@
  *   gqa_attn_decode_multi / gqa_attn_decode_paged_multi (+ combine with B * T_q
  *   rows); above 16 query rows per KV head at d = 128 they run on the tensor
  *   cores (T_q = 8: 27.4 us, against 397 us through the chunked prefill).
- * - A prompt: gqa_attn_prefill_causal (tensor cores, 77-81% of the measured
+ * - A prompt: gqa_attn_prefill_causal (tensor cores, 78-81% of the measured
  *   dense bf16 rate).
  * - A chunk of queries ending a cached sequence, optionally with a sliding
  *   window: gqa_attn_prefill_chunk, or gqa_attn_prefill_chunk_split for long
