@@ -369,7 +369,9 @@ def run_ours(args, rank, world, dist):
         }
     else:
         line["prefill"] = None
-    line["cpu_baseline"] = cpu_baseline(args, steps=5) if not args.no_cpu_baseline else None
+    # the oracle on the host cores: a single-GPU figure, taken on rank 0 at N = 1
+    line["cpu_baseline"] = (cpu_baseline(args, steps=5)
+                            if not args.no_cpu_baseline and world == 1 else None)
     return line
 
 
