@@ -8,8 +8,22 @@ One step = one pass of the whole path on seeded synthetic inputs:
               H_kv=8, d=128.
 ``value`` is the decode leg's KV-cache throughput (GB/s of K and V bytes read,
 inputs resident in HBM; rotating K/V copies, at least 1.5 GiB of them, so
-that no step finds its inputs in L2); the prefill leg's TFLOP/s (causal FLOPs only) is reported beside
-it under ``prefill``.
+that no step finds its inputs in L2); the prefill leg's TFLOP/s (causal FLOPs
+only) is reported beside it under ``prefill``.  The other workloads of the
+same family -- the tiny d = 32 decode, the ragged batch-8 decode and the 64K
+causal prefill -- are timed under the same rules and reported under
+``configs``, each with its roofline, its parity against the fp64 oracle and
+the oracle's own time on the host cores.
+
+Timing: the K steps of a workload are captured once in a CUDA graph (the same
+C-ABI launches, programmatic dependent launches included) and replayed once
+between CUDA events on the launching stream.  The GPU is kept busy right up to
+the start event: a GPU left idle runs the first few hundred microseconds of
+work measurably slower (20 decode steps read 26-29 us each instead of 24 us
+after 0.3-1 s of idle, with the SM and memory clocks reading full speed), so
+the clock sampler is started before the warm-up, and an untimed lead-in graph
+of the same workload is queued between the opening synchronise and the start
+event.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -25,6 +39,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -36,6 +51,9 @@ sys.path.insert(0, ROOT)
 METRIC = "decode KV GB/s (% HBM peak); causal prefill TFLOPS (% bf16 peak)"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+NOMINAL_HBM_GBS = 8000.0        # the ~8 TB/s the decode target is stated against
+NOMINAL_BF16_TFLOPS = 2250.0    # GB300 dense bf16 datasheet figure
+REPEATS = 5                     # extra replays of each timed graph for the median and the min
 
 
 def _peaks():
@@ -75,6 +93,28 @@ def _recorded_traffic(profile_name, files):
         return float(fields["traffic_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
+
+
+DECODE_SOURCES = ["decode.cu", "common.cuh", "internal.h"]
+PREFILL_SOURCES = ["prefill.cu", "tcgen05.cuh", "common.cuh", "internal.h"]
+
+
+def cpu_model():
+    """Host CPU model name (lscpu on Arm, /proc/cpuinfo elsewhere)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
 
 
 class ClockSampler:
@@ -133,7 +173,7 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-# ------------------------------------------------------------------- ours ---
+# ------------------------------------------------------------- helpers ---
 def max_over_ranks(values, dist, device):
     """Element-wise maximum of `values` over all ranks (identity when dist is None)."""
     import torch
@@ -149,18 +189,6 @@ def whole_job_rate(world, units_per_rank, seconds_slowest):
     return world * units_per_rank / seconds_slowest
 
 
-def _time_region(torch, fn, steps, stream):
-    """Events around `steps` back-to-back calls fn(i); returns mean ms per call."""
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(steps):
-        fn(i)
-    e1.record(stream)
-    e1.synchronize()
-    return e0.elapsed_time(e1) / steps
-
-
 # Decode inputs rotate through copies of the cache so that a copy is read again
 # only after at least ROTATION_BYTES of other cache reads (12 x the 126 MB L2).
 # The decode sweep loads K/V evict-first in L2, which leaves the lines that a
@@ -174,6 +202,249 @@ def n_copies(bytes_per_copy):
     return max(2, -(-ROTATION_BYTES // bytes_per_copy))
 
 
+def causal_flops(d, H_q, B, rows):
+    """4 d FLOPs per (query row, visible key, query head); causal row i sees i + 1 keys."""
+    return 4.0 * d * H_q * B * float(sum(int(r) + 1 for r in rows))
+
+
+class TimedGraph:
+    """A captured workload: `steps` timed steps plus the untimed steps around them."""
+
+    def __init__(self, graph, steps, e0=None, e1=None, lead=None):
+        self.graph, self.steps, self.e0, self.e1, self.lead = graph, steps, e0, e1, lead
+
+
+class GraphTimer:
+    """Times K steps of a workload from one replay of a CUDA graph that holds them.
+
+    The graph holds, in stream order, an untimed lead-in of the same workload
+    (~0.3 ms of GPU time, on the cache copies that precede the timed ones in the
+    rotation), the start event, the K timed steps, the end event and, for a
+    decode, one untimed step after them.  The events are event-record nodes of
+    the graph, so the timed steps start from the steady state of a continuously
+    loaded GPU, not from an idle one, and the count of timed steps does not
+    change the per-step figure.  Each replay is bracketed by a barrier and a
+    device synchronise on both sides.  Where the installed torch cannot record
+    events inside a graph, the lead-in is a graph of its own replayed just
+    before the start event."""
+
+    LEAD_MS = 0.3  # GPU time the lead-in covers
+
+    def __init__(self, torch, stream, dist):
+        self.torch = torch
+        self.stream = stream
+        self.dist = dist
+        self.side = torch.cuda.Stream()
+        try:
+            torch.cuda.Event(enable_timing=True, external=True)
+            self.inner_events = True
+        except TypeError:
+            self.inner_events = False
+
+    def _event(self):
+        if self.inner_events:
+            return self.torch.cuda.Event(enable_timing=True, external=True)
+        return self.torch.cuda.Event(enable_timing=True)
+
+    def _capture(self, body):
+        torch = self.torch
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        self.side.wait_stream(self.stream)
+        with torch.cuda.graph(graph, stream=self.side):
+            body(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        return graph
+
+    def _estimate_ms(self, fn, start):
+        """GPU ms per step of three eager steps (sizes the lead-in)."""
+        torch = self.torch
+        fn(start, self.stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for i in range(3):
+            fn(start + i, self.stream)
+        e1.record(self.stream)
+        e1.synchronize()
+        return max(e0.elapsed_time(e1) / 3, 1e-6)
+
+    def prepare(self, fn, steps, copies=None, lead_out=0):
+        """Capture fn(0..steps-1) as the timed steps; `copies` is the length of
+        the workload's cache rotation (None: no rotation)."""
+        n = max(1, math.ceil(self.LEAD_MS / self._estimate_ms(fn, 0)))
+        start = 0
+        if copies is not None:
+            n = min(n, copies)
+            start = copies - n
+        if self.inner_events:
+            e0, e1 = self._event(), self._event()
+
+            def body(s):
+                for i in range(n):
+                    fn(start + i, s)
+                e0.record(s)
+                for i in range(steps):
+                    fn(i, s)
+                e1.record(s)
+                for i in range(lead_out):
+                    fn(steps + i, s)
+
+            tg = TimedGraph(self._capture(body), steps, e0, e1)
+        else:
+            graph = self._capture(lambda s: [fn(i, s) for i in range(steps)])
+            lead = self._capture(lambda s: [fn(start + i, s) for i in range(n)])
+            tg = TimedGraph(graph, steps, lead=lead)
+        self.warm(tg)
+        return tg
+
+    def warm(self, tg):
+        if tg.lead is not None:
+            tg.lead.replay()
+        tg.graph.replay()
+        self.torch.cuda.synchronize()
+
+    def _barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+        self.torch.cuda.synchronize()
+
+    def time(self, tg):
+        """Mean ms per timed step of one replay."""
+        torch = self.torch
+        self._barrier()
+        with torch.cuda.stream(self.stream):
+            if tg.e0 is not None:
+                tg.graph.replay()
+                e0, e1 = tg.e0, tg.e1
+            else:
+                e0, e1 = self._event(), self._event()
+                tg.lead.replay()
+                e0.record(self.stream)
+                tg.graph.replay()
+                e1.record(self.stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        self._barrier()
+        return ms / tg.steps
+
+    def time_repeated(self, tg, repeats):
+        """(first replay, [all replays]) in ms per step."""
+        first = self.time(tg)
+        return first, [first] + [self.time(tg) for _ in range(repeats)]
+
+
+def _repeat_stats(ms_list):
+    return {"n": len(ms_list), "median_ms": round(statistics.median(ms_list), 6),
+            "min_ms": round(min(ms_list), 6), "max_ms": round(max(ms_list), 6)}
+
+
+# ------------------------------------------------------------ workloads ---
+class DecodeLeg:
+    """A decode workload: split kernel (+ combine when split) over rotating cache copies."""
+
+    def __init__(self, torch, g, cfg, dev, seed=0):
+        from gqa_attention_gb300 import inputs
+
+        self.torch, self.g, self.cfg, self.dev = torch, g, cfg, dev
+        q, k, v, lens = inputs.decode_inputs_for(cfg, seed=seed)
+        self.host = (q, k, v, lens)
+        self.kv_bytes = 4 * cfg.d * cfg.H_kv * int(lens.sum())
+        self.copies = n_copies(self.kv_bytes)
+        self.qd, self.ld = q.to(dev), lens.to(dev)
+        kd, vd = k.to(dev), v.to(dev)
+        # all copies in one allocation each for K and V (views per copy)
+        self.kall = torch.empty((self.copies,) + tuple(k.shape), dtype=k.dtype, device=dev)
+        self.vall = torch.empty_like(self.kall)
+        self.kall.copy_(kd.unsqueeze(0).expand_as(self.kall))
+        self.vall.copy_(vd.unsqueeze(0).expand_as(self.vall))
+        del kd, vd
+        self.n_split = g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, cfg.d)
+        self.ws = g.decode_workspace(cfg.B, cfg.H_q, cfg.d, self.n_split, dev)
+        self.out = torch.empty(cfg.B, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(cfg.B, cfg.H_q, dtype=torch.float32, device=dev)
+        self.launches_per_step = 2 if self.n_split > 1 else 1
+        self.ws_bytes = (g.gqa_attn_decode_workspace_bytes(cfg.B, cfg.H_q, cfg.d, self.n_split)
+                         if self.n_split > 1 else 0)
+
+    def split(self, i, stream):
+        c, g = self.cfg, self.g
+        j = i % self.copies
+        st = g.gqa_attn_decode(self.qd, self.kall[j], self.vall[j], self.ld, c.B, c.S_max, c.H_q,
+                               c.H_kv, c.d, c.scale, self.n_split, self.ws, self.out, self.lse,
+                               stream)
+        if st:
+            raise RuntimeError(f"decode failed: {g.status_str(st)}")
+
+    def step(self, i, stream):
+        # split kernel + combine kernel back to back (the combine may overlap the
+        # split kernel's tail through programmatic dependent launch)
+        self.split(i, stream)
+        if self.n_split > 1:
+            c, g = self.cfg, self.g
+            st = g.gqa_attn_decode_combine(self.ws, c.B, c.H_q, c.d, self.n_split, self.out,
+                                           self.lse, stream)
+            if st:
+                raise RuntimeError(f"combine failed: {g.status_str(st)}")
+
+    def all_bytes(self):
+        """Every byte the step moves: K/V, Q, the split partials written and read back, O, LSE."""
+        c = self.cfg
+        return (self.kv_bytes + c.B * c.H_q * c.d * 2 + 2 * self.ws_bytes
+                + c.B * c.H_q * (c.d * 2 + 4))
+
+    def results(self):
+        return self.out.float().cpu(), self.lse.float().cpu()
+
+
+class PrefillLeg:
+    """A causal prefill workload (inputs larger than L2, re-read every step)."""
+
+    def __init__(self, torch, g, cfg, dev, seed=0):
+        from gqa_attention_gb300 import inputs
+
+        self.torch, self.g, self.cfg, self.dev = torch, g, cfg, dev
+        q, k, v = inputs.prefill_inputs_for(cfg, seed=seed)
+        self.host = (q, k, v)
+        self.qd, self.kd, self.vd = q.to(dev), k.to(dev), v.to(dev)
+        self.out = torch.empty_like(self.qd)
+        self.lse = torch.empty(cfg.B, cfg.H_q, cfg.S, dtype=torch.float32, device=dev)
+        self.flops = causal_flops(cfg.d, cfg.H_q, cfg.B, range(cfg.S))
+        self.launches_per_step = 1
+        # query rows the oracle checks (and times): the configuration's own
+        # sample where it names one, else 512 seeded rows
+        self.rows = inputs.sample_rows(cfg.S, cfg.oracle_rows or 512, seed=seed)
+
+    def step(self, i, stream):
+        c, g = self.cfg, self.g
+        st = g.gqa_attn_prefill_causal(self.qd, self.kd, self.vd, c.B, c.S, c.H_q, c.H_kv, c.d,
+                                       c.scale, self.out, self.lse, stream)
+        if st:
+            raise RuntimeError(f"prefill failed: {g.status_str(st)}")
+
+    def results(self):
+        r = self.rows.to(self.dev)
+        return (self.out.index_select(1, r).float().cpu(),
+                self.lse.index_select(2, r).float().cpu())
+
+
+def _hbm_roofline(kernel, bytes_per_launch, ms, hbm_gbs, peak_kind, traffic):
+    achieved = bytes_per_launch / (ms * 1e-3) / 1e9
+    return {"kernel": kernel, "bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_gbs,
+            "unit": "GB/s", "frac": round(achieved / hbm_gbs, 4), "peak_kind": peak_kind,
+            "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM_GBS, 4),
+            "traffic": traffic, "algorithmic_bytes_per_launch": bytes_per_launch}
+
+
+def _tensor_roofline(kernel, flops, ms, bf16_tf, bf16_tf_sus, peak_kind, traffic):
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"kernel": kernel, "bound": "tensor", "achieved": round(tf, 2), "peak": bf16_tf,
+            "unit": "TFLOP/s", "frac": round(tf / bf16_tf, 4), "peak_kind": peak_kind + " (burst)",
+            "frac_of_sustained": round(tf / bf16_tf_sus, 4),
+            "frac_of_nominal_2250TF": round(tf / NOMINAL_BF16_TFLOPS, 4),
+            "traffic": traffic, "algorithmic_flops_per_launch": flops}
+
+
+# ------------------------------------------------------------------- ours ---
 def run_ours(args, rank, world, dist):
     import torch
 
@@ -185,194 +456,352 @@ def run_ours(args, rank, world, dist):
     g.load()
     stream = torch.cuda.current_stream()
     hbm_gbs, bf16_tf, bf16_tf_sus, peak_kind = _peaks()
+    K = args.steps
+    want_decode = args.only in (None, "decode")
+    want_prefill = args.only in (None, "prefill")
+    want_configs = args.only is None
 
-    # ---------------- decode leg (Llama3-70B decode, ctx 32768) ----------------
-    dc = inputs.LLAMA70B_DECODE
-    q, k, v, lens = inputs.decode_inputs_for(dc, seed=0)
-    kv_bytes = 2 * int(lens.sum()) * dc.H_kv * dc.d * 2
-    qd, ld = q.to(dev), lens.to(dev)
-    N_KV_COPIES = n_copies(kv_bytes)
-    kds = [k.to(dev) for _ in range(N_KV_COPIES)]
-    vds = [v.to(dev) for _ in range(N_KV_COPIES)]
-    n_split = g.gqa_attn_decode_default_splits(dc.B, dc.H_kv, dc.S_max, dc.d)
-    ws = g.decode_workspace(dc.B, dc.H_q, dc.d, n_split, dev)
-    out = torch.empty(dc.B, dc.H_q, dc.d, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(dc.B, dc.H_q, dtype=torch.float32, device=dev)
+    # ---------------- workloads ----------------
+    dec = DecodeLeg(torch, g, inputs.LLAMA70B_DECODE, dev) if want_decode else None
+    pre = PrefillLeg(torch, g, inputs.LLAMA70B_PREFILL_8K, dev) if want_prefill else None
+    extra = {}
+    if want_configs:
+        extra["decode_tiny"] = DecodeLeg(torch, g, inputs.TINY_DECODE, dev)
+        extra["decode_ragged"] = DecodeLeg(torch, g, inputs.LLAMA70B_DECODE_RAGGED, dev)
+        extra["prefill_64k"] = PrefillLeg(torch, g, inputs.PREFILL_64K, dev)
+    legs = [x for x in (dec, pre, *extra.values()) if x is not None]
 
-    def split_only(i):
-        st = g.gqa_attn_decode(qd, kds[i % N_KV_COPIES], vds[i % N_KV_COPIES], ld, dc.B,
-                               dc.S_max, dc.H_q, dc.H_kv, dc.d, dc.scale, n_split, ws, out, lse,
-                               stream)
-        if st:
-            raise RuntimeError(f"decode failed: {g.status_str(st)}")
-
-    def decode_step(i):
-        # split kernel + combine kernel back to back (the combine may overlap the
-        # split kernel's tail through programmatic dependent launch)
-        split_only(i)
-        st = g.gqa_attn_decode_combine(ws, dc.B, dc.H_q, dc.d, n_split, out, lse, stream)
-        if st:
-            raise RuntimeError(f"combine failed: {g.status_str(st)}")
-
-    # ---------------- prefill leg (Llama3-70B causal prefill, S 8192) ----------
-    pc = inputs.LLAMA70B_PREFILL_8K
-    pq, pk, pv = inputs.prefill_inputs_for(pc, seed=0)
-    pqd, pkd, pvd = (x.to(dev) for x in (pq, pk, pv))
-    pout = torch.empty_like(pqd)
-    plse = torch.empty(pc.B, pc.H_q, pc.S, dtype=torch.float32, device=dev)
-    causal_flops = 4.0 * pc.d * pc.H_q * pc.B * pc.S * (pc.S + 1) / 2
-    prefill_ok = g.gqa_attn_prefill_causal(pqd, pkd, pvd, pc.B, pc.S, pc.H_q, pc.H_kv, pc.d,
-                                           pc.scale, pout, plse, stream) == g.GQA_OK
-    torch.cuda.synchronize()
-
-    def prefill_step(i):
-        st = g.gqa_attn_prefill_causal(pqd, pkd, pvd, pc.B, pc.S, pc.H_q, pc.H_kv, pc.d,
-                                       pc.scale, pout, plse, stream)
-        if st:
-            raise RuntimeError(f"prefill failed: {g.status_str(st)}")
-
-    run_decode = args.only in (None, "decode")
-    if args.only == "decode":
-        prefill_ok = False
-
-    # ---------------- warm-up ----------------
-    for i in range(args.warmup):
-        if run_decode:
-            decode_step(i)
-            split_only(i)
-        if prefill_ok:
-            prefill_step(i)
+    # one eager call of each workload (library set-up happens outside any capture)
+    for leg in legs:
+        leg.step(0, stream)
     torch.cuda.synchronize()
     if g.gqa_last_device_error(stream) != g.GQA_OK:
-        raise RuntimeError("device error during warm-up")
+        raise RuntimeError("device error in the first calls")
 
-    # ---------------- timed region ----------------
+    timer = GraphTimer(torch, stream, dist)
+    graphs, split_graphs = {}, {}
+    for leg in legs:
+        dec_leg = isinstance(leg, DecodeLeg)
+        copies = leg.copies if dec_leg else None
+        graphs[id(leg)] = timer.prepare(leg.step, K, copies, lead_out=1 if dec_leg else 0)
+        if dec_leg and leg.n_split > 1:
+            split_graphs[id(leg)] = timer.prepare(leg.split, K, copies, lead_out=1)
+
     with ClockSampler(dev.index) as clk:
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
         t_wall = time.perf_counter()
-        dec_ms = _time_region(torch, decode_step, args.steps, stream) if run_decode else float("nan")
-        split_ms = _time_region(torch, split_only, args.steps, stream) if run_decode else float("nan")
-        pre_ms = _time_region(torch, prefill_step, args.steps, stream) if prefill_ok else None
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
+        timed = {}
+        for leg in legs:
+            # warm-up right before this workload's timed regions: W steps, one
+            # read of every rotating cache copy, one replay of its graphs
+            for i in range(args.warmup):
+                leg.step(i, stream)
+            if isinstance(leg, DecodeLeg):
+                for c in range(leg.copies):
+                    leg.step(c, stream)
+            timer.warm(graphs[id(leg)])
+            if g.gqa_last_device_error(stream) != g.GQA_OK:
+                raise RuntimeError("device error during warm-up")
+            # timed regions: K steps each
+            timed[id(leg)] = timer.time_repeated(graphs[id(leg)], REPEATS)
+            if id(leg) in split_graphs:
+                timer.warm(split_graphs[id(leg)])
+                timed[("split", id(leg))] = timer.time_repeated(split_graphs[id(leg)], REPEATS)
         wall_s = time.perf_counter() - t_wall
     clocks = clk.summary()
     if g.gqa_last_device_error(stream) != g.GQA_OK:
-        raise RuntimeError("device error during the timed region")
+        raise RuntimeError("device error during the timed regions")
+    results = {id(leg): leg.results() for leg in legs}
 
     # ---------------- end to end through the C ABI from pinned host buffers -----
-    hq, hk, hv, hl = (x.pin_memory() for x in (q, k, v, lens))
-    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hl))
-    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+    e2e = None
+    if dec is not None and args.only is None:
+        q, k, v, lens = dec.host
+        hq, hk, hv, hl = (x.pin_memory() for x in (q, k, v, lens))
+        hout = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
+        hlse = torch.empty(dec.lse.shape, dtype=dec.lse.dtype).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hl))
+        d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
 
-    def e2e_step(i):
-        qd.copy_(hq, non_blocking=True)
-        kds[0].copy_(hk, non_blocking=True)
-        vds[0].copy_(hv, non_blocking=True)
-        ld.copy_(hl, non_blocking=True)
-        decode_step(0)
-        hout.copy_(out, non_blocking=True)
-        hlse.copy_(lse, non_blocking=True)
+        def e2e_step():
+            dec.qd.copy_(hq, non_blocking=True)
+            dec.kall[0].copy_(hk, non_blocking=True)
+            dec.vall[0].copy_(hv, non_blocking=True)
+            dec.ld.copy_(hl, non_blocking=True)
+            dec.step(0, stream)
+            hout.copy_(dec.out, non_blocking=True)
+            hlse.copy_(dec.lse, non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 50))
-    if run_decode:
-        _time_region(torch, e2e_step, 2, stream)
-        e2e_ms = _time_region(torch, e2e_step, e2e_steps, stream)
-    else:
-        e2e_ms = float("nan")
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_steps = max(3, min(K, 50))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e2e = {"ms": e0.elapsed_time(e1) / e2e_steps, "h2d": h2d, "d2h": d2h}
 
-    # max over ranks
-    dec_ms, split_ms, pre_ms_max, e2e_ms = max_over_ranks(
-        [dec_ms, split_ms, pre_ms or 0.0, e2e_ms], dist, dev)
-    pre_ms = pre_ms_max if pre_ms is not None else None
+    # ---------------- max over ranks ----------------
+    keys = sorted(timed, key=str)
+    flat = []
+    for key in keys:
+        first, allv = timed[key]
+        flat += [first] + allv
+    flat.append(e2e["ms"] if e2e else 0.0)
+    flat = max_over_ranks(flat, dist, dev)
+    pos = 0
+    for key in keys:
+        n = 1 + len(timed[key][1])
+        timed[key] = (flat[pos], flat[pos + 1:pos + n])
+        pos += n
+    if e2e:
+        e2e["ms"] = flat[pos]
     if rank != 0:
         return None
 
-    value = whole_job_rate(world, kv_bytes, dec_ms * 1e-3) / 1e9
-    ws_bytes = g.gqa_attn_decode_workspace_bytes(dc.B, dc.H_q, dc.d, n_split) if n_split > 1 else 0
-    all_bytes = (kv_bytes + dc.B * dc.H_q * dc.d * 2          # K/V read, Q read
-                 + 2 * ws_bytes                                # partials written, read back
-                 + dc.B * dc.H_q * (dc.d * 2 + 4))             # O (bf16) and LSE written
-    achieved = kv_bytes / (split_ms * 1e-3) / 1e9
-    traffic = _recorded_traffic("decode_split_llama70b_ctx32768.md",
-                                ["decode.cu", "common.cuh", "internal.h"])
+    def leg_report(leg):
+        first, allv = timed[id(leg)]
+        rep = {"ms_per_step": round(first, 6), "repeats": _repeat_stats(allv),
+               "launches_per_step": leg.launches_per_step}
+        c = leg.cfg
+        if isinstance(leg, DecodeLeg):
+            gbs = whole_job_rate(world, leg.kv_bytes, first * 1e-3) / 1e9
+            rep.update({"value": round(gbs, 2), "unit": "GB/s",
+                        "frac_of_" + peak_kind + "_hbm": round(gbs / world / hbm_gbs, 4),
+                        "frac_of_nominal_8TBs": round(gbs / world / NOMINAL_HBM_GBS, 4),
+                        "B": c.B, "H_q": c.H_q, "H_kv": c.H_kv, "d": c.d, "S_max": c.S_max,
+                        "seq_lens": [int(x) for x in leg.host[3]] if c.B > 1 else c.S_max,
+                        "n_split": leg.n_split, "kv_bytes": leg.kv_bytes,
+                        "all_bytes": leg.all_bytes(),
+                        "all_bytes_GBs": round(leg.all_bytes() / (first * 1e-3) / 1e9, 2),
+                        "l2": f"{leg.copies} rotating cache copies "
+                              f"({leg.copies * leg.kv_bytes >> 20} MiB of K/V read)"})
+            split_key = ("split", id(leg))
+            if split_key in timed:
+                s_first, s_all = timed[split_key]
+                rep["ms_split_kernel"] = round(s_first, 6)
+                rep["split_repeats"] = _repeat_stats(s_all)
+                kern_ms = s_first
+            else:
+                kern_ms = first
+            traffic = (_recorded_traffic("decode_split_llama70b_ctx32768.md", DECODE_SOURCES)
+                       if c is inputs.LLAMA70B_DECODE else None)
+            rep["roofline"] = _hbm_roofline("gqa_decode_split_kernel", leg.kv_bytes, kern_ms,
+                                            hbm_gbs, peak_kind, traffic)
+        else:
+            tf = whole_job_rate(world, leg.flops, first * 1e-3) / 1e12
+            rep.update({"value": round(tf, 2), "unit": "TFLOP/s",
+                        "frac_of_" + peak_kind + "_bf16": round(tf / world / bf16_tf, 4),
+                        "frac_of_nominal_2250TF": round(tf / world / NOMINAL_BF16_TFLOPS, 4),
+                        "B": c.B, "S": c.S, "H_q": c.H_q, "H_kv": c.H_kv, "d": c.d,
+                        "value_scale": c.value_scale, "causal_flops": leg.flops,
+                        "l2": f"inputs {(leg.qd.numel() + 2 * leg.kd.numel()) * 2 >> 20} MiB "
+                              "(> L2), read again every step"})
+            traffic = (_recorded_traffic("prefill_causal_llama70b_s8192.md", PREFILL_SOURCES)
+                       if c is inputs.LLAMA70B_PREFILL_8K else None)
+            rep["roofline"] = _tensor_roofline("gqa_prefill_causal_kernel", leg.flops, first,
+                                               bf16_tf, bf16_tf_sus, peak_kind, traffic)
+        return rep
+
+    reports = {}
+    if dec is not None:
+        reports["decode_llama70b"] = leg_report(dec)
+    if pre is not None:
+        reports["prefill_8k"] = leg_report(pre)
+    for name, leg in extra.items():
+        reports[name] = leg_report(leg)
+
+    # launches of this library's kernels inside the timed regions (each region
+    # is K steps; every graph is replayed 1 + REPEATS times)
+    launches = 0
+    for leg in legs:
+        launches += (1 + REPEATS) * K * leg.launches_per_step
+        if id(leg) in split_graphs:
+            launches += (1 + REPEATS) * K
+
+    dr = reports.get("decode_llama70b")
+    pr = reports.get("prefill_8k")
+    value = dr["value"] if dr else None
     line = {
         "metric": METRIC,
-        "value": round(value, 2),
+        "value": value,
         "unit": "GB/s",
         "n_gpus": world,
-        "steps": args.steps,
+        "steps": K,
         "warmup": args.warmup,
-        "ms_per_step": round(dec_ms + (pre_ms or 0.0), 5),
+        "ms_per_step": round((dr["ms_per_step"] if dr else 0.0) + (pr["ms_per_step"] if pr else 0.0), 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded torch.randn, rounded to bf16)",
         "config": {
-            "workload": f"{dc.name} (value) + {pc.name} (prefill)",
-            "decode": {"B": dc.B, "H_q": dc.H_q, "H_kv": dc.H_kv, "d": dc.d, "ctx": dc.S_max,
-                       "n_split": n_split, "kv_bytes": kv_bytes,
-                       # every byte the two launches move: K/V, Q, the split partials
-                       # written and read back, O and LSE
-                       "all_bytes": all_bytes,
-                       "all_bytes_GBs": round(all_bytes / (dec_ms * 1e-3) / 1e9, 2),
-                       "ms_split_plus_combine": round(dec_ms, 5),
-                       "ms_split_kernel": round(split_ms, 5),
-                       "hbm_frac_of_" + peak_kind: round(value / world / hbm_gbs, 4),
-                       "hbm_frac_of_nominal_8TBs": round(value / world / 8000.0, 4)},
-            "prefill": {"B": pc.B, "S": pc.S, "H_q": pc.H_q, "H_kv": pc.H_kv, "d": pc.d},
-            "l2": (f"decode: {N_KV_COPIES} rotating K/V copies ({N_KV_COPIES * kv_bytes >> 20} MiB), "
-                   "a copy is read again only after >= 1.5 GiB (12 x L2) of other cache reads; "
-                   "prefill inputs (160 MiB) exceed L2"),
-            "timing": "CUDA events around K back-to-back steps on the launching stream",
+            "workload": f"{inputs.LLAMA70B_DECODE.name} (value) + "
+                        f"{inputs.LLAMA70B_PREFILL_8K.name} (prefill)",
+            "decode": ({k: dr[k] for k in ("B", "H_q", "H_kv", "d", "n_split", "kv_bytes",
+                                           "all_bytes", "all_bytes_GBs", "l2")}
+                       | {"ctx": inputs.LLAMA70B_DECODE.S_max,
+                          "ms_split_plus_combine": dr["ms_per_step"],
+                          "ms_split_kernel": dr.get("ms_split_kernel"),
+                          "step_median_ms": dr["repeats"]["median_ms"],
+                          "step_min_ms": dr["repeats"]["min_ms"],
+                          "hbm_frac_of_" + peak_kind: dr["frac_of_" + peak_kind + "_hbm"],
+                          "hbm_frac_of_nominal_8TBs": dr["frac_of_nominal_8TBs"]}) if dr else None,
+            "prefill": {k: pr[k] for k in ("B", "S", "H_q", "H_kv", "d")} if pr else None,
+            "l2": "decode: rotating K/V copies, a copy is read again only after >= 1.5 GiB "
+                  "(12 x L2) of other cache reads; prefill inputs exceed L2",
+            "timing": ("each workload: one CUDA graph holding an untimed lead-in of the same "
+                       "workload (~0.3 ms), the start event, the K timed steps, the end event "
+                       "(and one untimed decode step); replayed with a barrier + synchronize on "
+                       "both sides, warmed right before; events on the launching stream; "
+                       f"{REPEATS} more replays give the median and the min"),
+            "events_inside_graph": timer.inner_events,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "clocks": clocks,
-        "roofline": {
-            "kernel": "gqa_decode_split_kernel",
-            "bound": "hbm",
-            "achieved": round(achieved, 2),
-            "peak": hbm_gbs,
-            "unit": "GB/s",
-            "frac": round(achieved / hbm_gbs, 4),
-            "peak_kind": peak_kind,
-            "traffic": traffic,
-            "algorithmic_bytes_per_launch": kv_bytes,
-        },
-        "gpu_launches": args.steps * (3 + (1 if prefill_ok else 0)),
-        "e2e": {"value": round(whole_job_rate(world, kv_bytes, e2e_ms * 1e-3) / 1e9, 2),
-                "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 4)},
-        "wall_s_timed_region": round(wall_s, 3),
+        "roofline": dr["roofline"] if dr else (pr["roofline"] if pr else None),
+        "gpu_launches": launches,
+        "wall_s_timed_regions": round(wall_s, 3),
     }
-    if pre_ms is not None:
-        tflops = causal_flops / (pre_ms * 1e-3) / 1e12
-        line["prefill"] = {
-            "value": round(whole_job_rate(world, causal_flops, pre_ms * 1e-3) / 1e12, 2),
-            "unit": "TFLOP/s", "ms": round(pre_ms, 4),
-            "causal_flops": causal_flops,
-            "roofline": {"kernel": "gqa_prefill_causal_kernel", "bound": "tensor",
-                         "achieved": round(tflops, 2), "peak": bf16_tf, "unit": "TFLOP/s",
-                         "frac": round(tflops / bf16_tf, 4),
-                         "peak_kind": peak_kind + " (burst)",
-                         "frac_of_sustained": round(tflops / bf16_tf_sus, 4),
-                         "traffic": _recorded_traffic("prefill_causal_llama70b_s8192.md",
-                                                      ["prefill.cu", "tcgen05.cuh", "common.cuh",
-                                                       "internal.h"])},
+    if e2e:
+        line["e2e"] = {"value": round(whole_job_rate(world, dec.kv_bytes, e2e["ms"] * 1e-3) / 1e9, 2),
+                       "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
+                       "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e["ms"], 4),
+                       "path": "gqa_attn_decode + gqa_attn_decode_combine through the C ABI, "
+                               "eager launches, pinned host buffers copied in and out every step"}
+    line["prefill"] = ({"value": pr["value"], "unit": "TFLOP/s", "ms": pr["ms_per_step"],
+                        "causal_flops": pr["causal_flops"], "repeats": pr["repeats"],
+                        "roofline": pr["roofline"]} if pr else None)
+    if want_configs:
+        line["configs"] = {
+            "decode_tiny": reports["decode_tiny"] | {"workload": inputs.TINY_DECODE.name},
+            "decode_llama70b": {"see": "value, config.decode, roofline",
+                                "workload": inputs.LLAMA70B_DECODE.name},
+            "decode_ragged": reports["decode_ragged"] | {"workload": inputs.LLAMA70B_DECODE_RAGGED.name},
+            "prefill_8k": {"see": "prefill", "workload": inputs.LLAMA70B_PREFILL_8K.name},
+            "prefill_64k": reports["prefill_64k"] | {"workload": inputs.PREFILL_64K.name},
         }
+    # the oracle on the host cores (and the parity of every timed output
+    # against it): a single-GPU figure, taken on rank 0 at N = 1
+    if not args.no_cpu_baseline and world == 1:
+        oracle_legs = {"decode_llama70b": dec, "prefill_8k": pre, **extra}
+        cpu = cpu_baseline(oracle_legs, {id(l): results[id(l)] for l in legs})
+        if "decode_llama70b" in cpu:
+            line["cpu_baseline"] = cpu["decode_llama70b"]["cpu_baseline"]
+            line["parity"] = cpu["decode_llama70b"]["parity"]
+        if pr and "prefill_8k" in cpu:
+            line["prefill"]["cpu_baseline"] = cpu["prefill_8k"]["cpu_baseline"]
+            line["prefill"]["parity"] = cpu["prefill_8k"]["parity"]
+        for name in ("decode_tiny", "decode_ragged", "prefill_64k"):
+            if want_configs and name in cpu:
+                line["configs"][name].update(cpu[name])
     else:
-        line["prefill"] = None
-    # the oracle on the host cores: a single-GPU figure, taken on rank 0 at N = 1
-    line["cpu_baseline"] = (cpu_baseline(args, steps=5)
-                            if not args.no_cpu_baseline and world == 1 else None)
+        line["cpu_baseline"] = None
     return line
+
+
+# ------------------------------------------------------ CPU oracle baseline --
+PARITY_BAR = {"max_dO": 2e-2, "mean_dO": 2e-3, "max_dLSE": 1e-3}
+
+
+def _parity(out_gpu, lse_gpu, out_ref, lse_ref, what):
+    import numpy as np
+
+    o = np.asarray(out_gpu.numpy(), dtype=np.float64)
+    l_ = np.asarray(lse_gpu.numpy(), dtype=np.float64)
+    do, dl = np.abs(o - out_ref), np.abs(l_ - lse_ref)
+    r = {"compared": what, "max_dO": float(do.max()), "mean_dO": float(do.mean()),
+         "max_dLSE": float(dl.max()), "finite": bool(np.isfinite(o).all() and np.isfinite(l_).all())}
+    r["pass"] = bool(r["finite"] and all(r[k] <= v for k, v in PARITY_BAR.items()))
+    return r
+
+
+def cpu_baseline(legs, results):
+    """Time the fp64 oracle on the host cores on each workload (whole, or a stated
+    row sample) and compare the GPU outputs of the timed regions with it."""
+    import oracle
+
+    oracle.build()
+    cores = os.cpu_count() or 1
+    model = cpu_model()
+    out = {}
+    for name, leg in legs.items():
+        if leg is None:
+            continue
+        if isinstance(leg, DecodeLeg):
+            q, k, v, lens = leg.host
+            reps = 5 if leg.kv_bytes < (256 << 20) else 1
+            times = []
+            for _ in range(reps):
+                t0 = time.perf_counter()
+                ref_o, ref_l = oracle.decode(q, k, v, lens, leg.cfg.scale, nthreads=cores)
+                times.append(time.perf_counter() - t0)
+            t = statistics.median(times)
+            cb = {"value": round(leg.kv_bytes / t / 1e9, 4), "unit": "GB/s", "cores": cores,
+                  "cpu": model, "kind": "oracle",
+                  "sample": f"whole {leg.cfg.name} decode (every query head, every visible key), "
+                            f"fp64, median of {reps} run(s), {t:.3f} s each"}
+            if leg.kv_bytes < (256 << 20):  # the same sample on one core
+                t0 = time.perf_counter()
+                oracle.decode(q, k, v, lens, leg.cfg.scale, nthreads=1)
+                cb["value_1core"] = round(leg.kv_bytes / (time.perf_counter() - t0) / 1e9, 4)
+            o_gpu, l_gpu = results[id(leg)]
+            par = _parity(o_gpu, l_gpu, ref_o, ref_l, "every output row")
+        else:
+            q, k, v = leg.host
+            rows = leg.rows
+            t0 = time.perf_counter()
+            ref_o, ref_l = oracle.prefill_causal_rows(q, k, v, leg.cfg.scale, rows=rows,
+                                                      nthreads=cores)
+            t = time.perf_counter() - t0
+            fl = causal_flops(leg.cfg.d, leg.cfg.H_q, leg.cfg.B, rows.tolist())
+            cb = {"value": round(fl / t / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+                  "cpu": model, "kind": "oracle",
+                  "sample": f"{len(rows)} seeded query rows (rows 0 and S-1 included) x "
+                            f"{leg.cfg.H_q} heads of {leg.cfg.name}, fp64, {t:.3f} s; the rate "
+                            "counts the causal FLOPs of those rows only"}
+            o_gpu, l_gpu = results[id(leg)]
+            par = _parity(o_gpu, l_gpu, ref_o, ref_l, f"{len(rows)} sampled query rows x all heads")
+        out[name] = {"cpu_baseline": cb, "parity": par}
+        del ref_o, ref_l
+    return out
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: K timed steps of the whole decode workload on CPU."""
+    if rank != 0:
+        return None
+    import oracle
+    from gqa_attention_gb300 import inputs
+
+    oracle.build()
+    dc = inputs.LLAMA70B_DECODE
+    q, k, v, lens = inputs.decode_inputs_for(dc, seed=0)
+    kv_bytes = 2 * int(lens.sum()) * dc.H_kv * dc.d * 2
+    cores = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle.decode(q, k, v, lens, dc.scale, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode(q, k, v, lens, dc.scale, nthreads=cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = kv_bytes / dt / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded torch.randn, bf16)",
+        "config": {"workload": f"{dc.name} (value)", "l2": "n/a (CPU)",
+                   "parallelism": "CPU threads"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "cpu": cpu_model(), "kind": "oracle",
+                         "sample": f"whole {dc.name} decode per step (fp64 oracle)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
 
 
 # ---------------------------------------------------- further workloads ---
@@ -415,15 +844,32 @@ def run_workload(name, args):
     stream = torch.cuda.current_stream()
     hbm_gbs, bf16_tf, _, peak_kind = _peaks()
     steps = max(1, args.steps)
+    timer = GraphTimer(torch, stream, None)
 
-    def timed(fn):
-        for i in range(max(3, args.warmup)):
-            fn(i)
+    def timed(fn, copies=None):
+        fn(0, stream)
         torch.cuda.synchronize()
-        ms = _time_region(torch, fn, steps, stream)
+        tg = timer.prepare(fn, steps, copies, lead_out=1 if copies is not None else 0)
+        for i in range(max(3, args.warmup)):
+            fn(i, stream)
+        timer.warm(tg)
+        first, allv = timer.time_repeated(tg, REPEATS)
         if g.gqa_last_device_error(stream) != g.GQA_OK:
             raise RuntimeError("device error")
-        return ms
+        return first, _repeat_stats(allv)
+
+    if name in ("decode_tiny", "decode_ragged"):
+        cfg = inputs.TINY_DECODE if name == "decode_tiny" else inputs.LLAMA70B_DECODE_RAGGED
+        leg = DecodeLeg(torch, g, cfg, dev)
+        for c in range(leg.copies):
+            leg.step(c, stream)
+        ms, rep = timed(leg.step, leg.copies)
+        gbs = leg.kv_bytes / (ms * 1e-3) / 1e9
+        return {"metric": f"decode KV GB/s ({cfg.name})", "value": round(gbs, 2), "unit": "GB/s",
+                "ms_per_step": round(ms, 5), "repeats": rep, "steps": steps,
+                "n_split": leg.n_split, "kv_bytes": leg.kv_bytes,
+                "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
+                "l2": f"{leg.copies} rotating K/V copies", "dtype": "bf16", "data": "synthetic"}
 
     if name.startswith("decode_fp8"):
         cfg = inputs.LLAMA70B_DECODE if name == "decode_fp8" else inputs.LLAMA70B_DECODE_RAGGED
@@ -439,20 +885,23 @@ def run_workload(name, args):
         out = torch.empty(cfg.B, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
         lse = torch.empty(cfg.B, cfg.H_q, dtype=torch.float32, device=dev)
 
-        def fstep(i):
+        def fstep(i, s):
             kc, vc, ksc, vsc = caches[i % copies]
             assert g.gqa_attn_decode_fp8(qd, kc, vc, ksc, vsc, ld, cfg.B, cfg.S_max, cfg.H_q,
                                          cfg.H_kv, cfg.d, cfg.scale, n, ws, out, lse,
-                                         stream) == g.GQA_OK
+                                         s) == g.GQA_OK
             assert g.gqa_attn_decode_combine(ws, cfg.B, cfg.H_q, cfg.d, n, out, lse,
-                                             stream) == g.GQA_OK
+                                             s) == g.GQA_OK
 
-        ms = timed(fstep)
+        for c in range(copies):
+            fstep(c, stream)
+        ms, rep = timed(fstep, copies)
         gbs = kv_bytes / (ms * 1e-3) / 1e9
         bf16_equiv = 2 * int(lens.sum()) * cfg.H_kv * cfg.d * 2
         return {"metric": f"FP8-cache decode GB/s ({cfg.name})", "value": round(gbs, 2),
-                "unit": "GB/s", "ms_per_step": round(ms, 5), "steps": steps, "n_split": n,
-                "fp8_bytes": kv_bytes, "bf16_equivalent_GBs": round(bf16_equiv / (ms * 1e-3) / 1e9, 2),
+                "unit": "GB/s", "ms_per_step": round(ms, 5), "repeats": rep, "steps": steps,
+                "n_split": n, "fp8_bytes": kv_bytes,
+                "bf16_equivalent_GBs": round(bf16_equiv / (ms * 1e-3) / 1e9, 2),
                 "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
                 "l2": f"{copies} rotating cache copies",
                 "dtype": "e4m3 cache, bf16 q/out", "data": "synthetic"}
@@ -479,25 +928,28 @@ def run_workload(name, args):
         lse = torch.empty(cfg.B, T_q, cfg.H_q, dtype=torch.float32, device=dev)
         lse_c = torch.empty(cfg.B, cfg.H_q, T_q, dtype=torch.float32, device=dev)
 
-        def mstep(i):
+        def mstep(i, s):
             assert g.gqa_attn_decode_multi(qd, kds[i % nc], vds[i % nc], ld, cfg.B, T_q, cfg.S_max,
                                            cfg.H_q, cfg.H_kv, cfg.d, cfg.scale, n, ws, out, lse,
-                                           stream) == g.GQA_OK
+                                           s) == g.GQA_OK
             assert g.gqa_attn_decode_combine(ws, cfg.B * T_q, cfg.H_q, cfg.d, n, out, lse,
-                                             stream) == g.GQA_OK
+                                             s) == g.GQA_OK
 
-        def cstep(i):
+        def cstep(i, s):
             assert g.gqa_attn_prefill_chunk(qd, kds[i % nc], vds[i % nc], ld, cfg.B, T_q, cfg.S_max,
                                             cfg.H_q, cfg.H_kv, cfg.d, cfg.scale, -1, out, lse_c,
-                                            stream) == g.GQA_OK
+                                            s) == g.GQA_OK
 
-        ms = timed(mstep)
-        ms_chunk = timed(cstep)
+        for c in range(nc):
+            mstep(c, stream)
+        ms, rep = timed(mstep, nc)
+        ms_chunk, _ = timed(cstep, nc)
         gbs = kv_bytes / (ms * 1e-3) / 1e9
         return {"metric": f"multi-token decode KV GB/s ({cfg.name}, T_q={T_q})",
                 "value": round(gbs, 2),
-                "unit": "GB/s", "ms_per_step": round(ms, 5), "steps": steps, "n_split": n,
-                "kv_bytes": kv_bytes, "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
+                "unit": "GB/s", "ms_per_step": round(ms, 5), "repeats": rep, "steps": steps,
+                "n_split": n, "kv_bytes": kv_bytes,
+                "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
                 "chunked_prefill_ms_same_problem": round(ms_chunk, 5),
                 "l2": f"{nc} rotating K/V copies", "dtype": "bf16", "data": "synthetic"}
 
@@ -523,19 +975,21 @@ def run_workload(name, args):
         out = torch.empty(cfg.B, T_q, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
         lse = torch.empty(cfg.B, T_q, cfg.H_q, dtype=torch.float32, device=dev)
 
-        def pmstep(i):
+        def pmstep(i, s):
             assert g.gqa_attn_decode_paged_multi(qd, kps[i % nc], vps[i % nc], td, ld, cfg.B, T_q,
                                                  kp.shape[0], page, table.shape[1], cfg.H_q,
                                                  cfg.H_kv, cfg.d, cfg.scale, n, ws, out, lse,
-                                                 stream) == g.GQA_OK
+                                                 s) == g.GQA_OK
             assert g.gqa_attn_decode_combine(ws, cfg.B * T_q, cfg.H_q, cfg.d, n, out, lse,
-                                             stream) == g.GQA_OK
+                                             s) == g.GQA_OK
 
-        ms = timed(pmstep)
+        for c in range(nc):
+            pmstep(c, stream)
+        ms, rep = timed(pmstep, nc)
         gbs = kv_bytes / (ms * 1e-3) / 1e9
         return {"metric": f"paged multi-token decode KV GB/s ({cfg.name}, page {page}, T_q={T_q})",
                 "value": round(gbs, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
-                "steps": steps, "n_split": n, "kv_bytes": kv_bytes,
+                "repeats": rep, "steps": steps, "n_split": n, "kv_bytes": kv_bytes,
                 "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
                 "l2": f"{nc} rotating page pools", "dtype": "bf16", "data": "synthetic"}
 
@@ -554,49 +1008,22 @@ def run_workload(name, args):
         out = torch.empty(cfg.B, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
         lse = torch.empty(cfg.B, cfg.H_q, dtype=torch.float32, device=dev)
 
-        def pstep(i):
+        def pstep(i, s):
             assert g.gqa_attn_decode_paged(qd, kps[i % nc], vps[i % nc], td, ld, cfg.B, kp.shape[0],
                                            page, table.shape[1], cfg.H_q, cfg.H_kv, cfg.d,
-                                           cfg.scale, n, ws, out, lse, stream) == g.GQA_OK
+                                           cfg.scale, n, ws, out, lse, s) == g.GQA_OK
             assert g.gqa_attn_decode_combine(ws, cfg.B, cfg.H_q, cfg.d, n, out, lse,
-                                             stream) == g.GQA_OK
+                                             s) == g.GQA_OK
 
-        ms = timed(pstep)
+        for c in range(nc):
+            pstep(c, stream)
+        ms, rep = timed(pstep, nc)
         gbs = kv_bytes / (ms * 1e-3) / 1e9
         return {"metric": f"paged decode KV GB/s ({cfg.name}, page {page}, shuffled pages)",
                 "value": round(gbs, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
-                "steps": steps, "n_split": n, "kv_bytes": kv_bytes,
+                "repeats": rep, "steps": steps, "n_split": n, "kv_bytes": kv_bytes,
                 "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
                 "l2": f"{nc} rotating page pools", "dtype": "bf16", "data": "synthetic"}
-
-    if name.startswith("decode"):
-        cfg = inputs.TINY_DECODE if name == "decode_tiny" else inputs.LLAMA70B_DECODE_RAGGED
-        q, k, v, lens = inputs.decode_inputs_for(cfg, seed=0)
-        kv_bytes = 2 * int(lens.sum()) * cfg.H_kv * cfg.d * 2
-        copies = n_copies(kv_bytes)
-        qd, ld = q.to(dev), lens.to(dev)
-        kds = [k.to(dev) for _ in range(copies)]
-        vds = [v.to(dev) for _ in range(copies)]
-        n = g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, cfg.d)
-        ws = g.decode_workspace(cfg.B, cfg.H_q, cfg.d, n, dev)
-        out = torch.empty(cfg.B, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
-        lse = torch.empty(cfg.B, cfg.H_q, dtype=torch.float32, device=dev)
-
-        def step(i):
-            c = i % copies
-            assert g.gqa_attn_decode(qd, kds[c], vds[c], ld, cfg.B, cfg.S_max, cfg.H_q, cfg.H_kv,
-                                     cfg.d, cfg.scale, n, ws, out, lse, stream) == g.GQA_OK
-            if n > 1:
-                assert g.gqa_attn_decode_combine(ws, cfg.B, cfg.H_q, cfg.d, n, out, lse,
-                                                 stream) == g.GQA_OK
-
-        ms = timed(step)
-        gbs = kv_bytes / (ms * 1e-3) / 1e9
-        return {"metric": f"decode KV GB/s ({cfg.name})", "value": round(gbs, 2), "unit": "GB/s",
-                "ms_per_step": round(ms, 5), "steps": steps, "n_split": n, "kv_bytes": kv_bytes,
-                "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4),
-                "l2": f"{copies} rotating K/V copies",
-                "dtype": "bf16", "data": "synthetic"}
 
     # prefill workloads
     if name == "prefill_64k":
@@ -631,99 +1058,39 @@ def run_workload(name, args):
     ws = torch.empty(max(1, g.gqa_attn_prefill_chunk_workspace_bytes(B, T_q, H_q, d, n_part)),
                      dtype=torch.uint8, device=dev)
 
-    def step(i):
+    def step(i, s):
         if name == "prefill_64k":
-            st = g.gqa_attn_prefill_causal(qd, kd, vd, B, T_q, H_q, H_kv, d, scale, out, lse, stream)
+            st = g.gqa_attn_prefill_causal(qd, kd, vd, B, T_q, H_q, H_kv, d, scale, out, lse, s)
         else:
             st = g.gqa_attn_prefill_chunk_split(qd, kd, vd, lens, B, T_q, S_kv, H_q, H_kv, d, scale,
-                                                W, n_part, ws, out, lse, stream)
+                                                W, n_part, ws, out, lse, s)
         assert st == g.GQA_OK
 
-    ms = timed(step)
+    ms, rep = timed(step)
     tf = flops / (ms * 1e-3) / 1e12
     return {"metric": f"prefill TFLOPS ({label})", "value": round(tf, 2), "unit": "TFLOP/s",
-            "ms_per_step": round(ms, 4), "steps": steps, "flops_per_step": flops,
+            "ms_per_step": round(ms, 4), "repeats": rep, "steps": steps, "flops_per_step": flops,
             "n_part": n_part,
             "frac_of_" + peak_kind + "_bf16": round(tf / bf16_tf, 4), "dtype": "bf16",
             "data": "synthetic"}
 
 
-# ------------------------------------------------------ CPU oracle baseline --
-def cpu_baseline(args, steps=1):
-    """Time the fp64 oracle on the host cores on a bounded sample of the decode workload."""
-    import oracle
-    from gqa_attention_gb300 import inputs
-
-    oracle.build()
-    dc = inputs.LLAMA70B_DECODE
-    q, k, v, lens = inputs.decode_inputs_for(dc, seed=0)
-    kv_bytes = 2 * int(lens.sum()) * dc.H_kv * dc.d * 2
-    cores = os.cpu_count() or 1
-    times = []
-    for _ in range(max(1, steps)):
-        t0 = time.perf_counter()
-        oracle.decode(q, k, v, lens, dc.scale, nthreads=cores)
-        times.append(time.perf_counter() - t0)
-    t = statistics.median(times)
-    # the same sample on one core (the oracle's thread pool of one)
-    t0 = time.perf_counter()
-    oracle.decode(q, k, v, lens, dc.scale, nthreads=1)
-    t1 = time.perf_counter() - t0
-    return {"value": round(kv_bytes / t / 1e9, 4), "unit": "GB/s", "cores": cores,
-            "kind": "oracle",
-            "sample": f"whole {dc.name} decode (all 64 query heads, 32768 keys), fp64, "
-                      f"median of {len(times)} run(s), {t:.3f} s each",
-            "value_1core": round(kv_bytes / t1 / 1e9, 4)}
-
-
-def run_reference(args, rank, world):
-    """The oracle as the reference arm: K timed steps of the whole decode workload on CPU."""
-    if rank != 0:
-        return None
-    import oracle
-    from gqa_attention_gb300 import inputs
-
-    oracle.build()
-    dc = inputs.LLAMA70B_DECODE
-    q, k, v, lens = inputs.decode_inputs_for(dc, seed=0)
-    kv_bytes = 2 * int(lens.sum()) * dc.H_kv * dc.d * 2
-    cores = os.cpu_count() or 1
-    for _ in range(args.warmup):
-        oracle.decode(q, k, v, lens, dc.scale, nthreads=cores)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.decode(q, k, v, lens, dc.scale, nthreads=cores)
-    dt = (time.perf_counter() - t0) / args.steps
-    value = kv_bytes / dt / 1e9
-    return {
-        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded torch.randn, bf16)",
-        "config": {"workload": f"{dc.name} (value)", "l2": "n/a (CPU)",
-                   "parallelism": "CPU threads"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
-                         "kind": "oracle",
-                         "sample": f"whole {dc.name} decode per step (fp64 oracle)"},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
-    }
-
-
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=WORKLOADS, default=None,
                     help="measure one further workload instead of the headline step")
     ap.add_argument("--only", choices=["decode", "prefill"], default=None,
-                    help="run one leg only (for profiler captures); the JSON line is partial")
+                    help="run one leg of the headline step only (for profiler captures); "
+                         "the JSON line is partial")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    args.steps = max(1, args.steps)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
