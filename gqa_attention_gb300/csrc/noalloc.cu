@@ -4,10 +4,10 @@
 // followed by gqa_attn_decode_combine(), but keeps the split partials in a
 // fixed scratch array that lives in this library's device image instead of a
 // caller-provided workspace.  It exists for callers that must not call
-// cudaMalloc at decode time: code running inside a CUDA graph capture or a
-// custom allocator's critical section, or a serving process whose memory pool
-// is sized up front and may not grow.  Such callers still pass their own q,
-// K/V cache, seq_lens, out and lse buffers.
+// cudaMalloc at decode time: code running inside a custom allocator's critical
+// section (where a nested allocation would deadlock or recurse), or a serving
+// process whose device memory pool is sized up front and may not grow.  Such
+// callers still pass their own q, K/V cache, seq_lens, out and lse buffers.
 #include <mutex>
 
 #include "gqa_attn.h"
@@ -25,10 +25,13 @@ void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up once
 // per device with that device current.  In host code the array's name is
-// only a host-side stand-in, so the address must come from the runtime.
+// only a host-side stand-in, so the address must come from the runtime.  The
+// cached address belongs to the device's current context: after a
+// cudaDeviceReset() it is stale (see the header).
 gqa_status scratch_for_current_device(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return GQA_ERR_CUDA;
+  if (dev >= kMaxDevices) return GQA_ERR_UNSUPPORTED;  // ordinals past the address table
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;

@@ -199,10 +199,11 @@ gqa_status gqa_attn_decode_paged_fp8(const void* q, const void* k_pool, const vo
                                      void* out, float* lse, gqa_stream_t stream);
 
 /* Split-KV decode that allocates nothing, for callers that cannot call
- * cudaMalloc when they decode: code inside a CUDA graph capture or an
- * allocator's critical section, or a serving process whose device memory pool
- * is fixed up front.  The pages have no counterpart of this entry point; it is
- * a property of this library's interface.
+ * cudaMalloc when they decode: code running inside a custom allocator's
+ * critical section (a nested allocation there would deadlock or recurse), or
+ * a serving process whose device memory pool is fixed up front and may not
+ * grow.  The pages have no counterpart of this entry point; it is a property
+ * of this library's interface.
  *
  * Same arguments, layouts, checks and results as gqa_attn_decode() with the
  * same n_split followed by gqa_attn_decode_combine(), except that the split
@@ -214,8 +215,12 @@ gqa_status gqa_attn_decode_paged_fp8(const void* q, const void* k_pool, const vo
  *     (16777216 bytes) the call returns GQA_ERR_INVALID_ARG before any launch.
  *   - No cudaMalloc, cudaFree or other allocating call is made.  The first
  *     call with n_split > 1 on a device looks up the scratch array's device
- *     address (cudaGetSymbolAddress) with that device current; make that first
- *     call before any stream capture.
+ *     address (cudaGetSymbolAddress) with that device current and keeps it;
+ *     make that first call before any stream capture.  The kept address is
+ *     not valid after cudaDeviceReset() on that device: do not call this
+ *     entry point on a device that was reset after its first call.
+ *   - Devices with ordinal 64 or above return GQA_ERR_UNSUPPORTED (the
+ *     library keeps one address per device for ordinals 0..63).
  *   - Every call shares the one array per device and it keeps the previous
  *     call's contents.  Nothing in it needs to start at zero: each call writes
  *     every partial that its combine reads.  Calls whose kernels overlap on the

@@ -81,9 +81,11 @@ def test_partials_match_oracle_partials(oracle_mod):
     assert (np.isneginf(ml[..., 0]) == empty).all()
     assert (ml[..., 1][empty] == 0).all()
     ne = ~empty
-    # per-split LSE and normalised output (independent of the reference point m)
-    np.testing.assert_allclose((ml[..., 0] + np.log(ml[..., 1]))[ne], (m + np.log(l))[ne], atol=1e-3)
-    np.testing.assert_allclose((Og / ml[..., 1:2])[ne], (O / l[..., None])[ne], atol=1e-2)
+    # per-split LSE and normalised output (independent of the reference point
+    # m), over the non-empty splits only (an empty split has l = 0)
+    np.testing.assert_allclose(ml[..., 0][ne] + np.log(ml[..., 1][ne]), m[ne] + np.log(l[ne]),
+                               atol=1e-3)
+    np.testing.assert_allclose(Og[ne] / ml[..., 1][ne][:, None], O[ne] / l[ne][:, None], atol=1e-2)
 
 
 def test_combine_merges_arbitrary_partials(oracle_mod):
