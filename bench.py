@@ -808,7 +808,7 @@ def run_reference(args, rank, world):
 WORKLOADS = ("decode_tiny", "decode_ragged", "decode_paged16", "decode_paged128", "decode_fp8",
              "decode_fp8_ragged", "decode_multi2", "decode_multi4", "decode_multi8", "decode_multi16",
              "decode_paged16_multi8", "decode_paged128_multi8", "prefill_64k", "prefill_window",
-             "prefill_chunk")
+             "prefill_chunk", "prefill_d64", "prefill_d32")
 
 
 def _shuffled_pages(k, v, page_size, seed):
@@ -1031,6 +1031,12 @@ def run_workload(name, args):
         q, k, v = inputs.prefill_inputs_for(cfg, seed=0)
         B, T_q, S_kv, H_q, H_kv, d, W, L = cfg.B, cfg.S, cfg.S, cfg.H_q, cfg.H_kv, cfg.d, -1, cfg.S
         label = cfg.name
+    elif name in ("prefill_d64", "prefill_d32"):
+        # the Llama3-70B-shaped 8K causal prefill at a smaller head dimension
+        d = 64 if name == "prefill_d64" else 32
+        B, T_q, S_kv, H_q, H_kv, W, L = 1, 8192, 8192, 64, 8, -1, 8192
+        q, k, v = inputs.prefill_inputs(B, T_q, H_q, H_kv, d, seed=0)
+        label = f"prefill_causal_s8192_hq64_hkv8_d{d}"
     elif name == "prefill_window":
         cfg = inputs.LLAMA70B_PREFILL_8K
         q, k, v = inputs.prefill_inputs_for(cfg, seed=0)
@@ -1053,13 +1059,13 @@ def run_workload(name, args):
     vis = (a + 1) if W < 0 else torch.minimum(a, torch.full_like(a, W)) + 1
     flops = 4.0 * d * H_q * B * float(vis.sum())
 
-    n_part = 1 if name == "prefill_64k" else g.gqa_attn_prefill_chunk_default_parts(
-        B, T_q, S_kv, H_q, H_kv)
+    causal_only = name in ("prefill_64k", "prefill_d64", "prefill_d32")
+    n_part = 1 if causal_only else g.gqa_attn_prefill_chunk_default_parts(B, T_q, S_kv, H_q, H_kv)
     ws = torch.empty(max(1, g.gqa_attn_prefill_chunk_workspace_bytes(B, T_q, H_q, d, n_part)),
                      dtype=torch.uint8, device=dev)
 
     def step(i, s):
-        if name == "prefill_64k":
+        if causal_only:
             st = g.gqa_attn_prefill_causal(qd, kd, vd, B, T_q, H_q, H_kv, d, scale, out, lse, s)
         else:
             st = g.gqa_attn_prefill_chunk_split(qd, kd, vd, lens, B, T_q, S_kv, H_q, H_kv, d, scale,

@@ -557,7 +557,7 @@ gqa_status run_prefill(bool chunk, const void* q, const void* k, const void* v,
     return GQA_ERR_INVALID_ARG;
   if ((long long)B * S * H_q > 0x7fffffffLL || (long long)B * S_kv > 0x7fffffffLL)
     return GQA_ERR_INVALID_ARG;
-  if (d != 128) return GQA_ERR_UNSUPPORTED;
+  if (!head_dim_ok(d)) return GQA_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
       !aligned(lse, 4) || (seq_lens && !aligned(seq_lens, 4)))
     return GQA_ERR_INVALID_ARG;
@@ -566,7 +566,9 @@ gqa_status run_prefill(bool chunk, const void* q, const void* k, const void* v,
   if (st != GQA_OK) return st;
 
   // Q viewed as [B][S][H_q][d] with boxes of 128 rows of one head, 64 elements
-  // wide (two boxes per 128-wide row), 128-byte swizzle; K and V likewise.
+  // wide (two boxes per 128-wide row), 128-byte swizzle; K and V likewise.  For
+  // d = 32 the 64-element box is wider than the tensor: TMA fills elements
+  // 32..63 with zeros, the padding the kernel's 64-wide tiles expect.
   const uint64_t dq[4] = {(uint64_t)d, (uint64_t)H_q, (uint64_t)S, (uint64_t)B};
   const uint64_t sq[3] = {(uint64_t)d * 2, (uint64_t)H_q * d * 2, (uint64_t)S * H_q * d * 2};
   const uint64_t dk[4] = {(uint64_t)d, (uint64_t)H_kv, (uint64_t)S_kv, (uint64_t)B};

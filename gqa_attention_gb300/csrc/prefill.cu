@@ -26,11 +26,18 @@
 //   warps 2-3   idle.
 //   warps 4-7   softmax + epilogue of head A (thread = one query row).
 //   warps 8-11  softmax + epilogue of head B.
-// Tensor memory (512 columns x 128 lanes, fp32): S_A | S_B | O_A | O_B; P_X
-// (bf16, two per column) overwrites the first 64 columns of S_X once S_X has
-// been read, and is the tensor-memory A operand of O_X += P_X V.
-// Shared memory: Q_A, Q_B and five K/V slots, 32 KB each, every tile stored as
-// two 128-row x 128-byte halves with the 128-byte swizzle.
+// Tensor memory (512 columns x 128 lanes, fp32): S_A | S_B (128 columns each)
+// | O_A | O_B (DP columns each); P_X (bf16, two per column) overwrites the
+// first 64 columns of S_X once S_X has been read, and is the tensor-memory A
+// operand of O_X += P_X V.
+// Shared memory: Q_A, Q_B and the K/V slots, every tile stored as DP/64
+// halves of 128 rows x 128 bytes with the 128-byte swizzle.
+//
+// Head dimensions: DP = 128 serves d = 128 (five K/V slots of 32 KB); DP = 64
+// serves d = 64 (ten slots of 16 KB) and d = 32, whose tiles are loaded as
+// 64-element boxes over a 32-element-wide tensor: TMA fills columns 32..63 with
+// zeros, which add nothing to Q K^T and give zero columns of O that are never
+// stored.
 //
 // O is rescaled only when a row's running maximum grows by more than 2^8
 // (base 2); p = 2^(x - m_ref) then stays <= 2^8, and because l and O always
@@ -44,12 +51,18 @@ namespace gqa {
 namespace {
 
 constexpr int kPThreads = 384;
-constexpr int kSlots = 5;
-constexpr uint32_t kTileB = 128u * 128u * 2u;  // one 128 x 128 bf16 tile
-constexpr uint32_t kHalfB = kTileB / 2;        // 128 rows x 128 bytes
-constexpr uint32_t kOffQ = 0;                  // Q_A, Q_B
-constexpr uint32_t kOffRing = 2 * kTileB;      // K/V slots
-constexpr uint32_t kPrefillSmem = kOffRing + kSlots * kTileB + 1024;
+// Shared-memory layout for tiles of 128 rows x DP bf16 columns (DP = 64 or 128).
+template <int DP>
+struct PrefillLayout {
+  static_assert(DP == 64 || DP == 128, "padded head width");
+  static constexpr int kSlots = DP == 128 ? 5 : 10;         // K/V ring slots
+  static constexpr int kHalves = DP / 64;                    // 128-byte-wide halves per tile
+  static constexpr uint32_t kHalfB = 128u * 128u;            // 128 rows x 128 bytes
+  static constexpr uint32_t kTileB = kHalves * kHalfB;       // one 128 x DP tile
+  static constexpr uint32_t kOffQ = 0;                       // Q_A, Q_B
+  static constexpr uint32_t kOffRing = 2 * kTileB;           // K/V slots
+  static constexpr uint32_t kSmem = kOffRing + kSlots * kTileB + 1024;
+};
 constexpr float kRescaleLog2 = 8.f;
 // Registers per thread: 168 at launch (384 threads, one CTA per SM); warps
 // 0-3 (TMA, MMA, idle) give theirs up to the two softmax warpgroups.
@@ -121,11 +134,15 @@ __device__ __forceinline__ Geom item_geom(const PrefillParams& p, const Item& it
   return g;
 }
 
-template <bool GENERAL>
+template <bool GENERAL, int DP>
 __global__ void __launch_bounds__(kPThreads, 1)
     gqa_prefill_causal_kernel(const __grid_constant__ CUtensorMap tm_q,
                               const __grid_constant__ CUtensorMap tm_k,
                               const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  using Lay = PrefillLayout<DP>;
+  constexpr int kSlots = Lay::kSlots;
+  constexpr uint32_t kTileB = Lay::kTileB, kHalfB = Lay::kHalfB;
+  constexpr uint32_t kOffQ = Lay::kOffQ, kOffRing = Lay::kOffRing;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full, q_empty, drain;
   __shared__ __align__(8) uint64_t slot_full[kSlots], slot_empty[kSlots];
@@ -209,7 +226,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (q_iter > 0 && !wait(&q_empty, (q_iter - 1) & 1)) break;
           const uint32_t qb = smem_u32(&q_full);
           mbar_arrive_expect_tx(qb, pair ? 2 * kTileB : kTileB);
-          for (int dh = 0; dh < 2; ++dh) {
+          for (int dh = 0; dh < Lay::kHalves; ++dh) {
             tma_load_4d(sb + kOffQ + dh * kHalfB, &tm_q, qb, dh * 64, hA, it.qt * 128, it.b);
             if (pair)
               tma_load_4d(sb + kOffQ + kTileB + dh * kHalfB, &tm_q, qb, dh * 64, hA + 1,
@@ -227,7 +244,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
               const uint32_t fb = smem_u32(&slot_full[slot]);
               mbar_arrive_expect_tx(fb, kTileB);
               const CUtensorMap* m = t == 0 ? &tm_k : &tm_v;
-              for (int dh = 0; dh < 2; ++dh)
+              for (int dh = 0; dh < Lay::kHalves; ++dh)
                 tma_load_4d(sb + kOffRing + slot * kTileB + dh * kHalfB, m, fb, dh * 64, it.kv,
                             (gm.j0 + j) * 128, it.b);
               ++ring;
@@ -243,11 +260,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
       // ------------------------------------------------- MMA issuer (warp 1) --
       {
         constexpr uint32_t idS = instr_desc_bf16_f32(128, 128, false);
-        constexpr uint32_t idPV = instr_desc_bf16_f32(128, 128, true);
-        auto issue_s = [&](int x, uint32_t slot) {  // S_x = Q_x K^T
+        constexpr uint32_t idPV = instr_desc_bf16_f32(128, DP, true);
+        auto issue_s = [&](int x, uint32_t slot) {  // S_x = Q_x K^T, K = DP in steps of 16
           const uint32_t qa = sb + kOffQ + x * kTileB, kb = sb + kOffRing + slot * kTileB;
   #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
+          for (int kk = 0; kk < DP / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kHalfB + (kk & 3) * 32;
             tc_mma_ss(tmem + 128 * x, smem_desc_sw128(qa + off, 16, 1024),
                       smem_desc_sw128(kb + off, 16, 1024), idS, kk > 0);
@@ -257,7 +274,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           const uint32_t vb = sb + kOffRing + slot * kTileB;
   #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            tc_mma_ts(tmem + 256 + 128 * x, tmem + 128 * x + 8 * kk,
+            tc_mma_ts(tmem + 256 + DP * x, tmem + 128 * x + 8 * kk,
                       smem_desc_sw128(vb + kk * 2048, kHalfB, 1024), idPV, (acc || kk > 0) ? 1 : 0);
         };
         uint32_t ring = 0, q_iter = 0, pr_ph[2] = {0, 0}, oe_ph[2] = {0, 0};
@@ -346,7 +363,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_base + 128 * x;
-    const uint32_t tO = tmem + lane_base + 256 + 128 * x;
+    const uint32_t tO = tmem + lane_base + 256 + DP * x;
+    const int n_oc = p.d / 32;  // 32-column chunks of O that are stored
     const float c2 = p.scale_log2;
     uint32_t s_ph = 0, of_ph = 0;
     uint32_t ring_base = 0;  // ring position of this item's K_0 (chunk mode bookkeeping)
@@ -457,7 +475,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // P V is issued only after p_ready below.
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < n_oc; ++c) {
             uint32_t o[32];
             tmem_ld32(tO + 32 * c, o);
             tmem_wait_ld();
@@ -485,7 +503,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (128 * jt + r >= L_eff) {
               const uint32_t row = sb + kOffRing + (pos % kSlots) * kTileB + r * 128;
 #pragma unroll
-              for (int hh = 0; hh < 2; ++hh)
+              for (int hh = 0; hh < Lay::kHalves; ++hh)
 #pragma unroll
                 for (int c16 = 0; c16 < 8; ++c16) st_shared_v4(row + hh * kHalfB + c16 * 16, 0, 0, 0, 0);
             }
@@ -507,18 +525,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const bool store = q_row < p.S;
       if (GENERAL && gm.bad && x == 0 && warp == 4 && lane == 0) atomicOr(p.err, kErrBadSeqLen);
       const bool split = GENERAL && p.n_part > 1;
+      const int D = p.d;  // row width of out and of the O partials
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < n_oc; ++c) {
         uint32_t o[32];
         tmem_ld32(tO + 32 * c, o);
         tmem_wait_ld();
         reg_fence32(o);
-        if (split && store && !in_bounds((ws_row * p.n_part + it.part) * 128 + 32 * c, 32,
-                                         n_rows * p.n_part * 128, p.err))
+        if (split && store && !in_bounds((ws_row * p.n_part + it.part) * D + 32 * c, 32,
+                                         n_rows * p.n_part * D, p.err))
           continue;
         if (split && store) {  // this part's unnormalised O, fp32
-          // (the workspace is 256-byte aligned, a partial row 512 bytes)
-          float* d = p.ws_O + (ws_row * p.n_part + it.part) * 128 + 32 * c;
+          // (the workspace is 256-byte aligned, a partial row 4 D >= 128 bytes)
+          float* d = p.ws_O + (ws_row * p.n_part + it.part) * D + 32 * c;
 #pragma unroll
           for (int v = 0; v < 4; ++v)
             st_global_v8(d + 8 * v, o[8 * v], o[8 * v + 1], o[8 * v + 2], o[8 * v + 3], o[8 * v + 4],
@@ -556,8 +575,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
           for (int v = 0; v < 4; ++v) {  // u[v]: unit t of the quad's row v
             const int qrow = it.qt * 128 + quarter * 32 + (lane & ~3) + v;
             const size_t orow = (static_cast<size_t>(it.b) * p.S + qrow) * p.H_q + h;
-            if (qrow < p.S && in_bounds(orow * 128 + 32 * c + 8 * t, 8, n_rows * 128, p.err))
-              *reinterpret_cast<uint4*>(p.out + orow * 128 + 32 * c + 8 * t) =
+            if (qrow < p.S && in_bounds(orow * D + 32 * c + 8 * t, 8, n_rows * D, p.err))
+              *reinterpret_cast<uint4*>(p.out + orow * D + 32 * c + 8 * t) =
                   make_uint4(u[v][0], u[v][1], u[v][2], u[v][3]);
           }
         }
@@ -583,36 +602,53 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
 }
 
-template <bool GENERAL>
-cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                           const CUtensorMap& tm_v, int num_sms, cudaStream_t stream) {
+template <bool GENERAL, int DP>
+cudaError_t launch_prefill_dp(const PrefillParams& p, const CUtensorMap& tm_q,
+                              const CUtensorMap& tm_k, const CUtensorMap& tm_v, int num_sms,
+                              cudaStream_t stream) {
   static unsigned char attr_done[64];
+  constexpr uint32_t smem = PrefillLayout<DP>::kSmem;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  auto kern = gqa_prefill_causal_kernel<GENERAL>;
+  auto kern = gqa_prefill_causal_kernel<GENERAL, DP>;
   if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrefillSmem);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = 1;
   }
   const long long n_items =
       (long long)((p.S + 127) / 128) * p.B * p.H_kv * ((p.G + 1) / 2) * (GENERAL ? p.n_part : 1);
   const int grid = (int)(n_items < num_sms ? n_items : num_sms);
-  kern<<<grid, kPThreads, kPrefillSmem, stream>>>(tm_q, tm_k, tm_v, p);
+  kern<<<grid, kPThreads, smem, stream>>>(tm_q, tm_k, tm_v, p);
   return cudaGetLastError();
+}
+
+// d = 128 on 128-wide tiles; d = 64 and d = 32 on 64-wide tiles (d = 32 zero-padded by TMA).
+template <bool GENERAL>
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                           const CUtensorMap& tm_v, int num_sms, cudaStream_t stream) {
+  switch (p.d) {
+    case 128: return launch_prefill_dp<GENERAL, 128>(p, tm_q, tm_k, tm_v, num_sms, stream);
+    case 64:
+    case 32: return launch_prefill_dp<GENERAL, 64>(p, tm_q, tm_k, tm_v, num_sms, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // Folds the n_part partials of every (b, i, h) row of a split chunk prefill
 // (the associative merge of "Attention Kernel 계보" p.4): one warp per row,
-// four columns per lane.  A part whose rows saw no key is the identity
-// (m = -inf, l = 0); a NaN partial (bad sequence length) makes the row NaN.
+// four of the row's d columns per lane (lanes past d / 4 only help with the
+// weights).  A part whose rows saw no key is the identity (m = -inf, l = 0); a
+// NaN partial (bad sequence length) makes the row NaN.
 __global__ void __launch_bounds__(256) gqa_prefill_merge_kernel(const PrefillParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t rows = static_cast<size_t>(p.B) * p.S * p.H_q;
   const size_t row = static_cast<size_t>(blockIdx.x) * 8 + warp;
   if (row >= rows) return;
   const int P = p.n_part;
+  const int D = p.d;
+  const bool cols = lane * 4 < D;
   float M = -INFINITY;
   bool bad = false;
   for (int q = 0; q < P; ++q) {
@@ -628,7 +664,8 @@ __global__ void __launch_bounds__(256) gqa_prefill_merge_kernel(const PrefillPar
     if (ml.x == -INFINITY) continue;  // never written O is not read
     const float w = exp2f(ml.x - ref);
     L += w * ml.y;
-    const float4 o = reinterpret_cast<const float4*>(p.ws_O + (row * P + q) * 128)[lane];
+    const float4 o = cols ? reinterpret_cast<const float4*>(p.ws_O + (row * P + q) * D)[lane]
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
     acc.x += w * o.x;
     acc.y += w * o.y;
     acc.z += w * o.z;
@@ -639,8 +676,8 @@ __global__ void __launch_bounds__(256) gqa_prefill_merge_kernel(const PrefillPar
   uint2 packed;
   packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
   packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  if (in_bounds(row * 128 + lane * 4, 4, rows * 128, p.err))
-    reinterpret_cast<uint2*>(p.out + row * 128)[lane] = packed;
+  if (cols && in_bounds(row * D + lane * 4, 4, rows * D, p.err))
+    reinterpret_cast<uint2*>(p.out + row * D)[lane] = packed;
   if (lane == 0) {
     const int h = static_cast<int>(row % p.H_q);
     const size_t bi = row / p.H_q;

@@ -238,10 +238,11 @@ gqa_status gqa_attn_decode_noalloc(const void* q, const void* k_cache, const voi
  * diagonal are never loaded; only diagonal tiles are masked.
  *   q     device bf16 [B, S, H_q, d]     read only
  *   k, v  device bf16 [B, S, H_kv, d]    read only
- *   H_q % H_kv == 0, d == 128, S >= 1, B >= 1, scale finite > 0
+ *   H_q % H_kv == 0, d in {32, 64, 128}, S >= 1, B >= 1, scale finite > 0
  *   out   device bf16 [B, S, H_q, d]
  *   lse   device fp32 [B, H_q, S]
- */
+ * GQA_ERR_UNSUPPORTED for any other d.  d = 32 runs on the d = 64 tiles with
+ * the unused columns zero (the same result, at the d = 64 cost). */
 gqa_status gqa_attn_prefill_causal(const void* q, const void* k, const void* v, int B, int S,
                                    int H_q, int H_kv, int d, float scale, void* out, float* lse,
                                    gqa_stream_t stream);
@@ -260,7 +261,7 @@ gqa_status gqa_attn_prefill_causal(const void* q, const void* k, const void* v, 
  *   seq_lens  device int32 [B] with T_q <= L_b <= S_max, or NULL (every L_b =
  *             S_max).  A bad L_b is caught on the device: that sequence's
  *             rows are NaN and the GQA_ERR_INVALID_ARG error bit is set.
- *   H_q % H_kv == 0, d == 128, 1 <= T_q <= S_max, scale finite > 0
+ *   H_q % H_kv == 0, d in {32, 64, 128}, 1 <= T_q <= S_max, scale finite > 0
  *   out       device bf16 [B, T_q, H_q, d]
  *   lse       device fp32 [B, H_q, T_q]
  * With seq_lens == NULL, T_q == S_max and window < 0 this is exactly

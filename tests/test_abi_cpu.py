@@ -110,8 +110,9 @@ def test_multi_token_row_limits_and_splits(lib):
 def test_combine_and_prefill_reject_bad_arguments(lib):
     assert g.gqa_attn_decode_combine(None, 1, 8, 128, 2, FAKE, FAKE, stream=0) == g.GQA_ERR_INVALID_ARG
     assert g.gqa_attn_decode_combine(FAKE, 1, 8, 96, 2, FAKE, FAKE, stream=0) == g.GQA_ERR_UNSUPPORTED
-    assert g.gqa_attn_prefill_causal(FAKE, FAKE, FAKE, 1, 128, 8, 2, 64, 0.1, FAKE, FAKE,
-                                     stream=0) == g.GQA_ERR_UNSUPPORTED
+    for d in (16, 96, 256):  # prefill serves d in {32, 64, 128}
+        assert g.gqa_attn_prefill_causal(FAKE, FAKE, FAKE, 1, 128, 8, 2, d, 0.1, FAKE, FAKE,
+                                         stream=0) == g.GQA_ERR_UNSUPPORTED
     assert g.gqa_attn_prefill_causal(FAKE, FAKE, FAKE, 1, 128, 8, 3, 128, 0.1, FAKE, FAKE,
                                      stream=0) == g.GQA_ERR_INVALID_ARG
     assert g.gqa_attn_prefill_causal(FAKE, None, FAKE, 1, 128, 8, 2, 128, 0.1, FAKE, FAKE,

@@ -27,11 +27,11 @@ def _lib():
     assert g.gqa_last_device_error() == g.GQA_OK
 
 
-def _chunk_inputs(B, T_q, S_max, H_q, H_kv, lens, seed):
+def _chunk_inputs(B, T_q, S_max, H_q, H_kv, lens, seed, d=128):
     gen = torch.Generator().manual_seed(seed)
-    q = torch.randn(B, T_q, H_q, 128, generator=gen).to(torch.bfloat16)
-    k = torch.randn(B, S_max, H_kv, 128, generator=gen).to(torch.bfloat16)
-    v = torch.randn(B, S_max, H_kv, 128, generator=gen).to(torch.bfloat16)
+    q = torch.randn(B, T_q, H_q, d, generator=gen).to(torch.bfloat16)
+    k = torch.randn(B, S_max, H_kv, d, generator=gen).to(torch.bfloat16)
+    v = torch.randn(B, S_max, H_kv, d, generator=gen).to(torch.bfloat16)
     for b, L in enumerate(lens):  # rows past each sequence must never be read
         k[b, L:] = float("nan")
         v[b, L:] = float("nan")
@@ -55,6 +55,29 @@ def test_chunk_small_shapes(oracle_mod, T_q, S_max, lens, window):
                                                  window=window)
     out, lse = _gpu(q, k, v, sl, window)
     assert_parity(out, lse, ref_o, ref_l, f"T_q={T_q} S_max={S_max} lens={lens} W={window}")
+
+
+@pytest.mark.parametrize("d", [64, 32])
+@pytest.mark.parametrize("T_q,S_max,lens", [(5, 300, [5, 299]), (200, 1000, [777, 1000]),
+                                             (300, 300, [300, 300])])
+@pytest.mark.parametrize("window", [-1, 0, 127, 300])
+def test_chunk_small_head_dims(oracle_mod, T_q, S_max, lens, window, d):
+    q, k, v, sl = _chunk_inputs(2, T_q, S_max, 8, 2, lens, seed=T_q + window + d, d=d)
+    ref_o, ref_l = oracle_mod.prefill_chunk_rows(q, k, v, 1 / math.sqrt(d), seq_lens=sl,
+                                                 window=window)
+    out, lse = _gpu(q, k, v, sl, window)
+    assert_parity(out, lse, ref_o, ref_l, f"d={d} T_q={T_q} lens={lens} W={window}")
+
+
+@pytest.mark.parametrize("d", [64, 32])
+@pytest.mark.parametrize("n_part", [2, 3])
+def test_chunk_split_parts_small_head_dims(oracle_mod, d, n_part):
+    q, k, v, sl = _chunk_inputs(2, 200, 3000, 4, 2, [3000, 700], seed=11 + d, d=d)
+    ref_o, ref_l = oracle_mod.prefill_chunk_rows(q, k, v, 1 / math.sqrt(d), seq_lens=sl,
+                                                 window=-1)
+    out, lse = g.prefill_chunk(q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV), n_part=n_part)
+    torch.cuda.synchronize()
+    assert_parity(out.cpu(), lse.cpu(), ref_o, ref_l, f"d={d} n_part={n_part}")
 
 
 @pytest.mark.parametrize("H_q,H_kv", [(2, 2), (3, 1)])
@@ -88,8 +111,8 @@ def test_chunk_rejects_bad_host_arguments():
     x = torch.empty(16, dtype=torch.bfloat16, device=DEV)
     st = g.gqa_attn_prefill_chunk(x, x, x, None, 1, 300, 200, 8, 2, 128, 0.1, -1, x, x)
     assert st == g.GQA_ERR_INVALID_ARG  # T_q > S_max
-    st = g.gqa_attn_prefill_chunk(x, x, x, None, 1, 10, 200, 8, 2, 64, 0.1, -1, x, x)
-    assert st == g.GQA_ERR_UNSUPPORTED  # d != 128
+    st = g.gqa_attn_prefill_chunk(x, x, x, None, 1, 10, 200, 8, 2, 96, 0.1, -1, x, x)
+    assert st == g.GQA_ERR_UNSUPPORTED  # d not in {32, 64, 128}
 
 
 def test_sliding_window_prefill_8k_sampled_rows(oracle_mod):

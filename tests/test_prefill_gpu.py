@@ -37,14 +37,25 @@ def _gpu(q, k, v, scale=None):
     return out.cpu(), lse.cpu()
 
 
+@pytest.mark.parametrize("d", [128, 64, 32])
 @pytest.mark.parametrize("S", [1, 17, 128, 129, 300, 512])
 @pytest.mark.parametrize("H_q,H_kv", [(8, 2), (2, 2), (6, 2), (3, 1)])
-def test_small_shapes_all_rows(oracle_mod, S, H_q, H_kv):
+def test_small_shapes_all_rows(oracle_mod, S, H_q, H_kv, d):
     B = 2 if S <= 300 else 1
-    q, k, v = inputs.prefill_inputs(B, S, H_q, H_kv, 128, seed=S + H_q)
-    ref_o, ref_l = oracle_mod.prefill_causal_rows(q, k, v, 1 / math.sqrt(128))
+    q, k, v = inputs.prefill_inputs(B, S, H_q, H_kv, d, seed=S + H_q + d)
+    ref_o, ref_l = oracle_mod.prefill_causal_rows(q, k, v, 1 / math.sqrt(d))
     out, lse = _gpu(q, k, v)
-    assert_parity(out, lse, ref_o, ref_l, f"S={S} H_q={H_q} H_kv={H_kv}")
+    assert_parity(out, lse, ref_o, ref_l, f"S={S} H_q={H_q} H_kv={H_kv} d={d}")
+
+
+@pytest.mark.parametrize("d", [64, 32])
+def test_small_head_dims_several_query_tiles_and_heads(oracle_mod, d):
+    # 9 query tiles (ragged tail), G = 5 (two head pairs and a lone head),
+    # B = 2: the d < 128 tiles through every scheduling path
+    q, k, v = inputs.prefill_inputs(2, 1100, 10, 2, d, seed=d)
+    ref_o, ref_l = oracle_mod.prefill_causal_rows(q, k, v, 1 / math.sqrt(d))
+    out, lse = _gpu(q, k, v)
+    assert_parity(out, lse, ref_o, ref_l, f"d={d}")
 
 
 def test_non_default_scale_and_value_range(oracle_mod):
@@ -54,11 +65,12 @@ def test_non_default_scale_and_value_range(oracle_mod):
     assert_parity(out, lse, ref_o, ref_l, "scale=0.05")
 
 
-def test_large_scores_trigger_rescaling(oracle_mod):
+@pytest.mark.parametrize("d", [128, 64, 32])
+def test_large_scores_trigger_rescaling(oracle_mod, d):
     # Every query shares a direction u and the keys move along u with their
     # position, so each row's running maximum keeps rising (by ~40 in base-2
     # units over the sequence): the lazy O rescale path runs many times.
-    B, S, H_q, H_kv, d = 1, 640, 2, 1, 128
+    B, S, H_q, H_kv = 1, 640, 2, 1
     q, k, v = inputs.prefill_inputs(B, S, H_q, H_kv, d, seed=4)
     gen = torch.Generator().manual_seed(5)
     u = torch.randn(d, generator=gen)
@@ -72,8 +84,9 @@ def test_large_scores_trigger_rescaling(oracle_mod):
     assert_parity(out, lse, ref_o, ref_l, "rescale")
 
 
-def test_deterministic_and_in_bounds():
-    B, S, H_q, H_kv, d = 1, 384, 8, 2, 128
+@pytest.mark.parametrize("d", [128, 64, 32])
+def test_deterministic_and_in_bounds(d):
+    B, S, H_q, H_kv = 1, 384, 8, 2
     q, k, v = inputs.prefill_inputs(B, S, H_q, H_kv, d, seed=1)
     pad = 1 << 16
     n_o, n_l = B * S * H_q * d, B * H_q * S
