@@ -29,6 +29,12 @@ namespace {
 #ifndef GQA_DECODE_STAGES_FP8
 #define GQA_DECODE_STAGES_FP8 3  // FP8 stages are half as large as bf16 ones
 #endif
+#ifndef GQA_DECODE_STAGES_FP8_ONE_WAVE
+#define GQA_DECODE_STAGES_FP8_ONE_WAVE 8  // FP8, every CTA has an SM to itself
+#endif
+#ifndef GQA_FP8_ONE_WAVE_GROUPS
+#define GQA_FP8_ONE_WAVE_GROUPS 2  // consumer groups of the one-wave FP8 CTAs
+#endif
 
 #ifndef GQA_DECODE_FUSED_STAGES_D128
 #define GQA_DECODE_FUSED_STAGES_D128 3
@@ -182,13 +188,21 @@ __device__ __forceinline__ float online_update(float (&x)[4], float& m, float& l
 // Two CTAs per SM; three for the FP8 cache with G <= 8, whose sweep is bound
 // by its per-tile integer work (E4M3 conversion, byte transposes) rather than
 // by HBM, so it gains from more warps at 128 registers.
-template <int D, bool ROWS16, int NSTAGE, bool PAGED, bool FP8, bool CLUSTER>
-__global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
+// NGRP = 2 (FP8 with one CTA per SM): two groups of four consumer warps take
+// alternate tiles, so that each SM has two warps per scheduler to hide the
+// latency of the per-tile E4M3 work; the eight warp partials are merged at
+// the end as the four are otherwise.
+template <int D, bool ROWS16, int NSTAGE, bool PAGED, bool FP8, bool CLUSTER, int NGRP = 1>
+__global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
+                                  NGRP > 1 ? 1 : ((FP8 && !ROWS16) ? 3 : 2))
     gqa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v,
                             const __grid_constant__ CUtensorMap tm_ks,
                             const __grid_constant__ CUtensorMap tm_vs, const DecodeParams p) {
   static_assert(!(CLUSTER && (PAGED || FP8)), "the cluster merge serves the contiguous bf16 cache");
+  static_assert(NGRP == 1 || (NGRP <= 3 && !CLUSTER), "several consumer groups: split CTAs only");
+  constexpr int kCW = kConsumerWarps * NGRP;  // consumer warps
+  constexpr int kThr = (kCW + 1) * 32;
   using Lay = DecodeLayout<D>;
   using F8 = Fp8Layout<D>;
   constexpr int kStageBytes = FP8 ? F8::kStageBytes : Lay::kStageBytes;
@@ -199,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
   __shared__ int abort_flag;
   __shared__ int bad_page;
   __shared__ int pages_sm[PAGED ? kMaxPagesPerCta : 1];
+
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -230,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
   // A prefetch hands no data to the kernel and L2 is where writes become
   // coherent, so it cannot expose stale values; at worst it fetches rows the
   // split will not use.
-  if (p.prefetch_tiles > 0 && warp == kConsumerWarps && rg == 0) {
+  if (p.prefetch_tiles > 0 && warp == kCW && rg == 0) {
     int L_hint;
     asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(L_hint) : "l"(p.seq_lens + b));
     if (lane == 0) {
@@ -277,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
   // ---- device-side argument check and empty splits (no pipeline needed) ----
   if (L < p.T_q || L > p.S_max || L < 1) {
     if (threadIdx.x == 0 && split == 0 && kv == 0 && rg == 0) atomicOr(p.err, kErrBadSeqLen);
-    for (int e = threadIdx.x; e < R * D; e += kThreads) {
+    for (int e = threadIdx.x; e < R * D; e += kThr) {
       const int r = e / D, c = e % D;
       const size_t row = out_row(r);
       if (p.n_split == 1 || CLUSTER) {
@@ -293,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
   }
   const int t0 = split * p.chunk;
   if (!CLUSTER && t0 >= L) {  // empty split: the merge identity (-inf, 0); O is not written
-    for (int r = threadIdx.x; r < R; r += kThreads)
+    for (int r = threadIdx.x; r < R; r += kThr)
       if (in_bounds(out_row(r) * p.n_split + split, 1, n_rows * p.n_split, p.err))
         p.ws_ml[out_row(r) * p.n_split + split] = make_float2(-INFINITY, 0.f);
     return;
@@ -314,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
   __syncthreads();
 
   // ------------------------------------------------------------ producer ----
-  if (warp == kConsumerWarps) {
+  if (warp == kCW) {
     const int page0 = PAGED ? t0 / p.page_size : 0;
     if (PAGED) {
       // Stage the page indices of tokens [t0, t_end); an index outside the
@@ -452,6 +467,8 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
 
   // ------------------------------------------------------------ consumers ---
   const int g = lane >> 2, t = lane & 3;
+  // 16-token slice of each tile this warp takes, and its group's tile parity
+  const int ws = warp % kConsumerWarps, grp = warp / kConsumerWarps;
   // Q group as the A operand: rows = query heads h0..h0+G-1 (zero past G).
   uint32_t qa[D / 16][4];
   {
@@ -494,17 +511,17 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
 
   // ldmatrix lane roles.  K (non-transposed): matrix mi = lane/8 covers tokens
   // (mi/2)*8.. and d-chunk (mi%2); V (transposed): tokens (mi%2)*8.., chunk mi/2.
-  const int k_row = warp * 16 + ((lane >> 4) << 3) + (lane & 7);
+  const int k_row = ws * 16 + ((lane >> 4) << 3) + (lane & 7);
   const int k_chk = (lane >> 3) & 1;
-  const int v_row = warp * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
+  const int v_row = ws * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
   const int v_chk = lane >> 4;
   // FP8 (see fp8_row): tile rows of this lane's K fragments (n-tiles 0, 1)
   // and of its V gathers (logical keys 4t .. 4t + 3).
-  const int k8_row0 = warp * 16 + fp8_row(2 * g - (g & 1));
-  const int k8_row1 = warp * 16 + fp8_row(2 * g - (g & 1) + 2);
+  const int k8_row0 = ws * 16 + fp8_row(2 * g - (g & 1));
+  const int k8_row1 = ws * 16 + fp8_row(2 * g - (g & 1) + 2);
   int v8_row[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) v8_row[e] = warp * 16 + fp8_row(4 * t + e);
+  for (int e = 0; e < 4; ++e) v8_row[e] = ws * 16 + fp8_row(4 * t + e);
 
   // Key limits of rows g and g + 8 in this split: query t sees keys below
   // L - T_q + 1 + t (the split end t_end for plain decode).
@@ -513,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
   const int lim_lo = min(lim0, lim1);
 
   bool aborted = false;
-  for (int i = 0; i < n_tiles; ++i) {
+  for (int i = grp; i < n_tiles; i += NGRP) {
     const int st = i % NSTAGE;
     bool ok = *reinterpret_cast<volatile int*>(&abort_flag) == 0;
     if (ok) ok = mbar_wait(smem_u32(&full_bar[st]), (i / NSTAGE) & 1, p.wait_ns, p.err);
@@ -525,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
     }
     uint32_t kbase = smem_base + st * kStageBytes;
     uint32_t vbase = kbase + Lay::kTileBytes;
-    const int tok0 = t0 + i * kTile + warp * 16;  // first token of this warp's slice
+    const int tok0 = t0 + i * kTile + ws * 16;  // first token of this warp's slice
     float ksv[4], vsv[4];  // FP8: scales of this thread's 4 score columns
     if constexpr (FP8) {
       // Key order inside a warp's 16-key slice (FP8 only): the lane with
@@ -576,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
     for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        const int tk = FP8 ? tok0 - warp * 16 + v8_row[2 * nt + c] : tok0 + nt * 8 + 2 * t + c;
+        const int tk = FP8 ? tok0 - ws * 16 + v8_row[2 * nt + c] : tok0 + nt * 8 + 2 * t + c;
         const bool ok0 = !partial || tk < lim0, ok1 = !partial || tk < lim1;
         const float sc = FP8 ? ksv[nt * 2 + c] * p.scale_log2 : p.scale_log2;
         x0[nt * 2 + c] = ok0 ? sacc[nt][c] * sc : -INFINITY;
@@ -632,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
     if (partial) {
       // k indices 2t, 2t + 1 (vm0) and 2t + 8, 2t + 9 (vm1): keys tok0 + 2t ..
       // (FP8: logical keys 4t .. 4t + 3, in token rows v8_row[0..3])
-      const int base = tok0 - warp * 16;
+      const int base = tok0 - ws * 16;
       const int ta = FP8 ? base + v8_row[0] : tok0 + 2 * t, tb = FP8 ? base + v8_row[1] : ta + 1;
       const int tc = FP8 ? base + v8_row[2] : tok0 + 2 * t + 8, td = FP8 ? base + v8_row[3] : tc + 1;
       vm0 = (ta < t_end ? 0x0000ffffu : 0u) | (tb < t_end ? 0xffff0000u : 0u);
@@ -708,11 +725,14 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
   if (ROWS16) l1 = quad_sum(l1);
 
   // ------------------------------------------- merge the four warp partials --
-  named_bar_sync(1, kConsumerWarps * 32);
+  named_bar_sync(1, kCW * 32);
   const bool failed = *reinterpret_cast<volatile int*>(&abort_flag) != 0 ||
                       (PAGED && *reinterpret_cast<volatile int*>(&bad_page) != 0);
   float* mO = reinterpret_cast<float*>(smem);  // [warps][16][D]
-  float2* mML = reinterpret_cast<float2*>(smem + kConsumerWarps * 16 * D * 4);  // [warps][16]
+  float2* mML = reinterpret_cast<float2*>(smem + kCW * 16 * D * 4);  // [warps][16]
+  static_assert(kCW * 16 * D * 4 + kCW * 16 * 8 <=
+                    NSTAGE * (FP8 ? Fp8Layout<D>::kStageBytes : DecodeLayout<D>::kStageBytes),
+                "the warp partials reuse the stage ring");
   if (!failed) {
     if constexpr (TPV) {  // O^T d-tile mt = 2J + u: rows g, g + 8 are d = (D/8) g + 4J + 2u, + 1
 #pragma unroll
@@ -746,20 +766,20 @@ __global__ void __launch_bounds__(kThreads, (FP8 && !ROWS16) ? 3 : 2)
       if (ROWS16) mML[warp * 16 + g + 8] = make_float2(m1, l1);
     }
   }
-  named_bar_sync(1, kConsumerWarps * 32);
+  named_bar_sync(1, kCW * 32);
 
   constexpr int V4 = D / 4;
-  for (int e = threadIdx.x; e < R * V4; e += kConsumerWarps * 32) {
+  for (int e = threadIdx.x; e < R * V4; e += kCW * 32) {
     const int r = e / V4, c4 = e % V4;
     const size_t row = out_row(r);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float M = -INFINITY, Lsum = 0.f;
     if (!failed) {
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mML[w * 16 + r].x);
+      for (int w = 0; w < kCW; ++w) M = fmaxf(M, mML[w * 16 + r].x);
       const float ref = (M == -INFINITY) ? 0.f : M;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
+      for (int w = 0; w < kCW; ++w) {
         const float2 ml = mML[w * 16 + r];
         const float a = exp2f(ml.x - ref);
         Lsum += a * ml.y;
@@ -1037,9 +1057,9 @@ inline cudaError_t set_smem_attr_once(const void* kern, int smem, unsigned char*
   return e;
 }
 
-// CTAs of `kern` (160 threads, `smem` bytes) the current device holds at once,
-// looked up once per device.
-inline cudaError_t resident_ctas(const void* kern, int smem, int* cache, int* out) {
+// CTAs of `kern` (`threads` threads, `smem` bytes) the current device holds at
+// once, looked up once per device.
+inline cudaError_t resident_ctas(const void* kern, int threads, int smem, int* cache, int* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1048,7 +1068,7 @@ inline cudaError_t resident_ctas(const void* kern, int smem, int* cache, int* ou
     return cudaSuccess;
   }
   int per_sm = 0, sms = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
@@ -1057,18 +1077,19 @@ inline cudaError_t resident_ctas(const void* kern, int smem, int* cache, int* ou
   return cudaSuccess;
 }
 
-template <int D, bool ROWS16, int NSTAGE, bool PAGED, bool FP8>
+template <int D, bool ROWS16, int NSTAGE, bool PAGED, bool FP8, int NGRP = 1>
 cudaError_t launch_split(const DecodeParams& p_in, const CUtensorMap& tm_k,
                          const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
                          const CUtensorMap& tm_vs, cudaStream_t stream) {
   constexpr int smem = decode_smem_bytes<D, NSTAGE, FP8>();
-  auto kern = gqa_decode_split_kernel<D, ROWS16, NSTAGE, PAGED, FP8, false>;
+  constexpr int threads = (kConsumerWarps * NGRP + 1) * 32;
+  auto kern = gqa_decode_split_kernel<D, ROWS16, NSTAGE, PAGED, FP8, false, NGRP>;
   static unsigned char done[64];
   static int resident[64];
   cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem, done);
   if (e != cudaSuccess) return e;
   int fit = 0;
-  e = resident_ctas(reinterpret_cast<const void*>(kern), smem, resident, &fit);
+  e = resident_ctas(reinterpret_cast<const void*>(kern), threads, smem, resident, &fit);
   if (e != cudaSuccess) return e;
   DecodeParams p = p_in;
   // The L2 prefetch pays only when every CTA is resident while the previous
@@ -1077,7 +1098,7 @@ cudaError_t launch_split(const DecodeParams& p_in, const CUtensorMap& tm_k,
   p.prefetch_tiles = ctas <= fit ? kPrefetchTiles : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_split * p.n_rg, p.H_kv, p.B);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1110,6 +1131,21 @@ cudaError_t launch_split_rows(const DecodeParams& p, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
                               const CUtensorMap& tm_vs, cudaStream_t stream) {
   constexpr int NSTAGE = FP8 ? GQA_DECODE_STAGES_FP8 : (D >= 128 ? GQA_DECODE_STAGES_D128 : 6);
+  if constexpr (FP8) {
+    // One CTA per SM: two consumer groups and a deep ring (the per-tile E4M3
+    // conversions need more warps per SM than one group gives); otherwise
+    // several single-group CTAs share each SM.
+    constexpr int DEEP = GQA_DECODE_STAGES_FP8_ONE_WAVE;
+    int sms = 0;
+    cudaError_t e = sm_count(&sms);
+    if (e != cudaSuccess) return e;
+    if ((long long)p.n_split * p.n_rg * p.H_kv * p.B <= sms) {
+      constexpr int NG = GQA_FP8_ONE_WAVE_GROUPS;
+      if (p.T_q * p.G > 8)
+        return launch_split<D, true, DEEP, PAGED, FP8, NG>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+      return launch_split<D, false, DEEP, PAGED, FP8, NG>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+    }
+  }
   if constexpr (!FP8 && D >= 128) {
     // When the grid has at most one CTA per SM, a deeper ring (which leaves no
     // room for a second CTA) keeps more bytes in flight on each SM: measured

@@ -162,9 +162,21 @@ def test_decode_paged_multi(libs, T_q, page_size):
 
 
 @pytest.mark.parametrize("S", [128, 300, 1000])
-def test_prefill_causal(libs, S):
-    q, k, v = _dev(*inputs.prefill_inputs(2, S, 16, 2, 128, seed=S))
+@pytest.mark.parametrize("d", [128, 64, 32])
+def test_prefill_causal(libs, S, d):
+    q, k, v = _dev(*inputs.prefill_inputs(2, S, 16, 2, d, seed=S + d))
     _compare(libs, lambda: g.prefill_causal(q, k, v))
+
+
+@pytest.mark.parametrize("d", [64, 32])
+@pytest.mark.parametrize("n_part,window", [(1, -1), (3, 200)])
+def test_prefill_chunk_small_head_dims(libs, d, n_part, window):
+    gen = torch.Generator().manual_seed(d + n_part)
+    q = torch.randn(2, 200, 16, d, generator=gen).to(torch.bfloat16)
+    k = torch.randn(2, 1000, 2, d, generator=gen).to(torch.bfloat16)
+    v = torch.randn(2, 1000, 2, d, generator=gen).to(torch.bfloat16)
+    q, k, v, sl = _dev(q, k, v, torch.tensor([777, 1000], dtype=torch.int32))
+    _compare(libs, lambda: g.prefill_chunk(q, k, v, sl, window=window, n_part=n_part))
 
 
 @pytest.mark.parametrize("n_part,window", [(1, -1), (3, -1), (2, 200)])

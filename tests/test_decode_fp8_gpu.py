@@ -109,3 +109,36 @@ def test_fp8_deterministic_across_runs():
         runs.append((out.cpu(), lse.cpu()))
     assert torch.equal(runs[0][0].view(torch.int16), runs[1][0].view(torch.int16))
     assert torch.equal(runs[0][1], runs[1][1])
+
+
+def test_fp8_llama70b_one_wave_two_consumer_groups(oracle_mod):
+    """19 splits = 152 CTAs, at most one per SM: the kernel with two groups of
+    consumer warps taking alternate tiles and the deep stage ring."""
+    cfg = inputs.LLAMA70B_DECODE
+    q, k8, v8, ks, vs, lens = inputs.decode_inputs_fp8(cfg.B, cfg.H_q, cfg.H_kv, cfg.d, cfg.S_max,
+                                                       seed=4)
+    ref_o, ref_l = oracle_mod.decode_fp8(q, k8, v8, ks, vs, lens, cfg.scale)
+    args = _dev(q, k8, v8, ks, vs, lens)
+    runs = []
+    for _ in range(2):
+        out, lse = g.decode_fp8(*args, n_split=19)
+        torch.cuda.synchronize()
+        assert_parity(out, lse, ref_o, ref_l, "fp8 llama70b, 19 splits")
+        runs.append((out.cpu(), lse.cpu()))
+    assert torch.equal(runs[0][0].view(torch.int16), runs[1][0].view(torch.int16))
+    assert torch.equal(runs[0][1], runs[1][1])
+
+
+@pytest.mark.parametrize("page_size", [16, 128])
+def test_fp8_paged_one_wave_ragged_tail(oracle_mod, page_size):
+    # 2 sequences x 8 KV heads x 9 splits = 144 CTAs (one wave); lengths leave
+    # partial tiles and partial pages at the ends of splits
+    B, H_q, H_kv, d, S_max = 2, 64, 8, 128, 4000
+    q, k8, v8, ks, vs, lens = inputs.decode_inputs_fp8(B, H_q, H_kv, d, S_max, seed=8,
+                                                       seq_lens=[4000, 2777])
+    ref_o, ref_l = oracle_mod.decode_fp8(q, k8, v8, ks, vs, lens, 1 / math.sqrt(d))
+    kp, vp, ksp, vsp, table = _paginate_fp8(k8, v8, ks, vs, page_size, seed=9)
+    out, lse = g.decode_fp8(*_dev(q, kp, vp, ksp, vsp, lens), n_split=9,
+                            block_table=table.to(DEV))
+    torch.cuda.synchronize()
+    assert_parity(out, lse, ref_o, ref_l, f"paged fp8 one wave, page {page_size}")
