@@ -459,7 +459,7 @@ def run_ours(args, rank, world, dist):
     K = args.steps
     want_decode = args.only in (None, "decode")
     want_prefill = args.only in (None, "prefill")
-    want_configs = args.only is None
+    want_configs = args.only is None and not args.no_configs
 
     # ---------------- workloads ----------------
     dec = DecodeLeg(torch, g, inputs.LLAMA70B_DECODE, dev) if want_decode else None
@@ -1088,6 +1088,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time the headline step only, without the other workloads under "
+                         "'configs' (for profiler captures); the JSON line is partial")
     ap.add_argument("--workload", choices=WORKLOADS, default=None,
                     help="measure one further workload instead of the headline step")
     ap.add_argument("--only", choices=["decode", "prefill"], default=None,
