@@ -358,7 +358,7 @@ class DecodeLeg:
         self.kall.copy_(kd.unsqueeze(0).expand_as(self.kall))
         self.vall.copy_(vd.unsqueeze(0).expand_as(self.vall))
         del kd, vd
-        self.n_split = g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, cfg.d)
+        self.n_split = g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, dev.index)
         self.ws = g.decode_workspace(cfg.B, cfg.H_q, cfg.d, self.n_split, dev)
         self.out = torch.empty(cfg.B, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty(cfg.B, cfg.H_q, dtype=torch.float32, device=dev)
@@ -880,7 +880,7 @@ def run_workload(name, args):
         copies = n_copies(kv_bytes)
         qd, ld = q.to(dev), lens.to(dev)
         caches = [tuple(x.to(dev) for x in (k8, v8, ks, vs)) for _ in range(copies)]
-        n = 3 * g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, cfg.d)
+        n = 3 * g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, dev.index)
         ws = g.decode_workspace(cfg.B, cfg.H_q, cfg.d, n, dev)
         out = torch.empty(cfg.B, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
         lse = torch.empty(cfg.B, cfg.H_q, dtype=torch.float32, device=dev)

@@ -88,6 +88,12 @@ def _ptr(x) -> int | None:
     return x.data_ptr()
 
 
+def _device_index(x) -> int:
+    """CUDA device ordinal of a tensor (-1, the current device, for anything else)."""
+    dev = getattr(x, "device", None)
+    return dev.index if getattr(dev, "type", None) == "cuda" and dev.index is not None else -1
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         import torch
@@ -111,8 +117,8 @@ def gqa_attn_decode_workspace_bytes(B: int, H_q: int, d: int, n_split: int) -> i
     return load().gqa_attn_decode_workspace_bytes(B, H_q, d, n_split)
 
 
-def gqa_attn_decode_default_splits(B: int, H_kv: int, S_max: int, d: int) -> int:
-    return load().gqa_attn_decode_default_splits(B, H_kv, S_max, d)
+def gqa_attn_decode_default_splits(B: int, H_kv: int, S_max: int, device: int = -1) -> int:
+    return load().gqa_attn_decode_default_splits(B, H_kv, S_max, device)
 
 
 def gqa_attn_decode(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale, n_split,
@@ -257,7 +263,7 @@ def decode(q, k_cache, v_cache, seq_lens, scale=None, n_split=None, workspace=No
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if n_split is None:
-        n_split = gqa_attn_decode_default_splits(B, H_kv, S_max, d)
+        n_split = gqa_attn_decode_default_splits(B, H_kv, S_max, _device_index(q))
     if out is None:
         out = torch.empty((B, H_q, d), dtype=torch.bfloat16, device=q.device)
     if lse is None:
@@ -318,7 +324,7 @@ def decode_fused(q, k_cache, v_cache, seq_lens, scale=None, out=None, lse=None, 
 def paged_default_splits(B, H_kv, S_max, d, page_size):
     """Split count for the paged decode: the contiguous default, doubled for pages
     under 64 tokens (their smaller copies need two CTAs per SM in flight)."""
-    n = gqa_attn_decode_default_splits(B, H_kv, S_max, d)
+    n = gqa_attn_decode_default_splits(B, H_kv, S_max, -1)
     return 2 * n if page_size < 64 and n > 1 else n
 
 
@@ -377,7 +383,7 @@ def decode_fp8(q, k8, v8, k_scale, v_scale, seq_lens, scale=None, n_split=None, 
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if n_split is None:  # the on-chip conversion wants three CTAs per SM
-        n_split = 3 * gqa_attn_decode_default_splits(B, H_kv, S_max, d)
+        n_split = 3 * gqa_attn_decode_default_splits(B, H_kv, S_max, _device_index(q))
     if out is None:
         out = torch.empty((B, H_q, d), dtype=torch.bfloat16, device=q.device)
     if lse is None:

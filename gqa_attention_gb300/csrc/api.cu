@@ -137,9 +137,16 @@ size_t gqa_attn_decode_workspace_bytes(int B, int H_q, int d, int n_split) {
   return gqa::decode_ws_O_offset(B, H_q, n_split) + (size_t)B * H_q * n_split * d * sizeof(float);
 }
 
-int gqa_attn_decode_default_splits(int B, int H_kv, int S_max, int d) {
-  (void)d;
+int gqa_attn_decode_default_splits(int B, int H_kv, int S_max, int device) {
   if (B < 1 || H_kv < 1 || S_max < 1) return 1;
+  int sms = 0;
+  if (device < 0) {
+    sms = num_sms_current_device();
+  } else if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+             sms < 1) {
+    cudaGetLastError();  // (a device that cannot be queried leaves no sticky error)
+    return 1;
+  }
   // Up to 1024 tokens one CTA streams the whole sequence: the combine launch
   // then costs more than the split saves (measured: d = 32, 1024 tokens, 6.1 us
   // unsplit against 9.0 us with 8 splits + combine; d = 128 about equal).
@@ -148,7 +155,7 @@ int gqa_attn_decode_default_splits(int B, int H_kv, int S_max, int d) {
   // splits of at least 128 tokens and at most 8192 tokens (ragged batches then
   // have enough CTAs to balance).
   const long long groups = (long long)B * H_kv;
-  long long n = (num_sms_current_device() + groups - 1) / groups;
+  long long n = (sms + groups - 1) / groups;
   const long long most = (S_max + 127) / 128;
   const long long fill = (S_max + 8191) / 8192;
   if (n > most) n = most;
@@ -238,7 +245,7 @@ gqa_status gqa_attn_decode(const void* q, const void* k_cache, const void* v_cac
 
 int gqa_attn_decode_multi_default_splits(int B, int T_q, int H_q, int H_kv, int S_max, int d) {
   if (B < 1 || T_q < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0) return 1;
-  const int n = gqa_attn_decode_default_splits(B, H_kv, S_max, d);
+  const int n = gqa_attn_decode_default_splits(B, H_kv, S_max, -1);
   const long long groups = (T_q * (long long)(H_q / H_kv) + 15) / 16;
   if (groups <= 1) return n;
   // The tensor-core kernel: one CTA per SM, K/V read once per split.

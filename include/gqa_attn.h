@@ -106,11 +106,13 @@ int gqa_attn_decode_split_chunk(int S_max, int n_split);
  * argument is < 1. */
 size_t gqa_attn_decode_workspace_bytes(int B, int H_q, int d, int n_split);
 
-/* Deterministic split count for a (B, H_kv, S_max, d) decode on the current
- * device: 1 for S_max <= 1024 (one CTA per sequence and KV head; no combine
- * needed), otherwise about one CTA per SM, with splits of 128 to 8192 tokens.
- * Returns >= 1 (1 for invalid input). */
-int gqa_attn_decode_default_splits(int B, int H_kv, int S_max, int d);
+/* Deterministic split count for a (B, H_kv, S_max) decode on CUDA device
+ * `device` (its SM count; device < 0: the current device): 1 for S_max <= 1024
+ * (one CTA per sequence and KV head; no combine needed), otherwise about one
+ * CTA per SM, with splits of 128 to 8192 tokens.  The head dimension does not
+ * enter.  Returns >= 1 (1 for invalid input or a device that cannot be
+ * queried). */
+int gqa_attn_decode_default_splits(int B, int H_kv, int S_max, int device);
 
 /* Stage 1 of split-KV decode.
  *   q         device bf16 [B, H_q, d]           query (post-RoPE), read only

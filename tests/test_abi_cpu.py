@@ -61,10 +61,12 @@ def test_workspace_bytes_formula(lib):
 def test_default_splits_are_bounded(lib):
     # no GPU here: the SM count falls back to a default; the chunk bounds hold
     for B, H_kv, S in [(1, 2, 1024), (1, 8, 32768), (8, 8, 131072), (64, 8, 64), (1, 1, 1)]:
-        n = g.gqa_attn_decode_default_splits(B, H_kv, S, 128)
+        n = g.gqa_attn_decode_default_splits(B, H_kv, S, -1)
         assert 1 <= n <= max(1, -(-S // 128))
         assert n >= -(-S // 8192)
-    assert g.gqa_attn_decode_default_splits(0, 8, 100, 128) == 1
+    assert g.gqa_attn_decode_default_splits(0, 8, 100, -1) == 1
+    # an ordinal with no device behind it
+    assert g.gqa_attn_decode_default_splits(1, 8, 32768, 4096) == 1
 
 
 FAKE = 0x10000  # never dereferenced: every case below fails a host check first
@@ -104,7 +106,7 @@ def test_multi_token_row_limits_and_splits(lib):
     # the tensor-core tile runs one CTA per SM: the plain decode's split count
     for B, T_q, H_q, H_kv, S in [(1, 8, 64, 8, 32768), (1, 16, 64, 8, 32768), (2, 3, 64, 8, 5000)]:
         assert g.gqa_attn_decode_multi_default_splits(B, T_q, H_q, H_kv, S, 128) == \
-            g.gqa_attn_decode_default_splits(B, H_kv, S, 128)
+            g.gqa_attn_decode_default_splits(B, H_kv, S, -1)
 
 
 def test_combine_and_prefill_reject_bad_arguments(lib):
