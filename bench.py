@@ -808,7 +808,7 @@ def run_reference(args, rank, world):
 WORKLOADS = ("decode_tiny", "decode_ragged", "decode_paged16", "decode_paged128", "decode_fp8",
              "decode_fp8_ragged", "decode_multi2", "decode_multi4", "decode_multi8", "decode_multi16",
              "decode_paged16_multi8", "decode_paged128_multi8", "prefill_64k", "prefill_window",
-             "prefill_chunk", "prefill_d64", "prefill_d32")
+             "prefill_chunk", "prefill_d64", "prefill_d32", "decode_trace")
 
 
 def _shuffled_pages(k, v, page_size, seed):
@@ -831,6 +831,68 @@ def _shuffled_pages(k, v, page_size, seed):
     return kp, vp, table
 
 
+def run_decode_trace(args):
+    """Where the decode split kernel's time goes, from the trace build
+    (-DGQA_TRACE=1): per-phase cycles per tile and the CTA timeline of the
+    second of two back-to-back decode steps (bf16 at the default split count,
+    FP8 at three times it).  A diagnostic, not a timing."""
+    import numpy as np
+    import torch
+
+    import gqa_attention_gb300 as g
+    from gqa_attention_gb300 import build, inputs
+
+    pkg = os.path.join(ROOT, "gqa_attention_gb300")
+    path = build.build(extra_flags=["-DGQA_TRACE=1"],
+                       lib_path=os.path.join(pkg, "_build_trace", "libgqa_attn_trace.so"),
+                       build_dir=os.path.join(pkg, "_build_trace", "obj"))
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    g.load(path)
+    cfg = inputs.LLAMA70B_DECODE
+    n19 = g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, dev.index)
+    out = {"metric": "decode split-kernel trace (diagnostic build, not a timing)",
+           "workload": cfg.name, "units": "cycles per 64-token tile and consumer warp; "
+           "timeline in us from the first CTA's entry"}
+    for kind, n in (("bf16", n19), ("fp8", 3 * n19)):
+        if kind == "fp8":
+            host = inputs.decode_inputs_fp8(cfg.B, cfg.H_q, cfg.H_kv, cfg.d, cfg.S_max, seed=0)
+            call = g.decode_fp8
+        else:
+            host = inputs.decode_inputs_for(cfg, seed=0)
+            call = g.decode
+        a = [x.to(dev) for x in host]
+        for _ in range(max(3, args.warmup)):
+            call(*a, n_split=n)
+        torch.cuda.synchronize()
+        assert g.gqa_trace_clear() == g.GQA_OK
+        call(*a, n_split=n)
+        call(*a, n_split=n)
+        torch.cuda.synchronize()
+        ctas = n * cfg.H_kv
+        buf = np.zeros(ctas * 64, dtype=np.uint64)
+        assert g.gqa_trace_read(buf, buf.nbytes) == g.GQA_OK
+        rec = buf.reshape(ctas, 64).astype(np.float64)
+        warps = rec[:, 8:56].reshape(ctas, 8, 6)
+        used = warps[warps[:, :, 4] > 0]
+        tiles = used[:, 5].sum()
+        phases = {k: round(float(used[:, j].sum() / tiles), 1)
+                  for j, k in enumerate(("wait", "qk", "softmax", "pv", "loop"))}
+        t0 = rec[:, 0].min()
+        rel = (rec[:, :5] - t0) / 1e3
+
+        def pct(x):
+            return [round(float(np.percentile(x, q)), 2) for q in (0, 50, 100)]
+
+        out[f"{kind}_{n}_splits"] = {
+            "per_tile": phases,
+            "timeline_us_min_median_max": {
+                "entry": pct(rel[:, 0]), "release": pct(rel[:, 1]), "loop_start": pct(rel[:, 2]),
+                "loop_end": pct(rel[:, 3]), "epilogue_end": pct(rel[:, 4]),
+                "loop": pct(rel[:, 3] - rel[:, 2]), "epilogue": pct(rel[:, 4] - rel[:, 3])}}
+    return out
+
+
 def run_workload(name, args):
     """One JSON line for a workload other than the headline step (same timing rules)."""
     import torch
@@ -838,6 +900,8 @@ def run_workload(name, args):
     import gqa_attention_gb300 as g
     from gqa_attention_gb300 import inputs
 
+    if name == "decode_trace":
+        return run_decode_trace(args)
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     g.load()

@@ -39,6 +39,8 @@ from ._binding import (  # noqa: E402,F401
     gqa_attn_prefill_chunk_split,
     gqa_attn_prefill_chunk_workspace_bytes,
     gqa_last_device_error,
+    gqa_trace_clear,
+    gqa_trace_read,
     gqa_selftest_wait_timeout,
     gqa_set_wait_limit_ns,
     load,

@@ -48,6 +48,8 @@ SIGNATURES = {
     "gqa_attn_prefill_chunk_split": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P,
                                           _P, _P, _P]),
     "gqa_last_device_error": (_I, [_P]),
+    "gqa_trace_clear": (_I, []),
+    "gqa_trace_read": (_I, [_P, _SZ]),
     "gqa_set_wait_limit_ns": (_U64, [_U64]),
     "gqa_selftest_wait_timeout": (_I, [_U64, _P]),
 }
@@ -223,6 +225,17 @@ def gqa_attn_prefill_chunk_split(q, k_cache, v_cache, seq_lens, B, T_q, S_max, H
     return load().gqa_attn_prefill_chunk_split(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B, T_q, S_max, H_q, H_kv, d, scale,
         int(window), int(n_part), _ptr(workspace), _ptr(out), _ptr(lse), _stream(stream))
+
+
+def gqa_trace_clear() -> int:
+    return load().gqa_trace_clear()
+
+
+def gqa_trace_read(host, nbytes: int) -> int:
+    """Copy trace records into `host` (an integer address, or a numpy/CPU array)."""
+    addr = host if isinstance(host, int) else (
+        host.ctypes.data if hasattr(host, "ctypes") else host.data_ptr())
+    return load().gqa_trace_read(addr, nbytes)
 
 
 def gqa_last_device_error(stream=None) -> int:

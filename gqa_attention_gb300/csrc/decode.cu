@@ -14,10 +14,35 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "gqa_attn.h"
 #include "internal.h"
 
+// A build with GQA_TRACE=1 records where the split kernel's time goes: per CTA,
+// globaltimer stamps (entry, release of the dependency wait, start and end of
+// the tile loop, end of the epilogue) and the SM; per consumer warp, clock64
+// cycles spent waiting for tiles, in Q K^T, in the softmax update, in P V and in
+// the whole loop.  Phase boundaries wait for the phase's results (a register
+// move of one of them), which perturbs the schedule a little; no arithmetic
+// changes.  Other builds compile none of it.
+#ifndef GQA_TRACE
+#define GQA_TRACE 0
+#endif
+
 namespace gqa {
+// One record of kTraceWords 64-bit words per CTA (linear block index), for the
+// first kTraceCtas CTAs of the last launch: words 0-4 the stamps (ns), 5 the
+// SM, 6 = split, 7 = tiles; from word 8, six words per consumer warp: wait,
+// Q K^T, softmax, P V and loop cycles, and tiles the warp handled.
+constexpr int kTraceCtas = 4096, kTraceWords = 64;
+__device__ unsigned long long g_trace[GQA_TRACE ? kTraceCtas * kTraceWords : 1];
+
 namespace {
+constexpr bool kTrace = GQA_TRACE != 0;
+__device__ __forceinline__ unsigned long long trace_clock() { return kTrace ? clock64() : 0ull; }
+// Waits for `v` to be ready (a register move that reads it) in trace builds.
+__device__ __forceinline__ void trace_ready(float& v) {
+  if constexpr (kTrace) asm volatile("mov.b32 %0, %0;" : "+f"(v));
+}
 
 #ifndef GQA_SPLIT_PDL
 #define GQA_SPLIT_PDL 1  // launch the split kernel as a programmatic dependent
@@ -225,6 +250,10 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
   const int rg = CLUSTER ? 0 : blockIdx.x % p.n_rg;
   const int kv = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned long long tr_entry = kTrace ? globaltimer_ns() : 0ull;
+  const size_t tr_cta = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+  unsigned long long* const tr_rec =
+      (kTrace && tr_cta < (size_t)kTraceCtas) ? g_trace + tr_cta * kTraceWords : nullptr;
   const int G = p.G;
   const int h0 = kv * G;
   // mma row r (0..15) of row group rg is row x = 16 rg + r of the KV head:
@@ -287,6 +316,7 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
     }
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  const unsigned long long tr_release = kTrace ? globaltimer_ns() : 0ull;
   const int L = p.seq_lens[b];
 
   // ---- device-side argument check and empty splits (no pipeline needed) ----
@@ -530,10 +560,16 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
   const int lim_lo = min(lim0, lim1);
 
   bool aborted = false;
+  const unsigned long long tr_loop0 = kTrace ? globaltimer_ns() : 0ull;
+  unsigned long long tr_c[6] = {0, 0, 0, 0, trace_clock(), 0};  // wait, qk, softmax, pv, loop, tiles
   for (int i = grp; i < n_tiles; i += NGRP) {
     const int st = i % NSTAGE;
+    const unsigned long long tc0 = trace_clock();
     bool ok = *reinterpret_cast<volatile int*>(&abort_flag) == 0;
     if (ok) ok = mbar_wait(smem_u32(&full_bar[st]), (i / NSTAGE) & 1, p.wait_ns, p.err);
+    const unsigned long long tc1 = trace_clock();
+    tr_c[0] += tc1 - tc0;
+    tr_c[5] += 1;
     // Keep the warp converged for the warp-collective ldmatrix/mma below.
     if (!__all_sync(0xffffffffu, ok)) {
       *reinterpret_cast<volatile int*>(&abort_flag) = 1;
@@ -588,6 +624,10 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
 
     // Scores in base-2 units; tokens past the split end are masked by select.
     const bool partial = tok0 + 16 > lim_lo;
+    trace_ready(sacc[0][0]);
+    trace_ready(sacc[1][0]);
+    const unsigned long long tc2 = trace_clock();
+    tr_c[1] += tc2 - tc1;
     float x0[4], x1[4];  // row g (x0) and row g+8 (x1)
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -630,6 +670,10 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
       }
     }
     // P as the A operand of P V (k = this warp's 16 tokens).
+    trace_ready(p0[0]);
+    trace_ready(o[0][0]);
+    const unsigned long long tc3 = trace_clock();
+    tr_c[2] += tc3 - tc2;
     uint32_t pa[4];
     if constexpr (FP8) {  // fold the value scales into P (f16)
       pa[0] = pack_f16x2(p0[0] * vsv[0], p0[1] * vsv[1]);
@@ -716,10 +760,19 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
         mma_bf16_16816(o[2 * jj + 1], pa, v2 & vm0, v3 & vm1);
       }
     }
+    trace_ready(o[0][0]);
+    trace_ready(o[D / 16 - 1][3]);
+    tr_c[3] += trace_clock() - tc3;
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
   }
   (void)aborted;
+  const unsigned long long tr_loop1 = kTrace ? globaltimer_ns() : 0ull;
+  if (kTrace && tr_rec && lane == 0 && warp < 8) {
+    tr_c[4] = trace_clock() - tr_c[4];
+#pragma unroll
+    for (int k = 0; k < 6; ++k) tr_rec[8 + 6 * warp + k] = tr_c[k];
+  }
 
   l0 = quad_sum(l0);
   if (ROWS16) l1 = quad_sum(l1);
@@ -817,6 +870,18 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
     }
   }
 
+  if (kTrace && tr_rec && threadIdx.x == 0) {
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    tr_rec[0] = tr_entry;
+    tr_rec[1] = tr_release;
+    tr_rec[2] = tr_loop0;
+    tr_rec[3] = tr_loop1;
+    tr_rec[4] = globaltimer_ns();
+    tr_rec[5] = smid;
+    tr_rec[6] = split;
+    tr_rec[7] = n_tiles;
+  }
   if constexpr (CLUSTER) {
     __syncwarp();
     cluster_sync();  // every partial of the cluster is in place
@@ -1322,3 +1387,16 @@ cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t 
 }
 
 }  // namespace gqa
+
+extern "C" gqa_status gqa_trace_clear(void) {
+  if (!gqa::kTrace) return GQA_ERR_UNSUPPORTED;
+  static unsigned long long zeros[gqa::kTraceCtas * gqa::kTraceWords];
+  return cudaMemcpyToSymbol(gqa::g_trace, zeros, sizeof zeros) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+extern "C" gqa_status gqa_trace_read(void* host, size_t bytes) {
+  if (!gqa::kTrace) return GQA_ERR_UNSUPPORTED;
+  constexpr size_t total = sizeof(unsigned long long) * gqa::kTraceCtas * gqa::kTraceWords;
+  if (!host || bytes > total) return GQA_ERR_INVALID_ARG;
+  return cudaMemcpyFromSymbol(host, gqa::g_trace, bytes) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}

@@ -234,6 +234,25 @@ gqa_status gqa_attn_decode_noalloc(const void* q, const void* k_cache, const voi
                                    int d, float scale, int n_split, void* out, float* lse,
                                    gqa_stream_t stream);
 
+/* Diagnostics of a library built with -DGQA_TRACE=1 (the pages have no
+ * counterpart; every other build returns GQA_ERR_UNSUPPORTED from both calls
+ * and records nothing).  The split-KV decode kernel (gqa_attn_decode,
+ * _paged, _fp8, _multi on the mma.sync rows) then keeps, for the first 4096
+ * CTAs of its last launch (linear block index x + gridDim.x * (y + gridDim.y * z)),
+ * one record of 64 64-bit words: 0-4 globaltimer stamps in ns (CTA entry,
+ * release of the dependency wait, tile loop start, tile loop end, epilogue
+ * end), 5 the SM, 6 the split, 7 the CTA's tiles; from word 8, six words per
+ * consumer warp w (8 + 6w ..): clock64 cycles waiting for tiles, in Q K^T, in
+ * the softmax update, in P V and in the whole loop, and the tiles the warp
+ * handled.  CTAs that return before their tile loop (empty splits, bad
+ * lengths) write no record.
+ * gqa_trace_clear zeroes every record (synchronous); gqa_trace_read copies the
+ * first `bytes` bytes (at most 4096 * 64 * 8) into `host` after the stream has
+ * been synchronised by the caller.  GQA_ERR_INVALID_ARG for a null `host` or
+ * too many bytes. */
+gqa_status gqa_trace_clear(void);
+gqa_status gqa_trace_read(void* host, size_t bytes);
+
 /* ------------------------------------------------------------------------
  * Causal prefill ("Attention Kernel 계보", p.9 §4 and p.13 §1-§6)
  * ------------------------------------------------------------------------

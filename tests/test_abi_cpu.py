@@ -125,3 +125,13 @@ def test_wait_limit_setter_round_trips(lib):
     old = g.gqa_set_wait_limit_ns(5_000_000)
     assert g.gqa_set_wait_limit_ns(old) == 5_000_000
     assert g.gqa_set_wait_limit_ns(old) == old
+
+
+def test_trace_calls_are_unsupported_in_the_default_build(lib):
+    """The default library records no trace: both diagnostics calls say so
+    without touching the GPU."""
+    import numpy as np
+
+    buf = np.zeros(64, dtype=np.uint64)
+    assert g.gqa_trace_clear() == g.GQA_ERR_UNSUPPORTED
+    assert g.gqa_trace_read(buf, buf.nbytes) == g.GQA_ERR_UNSUPPORTED
