@@ -226,6 +226,16 @@ __device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Hardware base-2 exponential (MUFU), flushing subnormal results to zero; used
+// where the inputs are <= 0 (relative error about 2^-22, far below the bf16
+// rounding the results feed) and exp2(-inf) = +0 serves as the weight of an
+// empty or masked term.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

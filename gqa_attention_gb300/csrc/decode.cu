@@ -32,7 +32,8 @@ namespace gqa {
 // One record of kTraceWords 64-bit words per CTA (linear block index), for the
 // first kTraceCtas CTAs of the last launch: words 0-4 the stamps (ns), 5 the
 // SM, 6 = split, 7 = tiles; from word 8, six words per consumer warp: wait,
-// Q K^T, softmax, P V and loop cycles, and tiles the warp handled.
+// Q K^T, softmax, P V and loop cycles, and tiles the warp handled; words
+// 56-58 the epilogue's phases on thread 0 (cycles).
 constexpr int kTraceCtas = 4096, kTraceWords = 64;
 __device__ unsigned long long g_trace[GQA_TRACE ? kTraceCtas * kTraceWords : 1];
 
@@ -186,9 +187,9 @@ __device__ __forceinline__ float online_update(float (&x)[4], float& m, float& l
   const float mx = quad_max(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
   const float m_new = fmaxf(m, mx);
   const float ref = (m_new == -INFINITY) ? 0.f : m_new;  // no (-inf) - (-inf)
-  const float alpha = exp2f(m - ref);
+  const float alpha = ex2_approx(m - ref);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) p[i] = exp2f(x[i] - ref);
+  for (int i = 0; i < 4; ++i) p[i] = ex2_approx(x[i] - ref);
   l = l * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
   m = m_new;
   return alpha;
@@ -778,7 +779,9 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
   if (ROWS16) l1 = quad_sum(l1);
 
   // ------------------------------------------- merge the four warp partials --
+  const unsigned long long te0 = trace_clock();
   named_bar_sync(1, kCW * 32);
+  const unsigned long long te1 = trace_clock();
   const bool failed = *reinterpret_cast<volatile int*>(&abort_flag) != 0 ||
                       (PAGED && *reinterpret_cast<volatile int*>(&bad_page) != 0);
   float* mO = reinterpret_cast<float*>(smem);  // [warps][16][D]
@@ -820,6 +823,7 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
     }
   }
   named_bar_sync(1, kCW * 32);
+  const unsigned long long te2 = trace_clock();
 
   constexpr int V4 = D / 4;
   for (int e = threadIdx.x; e < R * V4; e += kCW * 32) {
@@ -834,7 +838,7 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
 #pragma unroll
       for (int w = 0; w < kCW; ++w) {
         const float2 ml = mML[w * 16 + r];
-        const float a = exp2f(ml.x - ref);
+        const float a = ex2_approx(ml.x - ref);
         Lsum += a * ml.y;
         const float4 ow = *reinterpret_cast<const float4*>(&mO[(w * 16 + r) * D + c4 * 4]);
         acc.x += a * ow.x;
@@ -871,6 +875,9 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
   }
 
   if (kTrace && tr_rec && threadIdx.x == 0) {
+    tr_rec[56] = te1 - te0;            // waiting for the other consumer warps
+    tr_rec[57] = te2 - te1;            // partials into shared memory
+    tr_rec[58] = trace_clock() - te2;  // merge and global stores
     unsigned smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
     tr_rec[0] = tr_entry;
@@ -910,7 +917,7 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
       for (int q = 0; q < kMaxClusterSplits; ++q) {
         if (q >= C) break;
         if (ml[q].x == -INFINITY) continue;  // empty split: weight 0
-        const float w = exp2f(ml[q].x - ref);
+        const float w = ex2_approx(ml[q].x - ref);
         Lt += w * ml[q].y;
         acc += w * ld_dsmem_f32(mapa_shared(cO + (r * D + c) * 4, q));
       }
@@ -996,7 +1003,7 @@ __global__ void __launch_bounds__(kCombineThreads, CHUNK == 8 ? 7 : 4)
     }
     const float Mn = fmaxf(M, cm);
     const float ref = (Mn == -INFINITY) ? 0.f : Mn;
-    const float a_old = (M == -INFINITY) ? 0.f : exp2f((M - ref) * kLog2e);
+    const float a_old = (M == -INFINITY) ? 0.f : ex2_approx((M - ref) * kLog2e);
     L *= a_old;
 #pragma unroll
     for (int v = 0; v < VEC; ++v) acc[v] *= a_old;
@@ -1004,7 +1011,7 @@ __global__ void __launch_bounds__(kCombineThreads, CHUNK == 8 ? 7 : 4)
     for (int c = 0; c < kCombineChunk; ++c) {
       // an empty split (m = -inf) has weight 0 and its O (never written) is not used
       const bool live = mlv[c].x != -INFINITY;
-      const float w = live ? exp2f((mlv[c].x - ref) * kLog2e) : 0.f;
+      const float w = live ? ex2_approx((mlv[c].x - ref) * kLog2e) : 0.f;
       L += w * mlv[c].y;
 #pragma unroll
       for (int v = 0; v < VEC; ++v) acc[v] += live ? w * ov[c][v] : 0.f;
@@ -1033,7 +1040,7 @@ __global__ void __launch_bounds__(kCombineThreads, CHUNK == 8 ? 7 : 4)
   for (int v = 0; v < VEC; ++v) tot[v] = 0.f;
 #pragma unroll
   for (int w = 0; w < kCombineWarps; ++w) {
-    const float a = (s_m[w] == -INFINITY) ? 0.f : exp2f((s_m[w] - ref) * kLog2e);
+    const float a = (s_m[w] == -INFINITY) ? 0.f : ex2_approx((s_m[w] - ref) * kLog2e);
     Lt += a * s_l[w];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) tot[v] += a * s_o[w][lane * VEC + v];
@@ -1088,7 +1095,7 @@ __global__ void __launch_bounds__(D, 4) gqa_decode_combine_cols_kernel(const Com
   for (int s = 0; s < kColsSplits; ++s) {
     // an empty split (m = -inf) has weight 0 and its O (never written) is not used
     const bool live = mlv[s].x != -INFINITY;
-    const float w = live ? exp2f((mlv[s].x - ref) * kLog2e) : 0.f;
+    const float w = live ? ex2_approx((mlv[s].x - ref) * kLog2e) : 0.f;
     L += w * mlv[s].y;
     acc += live ? w * ov[s] : 0.f;
   }

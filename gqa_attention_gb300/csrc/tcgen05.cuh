@@ -170,14 +170,6 @@ __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
                  "+r"(r[30]), "+r"(r[31]));
 }
 
-// Hardware base-2 exponential (MUFU), flushing subnormal results to zero; used
-// where the inputs are <= 0 and the results feed a bf16 operand and an fp32 sum.
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // max(a, b, c) in one instruction (three-input form of max.f32, sm_100 and later).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

@@ -244,8 +244,10 @@ gqa_status gqa_attn_decode_noalloc(const void* q, const void* k_cache, const voi
  * end), 5 the SM, 6 the split, 7 the CTA's tiles; from word 8, six words per
  * consumer warp w (8 + 6w ..): clock64 cycles waiting for tiles, in Q K^T, in
  * the softmax update, in P V and in the whole loop, and the tiles the warp
- * handled.  CTAs that return before their tile loop (empty splits, bad
- * lengths) write no record.
+ * handled; words 56-58: the epilogue's cycles on thread 0 waiting for the
+ * other consumer warps, writing the warp partials to shared memory, and
+ * merging them and storing the result.  CTAs that return before their tile
+ * loop (empty splits, bad lengths) write no record.
  * gqa_trace_clear zeroes every record (synchronous); gqa_trace_read copies the
  * first `bytes` bytes (at most 4096 * 64 * 8) into `host` after the stream has
  * been synchronised by the caller.  GQA_ERR_INVALID_ARG for a null `host` or
