@@ -888,7 +888,7 @@ def run_decode_trace(args):
             "per_tile": phases,
             "epilogue_cycles_median": {k: float(np.median(rec[:, 56 + j]))
                                        for j, k in enumerate(("warp_rendezvous", "partials_to_smem",
-                                                              "merge_and_store", "it0_start", "it0_math", "it1_start", "it1_math"))},
+                                                              "merge_and_store"))},
             "timeline_us_min_median_max": {
                 "entry": pct(rel[:, 0]), "release": pct(rel[:, 1]), "loop_start": pct(rel[:, 2]),
                 "loop_end": pct(rel[:, 3]), "epilogue_end": pct(rel[:, 4]),

@@ -260,9 +260,13 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
   // mma row r (0..15) of row group rg is row x = 16 rg + r of the KV head:
   // query t = x / G of head h0 + x % G; rows past T_q * G are padding.
   const int R = min(16, p.T_q * G - 16 * rg);
+  // x / G without an integer division: (x + 1/2) / G lies at least 1/32 from
+  // the nearest integer (G <= 16), far more than the float error for x < 2^20.
+  const float inv_g = 1.f / static_cast<float>(G);
   auto out_row = [&](int r) -> size_t {
     const int x = 16 * rg + r;
-    return ((size_t)b * p.T_q + x / G) * p.H_q + h0 + x % G;
+    const int tq = static_cast<int>((static_cast<float>(x) + 0.5f) * inv_g);
+    return ((size_t)b * p.T_q + tq) * p.H_q + h0 + (x - tq * G);
   };
   const size_t n_rows = (size_t)p.B * p.T_q * p.H_q;  // rows of out, lse and the workspace
   // Launched as a programmatic dependent of the previous kernel in the stream:
@@ -826,8 +830,9 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
   const unsigned long long te2 = trace_clock();
 
   constexpr int V4 = D / 4;
-  for (int e = threadIdx.x; e < R * V4; e += kCW * 32) {
-    const int r = e / V4, c4 = e % V4;
+  // Item e: row r = e / V4, columns 4 c4 .. 4 c4 + 3 of the merged partial.
+  auto merge_item = [&](int e, bool live) {
+    const int r = (e / V4) & 15, c4 = e % V4;
     const size_t row = out_row(r);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float M = -INFINITY, Lsum = 0.f;
@@ -851,6 +856,7 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
       Lsum = NAN;
       acc = make_float4(NAN, NAN, NAN, NAN);
     }
+    if (!live) return;
     if constexpr (CLUSTER) {
       // this CTA's partial, kept for the cluster merge (m in base-2 units)
       float* cO = reinterpret_cast<float*>(smem + kClusterPartOff<D>);
@@ -871,6 +877,21 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
         *reinterpret_cast<float4*>(&p.ws_O[idx * D + c4 * 4]) = acc;
       if (c4 == 0 && in_bounds(idx, 1, n_rows * p.n_split, p.err))
         p.ws_ml[idx] = make_float2(M * kLn2, Lsum);
+    }
+  };
+  if constexpr (FP8 && !ROWS16 && NGRP == 1) {
+    // (three CTAs per SM at 128 registers: the rolled loop)
+    for (int e = threadIdx.x; e < R * V4; e += kCW * 32) merge_item(e, true);
+  } else {
+    // A compile-time trip count (rows r < 16, and < 8 without ROWS16, keep
+    // every shared-memory read in bounds), so that the items' loads overlap;
+    // only the stores of items past R * V4 are skipped.
+    constexpr int kMaxR = ROWS16 || CLUSTER ? 16 : 8;
+    constexpr int kMergeIt = (kMaxR * V4 + kCW * 32 - 1) / (kCW * 32);
+#pragma unroll
+    for (int it = 0; it < kMergeIt; ++it) {
+      const int e = threadIdx.x + it * kCW * 32;
+      merge_item(e, e < R * V4);
     }
   }
 
