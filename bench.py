@@ -889,6 +889,9 @@ def run_decode_trace(args):
             "epilogue_cycles_median": {k: float(np.median(rec[:, 56 + j]))
                                        for j, k in enumerate(("warp_rendezvous", "partials_to_smem",
                                                               "merge_and_store"))},
+            "prologue_cycles_median": {k: float(np.median(rec[:, 59 + j]))
+                                       for j, k in enumerate(("seq_len_read", "barrier_setup",
+                                                              "query_fragments"))},
             "timeline_us_min_median_max": {
                 "entry": pct(rel[:, 0]), "release": pct(rel[:, 1]), "loop_start": pct(rel[:, 2]),
                 "loop_end": pct(rel[:, 3]), "epilogue_end": pct(rel[:, 4]),

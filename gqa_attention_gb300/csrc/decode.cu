@@ -33,7 +33,7 @@ namespace gqa {
 // first kTraceCtas CTAs of the last launch: words 0-4 the stamps (ns), 5 the
 // SM, 6 = split, 7 = tiles; from word 8, six words per consumer warp: wait,
 // Q K^T, softmax, P V and loop cycles, and tiles the warp handled; words
-// 56-58 the epilogue's phases on thread 0 (cycles).
+// 56-58 the epilogue's phases and 59-61 the prologue's on thread 0 (cycles).
 constexpr int kTraceCtas = 4096, kTraceWords = 64;
 __device__ unsigned long long g_trace[GQA_TRACE ? kTraceCtas * kTraceWords : 1];
 
@@ -322,7 +322,10 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const unsigned long long tr_release = kTrace ? globaltimer_ns() : 0ull;
-  const int L = p.seq_lens[b];
+  const unsigned long long tp0 = trace_clock();
+  int L = p.seq_lens[b];
+  if constexpr (kTrace) asm volatile("mov.b32 %0, %0;" : "+r"(L));
+  const unsigned long long tp1 = trace_clock();
 
   // ---- device-side argument check and empty splits (no pipeline needed) ----
   if (L < p.T_q || L > p.S_max || L < 1) {
@@ -362,6 +365,7 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
     fence_barrier_init();
   }
   __syncthreads();
+  const unsigned long long tp2 = trace_clock();
 
   // ------------------------------------------------------------ producer ----
   if (warp == kCW) {
@@ -565,6 +569,12 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
   const int lim_lo = min(lim0, lim1);
 
   bool aborted = false;
+  if constexpr (kTrace) {
+    float q_any = __uint_as_float(qa[0][0]);
+    trace_ready(q_any);
+    qa[0][0] = __float_as_uint(q_any);
+  }
+  const unsigned long long tp3 = trace_clock();
   const unsigned long long tr_loop0 = kTrace ? globaltimer_ns() : 0ull;
   unsigned long long tr_c[6] = {0, 0, 0, 0, trace_clock(), 0};  // wait, qk, softmax, pv, loop, tiles
   for (int i = grp; i < n_tiles; i += NGRP) {
@@ -899,6 +909,9 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
     tr_rec[56] = te1 - te0;            // waiting for the other consumer warps
     tr_rec[57] = te2 - te1;            // partials into shared memory
     tr_rec[58] = trace_clock() - te2;  // merge and global stores
+    tr_rec[59] = tp1 - tp0;            // the sequence length read after the release
+    tr_rec[60] = tp2 - tp1;            // barrier set-up and the CTA barrier
+    tr_rec[61] = tp3 - tp2;            // the query fragments
     unsigned smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
     tr_rec[0] = tr_entry;
