@@ -409,15 +409,17 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
     for (int i = 0; i < n_tiles; ++i) {
       const int st = i % NSTAGE;
       bool go = true;
-      if (lane == 0) {
-        if (i >= NSTAGE &&
-            !mbar_wait(smem_u32(&empty_bar[st]), ((i / NSTAGE) - 1) & 1, p.wait_ns, p.err)) {
+      if (lane == 0 && i >= NSTAGE) {
+        // A slot the consumers have released passes at once; the abort flag
+        // (a consumer that gave up stops arriving) is read only on the slow path.
+        const uint32_t eb = smem_u32(&empty_bar[st]), par = ((i / NSTAGE) - 1) & 1;
+        if (!mbar_try_wait(eb, par) && (*reinterpret_cast<volatile int*>(&abort_flag) ||
+                                        !mbar_wait(eb, par, p.wait_ns, p.err))) {
           *reinterpret_cast<volatile int*>(&abort_flag) = 1;
           go = false;
         }
-        if (go && *reinterpret_cast<volatile int*>(&abort_flag)) go = false;
-        if (go) mbar_arrive_expect_tx(smem_u32(&full_bar[st]), kTxBytes);
       }
+      if (lane == 0 && go) mbar_arrive_expect_tx(smem_u32(&full_bar[st]), kTxBytes);
       if (!__shfl_sync(0xffffffffu, go, 0)) break;  // (the barrier is armed before any copy)
       const uint32_t fb = smem_u32(&full_bar[st]);
       const uint32_t dst_k = smem_base + st * kStageBytes;
@@ -580,8 +582,11 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
   for (int i = grp; i < n_tiles; i += NGRP) {
     const int st = i % NSTAGE;
     const unsigned long long tc0 = trace_clock();
-    bool ok = *reinterpret_cast<volatile int*>(&abort_flag) == 0;
-    if (ok) ok = mbar_wait(smem_u32(&full_bar[st]), (i / NSTAGE) & 1, p.wait_ns, p.err);
+    // A stage that has landed passes at once; the abort flag is read only on
+    // the slow path.
+    const uint32_t fb = smem_u32(&full_bar[st]), par = (i / NSTAGE) & 1;
+    bool ok = mbar_try_wait(fb, par);
+    if (!ok) ok = *reinterpret_cast<volatile int*>(&abort_flag) == 0 && mbar_wait(fb, par, p.wait_ns, p.err);
     const unsigned long long tc1 = trace_clock();
     tr_c[0] += tc1 - tc0;
     tr_c[5] += 1;

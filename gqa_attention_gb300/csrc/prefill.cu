@@ -192,8 +192,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  // A bounded wait that also gives up once another role has aborted.
+  // A bounded wait that also gives up once another role has aborted.  A phase
+  // that has already completed passes at once: the abort flag is read only on
+  // the slow path, since a shared-memory load in front of every wait delays
+  // the MMA warp's next issue (the tensor core queues about one instruction).
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_try_wait(smem_u32(bar), parity)) return true;
     if (*abort_v) return false;
     if (mbar_wait(smem_u32(bar), parity, p.wait_ns, p.err)) return true;
     *abort_v = 1;
