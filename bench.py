@@ -808,7 +808,7 @@ def run_reference(args, rank, world):
 WORKLOADS = ("decode_tiny", "decode_ragged", "decode_paged16", "decode_paged128", "decode_fp8",
              "decode_fp8_ragged", "decode_multi2", "decode_multi4", "decode_multi8", "decode_multi16",
              "decode_paged16_multi8", "decode_paged128_multi8", "prefill_64k", "prefill_window",
-             "prefill_chunk", "prefill_d64", "prefill_d32", "decode_trace")
+             "prefill_chunk", "prefill_d64", "prefill_d32", "decode_trace", "prefill_trace", "mma_rate")
 
 
 def _shuffled_pages(k, v, page_size, seed):
@@ -839,16 +839,10 @@ def run_decode_trace(args):
     import numpy as np
     import torch
 
-    import gqa_attention_gb300 as g
-    from gqa_attention_gb300 import build, inputs
+    from gqa_attention_gb300 import inputs
 
-    pkg = os.path.join(ROOT, "gqa_attention_gb300")
-    path = build.build(extra_flags=["-DGQA_TRACE=1"],
-                       lib_path=os.path.join(pkg, "_build_trace", "libgqa_attn_trace.so"),
-                       build_dir=os.path.join(pkg, "_build_trace", "obj"))
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    g.load(path)
+    g = _trace_build()
+    dev = torch.device("cuda", torch.cuda.current_device())
     cfg = inputs.LLAMA70B_DECODE
     n19 = g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, dev.index)
     out = {"metric": "decode split-kernel trace (diagnostic build, not a timing)",
@@ -899,6 +893,90 @@ def run_decode_trace(args):
     return out
 
 
+def _trace_build():
+    """Build the diagnostic (-DGQA_TRACE=1) library beside the default one and load it."""
+    import torch
+
+    import gqa_attention_gb300 as g
+    from gqa_attention_gb300 import build
+
+    pkg = os.path.join(ROOT, "gqa_attention_gb300")
+    path = build.build(extra_flags=["-DGQA_TRACE=1"],
+                       lib_path=os.path.join(pkg, "_build_trace", "libgqa_attn_trace.so"),
+                       build_dir=os.path.join(pkg, "_build_trace", "obj"))
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    g.load(path)
+    return g
+
+
+def run_prefill_trace(args):
+    """Where a causal prefill step's cycles go, from the trace build: medians
+    over the recorded (CTA, head, tile) stamps of the Llama3-70B-shaped 8K
+    prefill (second of two launches).  A diagnostic, not a timing."""
+    import numpy as np
+    import torch
+
+    from gqa_attention_gb300 import inputs
+
+    g = _trace_build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cfg = inputs.LLAMA70B_PREFILL_8K
+    q, k, v = (x.to(dev) for x in inputs.prefill_inputs_for(cfg, seed=0))
+    for _ in range(max(3, args.warmup)):
+        g.prefill_causal(q, k, v)
+    torch.cuda.synchronize()
+    assert g.gqa_trace_clear() == g.GQA_OK
+    g.prefill_causal(q, k, v)
+    torch.cuda.synchronize()
+    buf = np.zeros(8 * 2 * 64 * 16, dtype=np.uint64)
+    assert g.gqa_trace_prefill_read(buf, buf.nbytes) == g.GQA_OK
+    t = buf.reshape(8, 2, 64, 16).astype(np.float64)
+
+    def med(f):
+        vals = [f(c, x, j) for c in range(8) for x in range(2) for j in range(4, 60)
+                if t[c, x, j + 1, 0] > 0 and t[c, x, j, 14] > 0]
+        return round(float(np.median(vals)), 0) if vals else None
+
+    return {
+        "metric": "causal prefill pipeline trace (diagnostic build, not a timing)",
+        "workload": cfg.name, "units": "SM cycles, medians over CTAs 0-7, both heads, tiles 4-59",
+        "head_period": med(lambda c, x, j: t[c, x, j + 1, 0] - t[c, x, j, 0]),
+        "softmax_quarter0": {
+            "s_to_registers": med(lambda c, x, j: t[c, x, j, 8] - t[c, x, j, 0]),
+            "row_max": med(lambda c, x, j: t[c, x, j, 9] - t[c, x, j, 8]),
+            "exponentials_and_p_stores": med(lambda c, x, j: t[c, x, j, 10] - t[c, x, j, 9]),
+            "to_release": med(lambda c, x, j: t[c, x, j, 4] - t[c, x, j, 10])},
+        "softmax_slowest_quarter": med(lambda c, x, j: max(t[c, x, j, 4:8]) - min(t[c, x, j, 0:4])),
+        "last_release_to_mma_passing_wait": med(lambda c, x, j: t[c, x, j, 12] - max(t[c, x, j, 4:8])),
+        "mma_wait_started_after_last_release": med(lambda c, x, j: t[c, x, j, 11] - max(t[c, x, j, 4:8])),
+        "issue_pv": med(lambda c, x, j: t[c, x, j, 13] - t[c, x, j, 12]),
+        "issue_next_s": med(lambda c, x, j: t[c, x, j, 14] - t[c, x, j, 13]),
+        "next_s_issued_to_softmax_sees_it": med(lambda c, x, j: min(t[c, x, j + 1, 0:4]) - t[c, x, j, 14]),
+        "mma_head_b_done_to_v_wait": med(lambda c, x, j: t[c, 0, j + 1, 15] - t[c, 1, j, 14]),
+        "head_b_offset": med(lambda c, x, j: t[c, 1, j, 0] - t[c, 0, j, 0]),
+    }
+
+
+def run_mma_rate(args):
+    """Cycles per tcgen05.mma of each operand form the tensor-core kernels use
+    (trace build; one CTA per SM, zero operands), against the nominal 8192
+    bf16 FLOP per clock per SM.  A diagnostic, not a timing of the path."""
+    g = _trace_build()
+    forms = ((0, "SS N=128", 64), (1, "TS N=128", 64), (2, "SS N=256", 128), (3, "SS N=64", 32),
+             (4, "TS N=128, B MN-major (P V)", 64), (5, "prefill head step: 8 SS + 8 TS", 64))
+    out = {"metric": "tcgen05.mma issue rate (diagnostic build, not a timing)",
+           "units": "SM cycles per instruction, median over SMs; M = 128, K = 16, bf16 -> fp32",
+           "iters": 512, "forms": {}}
+    for form, name, nominal in forms:
+        st, cyc = g.gqa_trace_mma_rate(form, 512)
+        if st != g.GQA_OK:
+            raise RuntimeError(f"gqa_trace_mma_rate({form}) -> {g.status_str(st)}")
+        out["forms"][name] = {"cycles": round(cyc, 1), "nominal": nominal,
+                              "fraction_of_nominal": round(nominal / cyc, 3)}
+    return out
+
+
 def run_workload(name, args):
     """One JSON line for a workload other than the headline step (same timing rules)."""
     import torch
@@ -908,6 +986,10 @@ def run_workload(name, args):
 
     if name == "decode_trace":
         return run_decode_trace(args)
+    if name == "mma_rate":
+        return run_mma_rate(args)
+    if name == "prefill_trace":
+        return run_prefill_trace(args)
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     g.load()

@@ -40,6 +40,8 @@ from ._binding import (  # noqa: E402,F401
     gqa_attn_prefill_chunk_workspace_bytes,
     gqa_last_device_error,
     gqa_trace_clear,
+    gqa_trace_mma_rate,
+    gqa_trace_prefill_read,
     gqa_trace_read,
     gqa_selftest_wait_timeout,
     gqa_set_wait_limit_ns,

@@ -50,6 +50,8 @@ SIGNATURES = {
     "gqa_last_device_error": (_I, [_P]),
     "gqa_trace_clear": (_I, []),
     "gqa_trace_read": (_I, [_P, _SZ]),
+    "gqa_trace_mma_rate": (_I, [_I, _I, _P]),
+    "gqa_trace_prefill_read": (_I, [_P, _SZ]),
     "gqa_set_wait_limit_ns": (_U64, [_U64]),
     "gqa_selftest_wait_timeout": (_I, [_U64, _P]),
 }
@@ -229,6 +231,20 @@ def gqa_attn_prefill_chunk_split(q, k_cache, v_cache, seq_lens, B, T_q, S_max, H
 
 def gqa_trace_clear() -> int:
     return load().gqa_trace_clear()
+
+
+def gqa_trace_prefill_read(host, nbytes: int) -> int:
+    """Copy the causal prefill's trace records into `host` (address or array)."""
+    addr = host if isinstance(host, int) else (
+        host.ctypes.data if hasattr(host, "ctypes") else host.data_ptr())
+    return load().gqa_trace_prefill_read(addr, nbytes)
+
+
+def gqa_trace_mma_rate(form: int, iters: int):
+    """Return (status, SM cycles per tcgen05.mma of `form`) from the trace build."""
+    out = ctypes.c_double(0.0)
+    st = load().gqa_trace_mma_rate(int(form), int(iters), ctypes.addressof(out))
+    return st, out.value
 
 
 def gqa_trace_read(host, nbytes: int) -> int:

@@ -1437,7 +1437,10 @@ cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t 
 extern "C" gqa_status gqa_trace_clear(void) {
   if (!gqa::kTrace) return GQA_ERR_UNSUPPORTED;
   static unsigned long long zeros[gqa::kTraceCtas * gqa::kTraceWords];
-  return cudaMemcpyToSymbol(gqa::g_trace, zeros, sizeof zeros) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  return cudaMemcpyToSymbol(gqa::g_trace, zeros, sizeof zeros) == cudaSuccess &&
+                 gqa::prefill_trace_clear() == cudaSuccess
+             ? GQA_OK
+             : GQA_ERR_CUDA;
 }
 
 extern "C" gqa_status gqa_trace_read(void* host, size_t bytes) {

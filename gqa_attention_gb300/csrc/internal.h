@@ -107,6 +107,8 @@ cudaError_t launch_prefill_chunk(const PrefillParams& p, const CUtensorMap& tm_q
                                  const CUtensorMap& tm_k, const CUtensorMap& tm_v, int num_sms,
                                  cudaStream_t stream);
 cudaError_t launch_prefill_merge(const PrefillParams& p, cudaStream_t stream);
+// Trace build: zero the causal prefill's stamp records (no-op otherwise).
+cudaError_t prefill_trace_clear();
 cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t stream);
 
 // Layout of the decode workspace: byte offset of the O partials.

@@ -45,10 +45,42 @@
 // for any reference value, not only the running maximum).
 #include <climits>
 
+#include "gqa_attn.h"
 #include "tcgen05.cuh"
 
+#ifndef GQA_TRACE
+#define GQA_TRACE 0
+#endif
+
 namespace gqa {
+
+// A build with GQA_TRACE=1 records clock64 stamps of the causal kernel's
+// pipeline: for the first work item of CTAs 0..7 and its first 64 key tiles,
+// one record of 16 words per (CTA, head X of the pair, tile j), laid out
+// [CTA][X][j][word]; see gqa_trace_prefill_read in the public header.
+constexpr bool kPTrace = GQA_TRACE != 0;
+constexpr int kPtCtas = 8, kPtTiles = 64, kPtWords = 16;
+__device__ unsigned long long g_ptrace[kPTrace ? kPtCtas * 2 * kPtTiles * kPtWords : 1];
+
+cudaError_t prefill_trace_clear() {
+  if (!kPTrace) return cudaSuccess;
+  static unsigned long long zeros[kPtCtas * 2 * kPtTiles * kPtWords];
+  return cudaMemcpyToSymbol(g_ptrace, zeros, sizeof zeros);
+}
+
 namespace {
+
+// Stamp word `w` of the record of (this CTA, head x, tile j) of the CTA's
+// first item (k == 0); a no-op in other builds.
+__device__ __forceinline__ void pt_stamp(int k, int x, int j, int w) {
+  if constexpr (kPTrace) {
+    if (k == 0 && blockIdx.x < kPtCtas && j < kPtTiles) {
+      unsigned long long t;
+      asm volatile("mov.u64 %0, %%clock64;" : "=l"(t)::"memory");
+      g_ptrace[((blockIdx.x * 2 + x) * kPtTiles + j) * kPtWords + w] = t;
+    }
+  }
+}
 
 constexpr int kPThreads = 384;
 // Shared-memory layout for tiles of 128 rows x DP bf16 columns (DP = 64 or 128).
@@ -305,6 +337,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (n == 1) tc_commit(smem_u32(&q_empty));
           for (int j = 0; ok && j < n; ++j) {
             const uint32_t vslot = ring % kSlots;
+            if (lane == 0) pt_stamp(k, 0, j, 15);
             if (!wait_all(&slot_full[vslot], (ring / kSlots) & 1)) {
               ok = false;
               break;
@@ -312,11 +345,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
             ++ring;
             const bool more = j + 1 < n;
             for (int x = 0; x < nx; ++x) {
+              if (lane == 0) pt_stamp(k, x, j, 11);
               if (!wait_all(&p_ready[x], pr_ph[x])) {
                 ok = false;
                 break;
               }
               pr_ph[x] ^= 1;
+              if (lane == 0) pt_stamp(k, x, j, 12);
               if (j == 0 && o_busy[x]) {  // the previous item's epilogue must have read O_x
                 if (!wait_all(&o_empty[x], oe_ph[x])) {
                   ok = false;
@@ -327,6 +362,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
               }
               tc_fence_after();
               issue_pv(x, vslot, j > 0);
+              if (lane == 0) pt_stamp(k, x, j, 13);
               if (more) {
                 if (x == 0) {
                   kslot = ring % kSlots;
@@ -339,6 +375,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
                 issue_s(x, kslot);
                 tc_commit(smem_u32(&s_full[x]));
+                if (lane == 0) pt_stamp(k, x, j, 14);
               } else {
                 tc_commit(smem_u32(&o_full[x]));
                 o_busy[x] = true;
@@ -396,6 +433,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           break;
         }
         s_ph ^= 1;
+        if (lane == 0) pt_stamp(k, x, j, quarter);
         tc_fence_after();
         uint32_t sr[128];
 #pragma unroll
@@ -404,6 +442,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+        if (quarter == 0 && lane == 0) pt_stamp(k, x, j, 8);
 
         // Row maximum.  Diagonal tile: key column c is visible from row r iff
         // c <= r (select, only on this tile); other tiles are unmasked.
@@ -433,6 +472,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
             m4[t] = fmax3(m4[t], __uint_as_float(sr[c + 2 * t]), __uint_as_float(sr[c + 2 * t + 1]));
         }
         const float m_tile = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * c2;  // c2 > 0
+        if constexpr (kPTrace) {  // stamp once the maximum is known
+          float mt = m_tile;
+          asm volatile("mov.b32 %0, %0;" : "+f"(mt));
+          if (quarter == 0 && lane == 0) pt_stamp(k, x, j, 9);
+        }
         float alpha = 1.f;
         bool rescale = false;
         // First tile (causal: key 0 is always visible), or, in chunk mode, no
@@ -473,6 +517,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
           tmem_st8(tS + c0 / 2, pk);
         }
         l = l * alpha + ((sa0 + sa1) + (sb0 + sb1));
+        if constexpr (kPTrace) {  // stamp once the exponentials are summed
+          float lt = l;
+          asm volatile("mov.b32 %0, %0;" : "+f"(lt));
+          if (quarter == 0 && lane == 0) pt_stamp(k, x, j, 10);
+        }
 
         // O rows of this warp whose reference moved: O *= alpha.  O is stable:
         // the commit that signalled S also covered the previous P V; the next
@@ -517,6 +566,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
+        if (lane == 0) pt_stamp(k, x, j, 4 + quarter);
         if (lane == 0) mbar_arrive(smem_u32(&p_ready[x]));
       }
       if (!alive) break;
@@ -715,3 +765,12 @@ cudaError_t launch_prefill_chunk(const PrefillParams& p, const CUtensorMap& tm_q
 }
 
 }  // namespace gqa
+
+extern "C" gqa_status gqa_trace_prefill_read(void* host, size_t bytes) {
+  if (!gqa::kPTrace) return GQA_ERR_UNSUPPORTED;
+  constexpr size_t total =
+      sizeof(unsigned long long) * gqa::kPtCtas * 2 * gqa::kPtTiles * gqa::kPtWords;
+  if (!host || bytes > total) return GQA_ERR_INVALID_ARG;
+  return cudaMemcpyFromSymbol(host, gqa::g_ptrace, bytes) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+

@@ -257,6 +257,34 @@ gqa_status gqa_attn_decode_noalloc(const void* q, const void* k_cache, const voi
 gqa_status gqa_trace_clear(void);
 gqa_status gqa_trace_read(void* host, size_t bytes);
 
+/* Trace build only: clock64 stamps (SM cycles) of the causal prefill's pipeline
+ * (gqa_attn_prefill_causal and the chunk kernels), for the first work item of
+ * CTAs 0..7 of the last launch and that item's first 64 key tiles: records of
+ * 16 64-bit words laid out [CTA 0..7][head X 0..1 of the pair][tile j 0..63].
+ * Words 0-3: softmax warp of tensor-memory quarter q saw S_X(j) ready; 4-7:
+ * quarter q released P_X(j); 8, 9, 10: quarter 0 had S in registers, the row
+ * maximum, and the exponentials summed; 11, 12: the MMA warp started and
+ * passed its wait for P_X(j); 13: it had issued O_X += P_X(j) V_j; 14: it had
+ * issued and committed S_X(j + 1) (absent on the item's last tile); 15 (head A's
+ * records only): it started waiting for V_j.  Unwritten words stay 0 after
+ * gqa_trace_clear, which zeroes these records too.  GQA_ERR_INVALID_ARG for a
+ * null `host` or more than 8 * 2 * 64 * 16 * 8 bytes. */
+gqa_status gqa_trace_prefill_read(void* host, size_t bytes);
+
+/* Trace build only: the issue rate of one tcgen05.mma form (M = 128, K = 16,
+ * bf16 in, fp32 accumulate).  One CTA per SM issues `iters` rounds of
+ * back-to-back instructions on zero operands from one converged warp; the
+ * median over SMs of SM clock cycles per instruction is written to
+ * *cycles_per_instruction (host memory).  Forms: 0 A and B in shared memory
+ * (SS), N = 128; 1 A in tensor memory (TS), N = 128; 2 SS, N = 256; 3 SS,
+ * N = 64; 4 TS, N = 128 with B MN-major; 5 the causal prefill's per-head step
+ * (8 SS then 8 TS, N = 128, head and ring slot chosen at run time).  Nominal:
+ * 32 cycles at N = 64, 64 at N = 128, 128 at N = 256 (8192 FLOP per clock per
+ * SM).  Synchronous; uses the whole device.  GQA_ERR_INVALID_ARG for a null
+ * pointer, a form outside 0..5 or iters outside 1..65536; GQA_ERR_TIMEOUT if
+ * the final commit did not land within 2 s. */
+gqa_status gqa_trace_mma_rate(int form, int iters, double* cycles_per_instruction);
+
 /* ------------------------------------------------------------------------
  * Causal prefill ("Attention Kernel 계보", p.9 §4 and p.13 §1-§6)
  * ------------------------------------------------------------------------

@@ -128,10 +128,12 @@ def test_wait_limit_setter_round_trips(lib):
 
 
 def test_trace_calls_are_unsupported_in_the_default_build(lib):
-    """The default library records no trace: both diagnostics calls say so
+    """The default library records no trace: every diagnostics call says so
     without touching the GPU."""
     import numpy as np
 
     buf = np.zeros(64, dtype=np.uint64)
     assert g.gqa_trace_clear() == g.GQA_ERR_UNSUPPORTED
     assert g.gqa_trace_read(buf, buf.nbytes) == g.GQA_ERR_UNSUPPORTED
+    assert g.gqa_trace_mma_rate(0, 1)[0] == g.GQA_ERR_UNSUPPORTED
+    assert g.gqa_trace_prefill_read(buf, buf.nbytes) == g.GQA_ERR_UNSUPPORTED
