@@ -181,8 +181,8 @@ gqa_status gqa_attn_decode_paged(const void* q, const void* k_pool, const void* 
  *                     (else GQA_ERR_UNSUPPORTED)
  * Every other argument, the workspace and the follow-up combine are those of
  * gqa_attn_decode().  Codes and scales past seq_lens[b] are never used.  The
- * on-chip conversion favours two CTAs per SM: twice
- * gqa_attn_decode_default_splits() measured best. */
+ * on-chip conversion favours several CTAs per SM: three times
+ * gqa_attn_decode_default_splits() measured best (three CTAs per SM). */
 gqa_status gqa_attn_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
                                const float* k_scale, const float* v_scale,
                                const int32_t* seq_lens, int B, int S_max, int H_q, int H_kv,
