@@ -884,7 +884,7 @@ def run_decode_trace(args):
                                        for j, k in enumerate(("warp_rendezvous", "partials_to_smem",
                                                               "merge_and_store"))},
             "prologue_cycles_median": {k: float(np.median(rec[:, 59 + j]))
-                                       for j, k in enumerate(("seq_len_read", "barrier_setup",
+                                       for j, k in enumerate(("seq_len_read", "length_checks",
                                                               "query_fragments"))},
             "timeline_us_min_median_max": {
                 "entry": pct(rel[:, 0]), "release": pct(rel[:, 1]), "loop_start": pct(rel[:, 2]),

@@ -269,8 +269,20 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
     return ((size_t)b * p.T_q + tq) * p.H_q + h0 + (x - tq * G);
   };
   const size_t n_rows = (size_t)p.B * p.T_q * p.H_q;  // rows of out, lse and the workspace
+  // The ring's barriers touch shared memory only: they are set up while the
+  // previous kernel finishes (the CTA barrier that publishes them comes
+  // before the dependency wait as well).
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), kConsumerWarps);
+    }
+    abort_flag = 0;
+    bad_page = 0;
+    fence_barrier_init();
+  }
   // Launched as a programmatic dependent of the previous kernel in the stream:
-  // nothing is read or written before that kernel has completed.  While it
+  // no global memory is read or written before that kernel has completed.  While it
   // finishes, the producer warp of each split's first row group prefetches the
   // split's first K/V tiles into L2, one (tile, page segment) per lane.  The
   // extent comes from relaxed loads of seq_lens[b] and, for a paged cache, of
@@ -320,6 +332,7 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
       }
     }
   }
+  __syncthreads();
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const unsigned long long tr_release = kTrace ? globaltimer_ns() : 0ull;
   const unsigned long long tp0 = trace_clock();
@@ -355,16 +368,6 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
   const int t_end = min(t0 + p.chunk, L);
   const int n_tiles = t_end > t0 ? (t_end - t0 + kTile - 1) / kTile : 0;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(smem_u32(&full_bar[s]), 1);
-      mbar_init(smem_u32(&empty_bar[s]), kConsumerWarps);
-    }
-    abort_flag = 0;
-    bad_page = 0;
-    fence_barrier_init();
-  }
-  __syncthreads();
   const unsigned long long tp2 = trace_clock();
 
   // ------------------------------------------------------------ producer ----
@@ -915,7 +918,7 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
     tr_rec[57] = te2 - te1;            // partials into shared memory
     tr_rec[58] = trace_clock() - te2;  // merge and global stores
     tr_rec[59] = tp1 - tp0;            // the sequence length read after the release
-    tr_rec[60] = tp2 - tp1;            // barrier set-up and the CTA barrier
+    tr_rec[60] = tp2 - tp1;            // the length checks before the roles start
     tr_rec[61] = tp3 - tp2;            // the query fragments
     unsigned smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));

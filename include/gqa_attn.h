@@ -247,8 +247,8 @@ gqa_status gqa_attn_decode_noalloc(const void* q, const void* k_cache, const voi
  * handled; words 56-58: the epilogue's cycles on thread 0 waiting for the
  * other consumer warps, writing the warp partials to shared memory, and
  * merging them and storing the result; words 59-61: the prologue's cycles on
- * thread 0 after the dependency wait reading the sequence length, setting up
- * the barriers, and loading the query fragments.  CTAs that return before their tile
+ * thread 0 after the dependency wait reading the sequence length, checking it
+ * (the barriers are set up before the wait), and loading the query fragments.  CTAs that return before their tile
  * loop (empty splits, bad lengths) write no record.
  * gqa_trace_clear zeroes every record (synchronous); gqa_trace_read copies the
  * first `bytes` bytes (at most 4096 * 64 * 8) into `host` after the stream has
