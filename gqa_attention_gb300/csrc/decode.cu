@@ -53,7 +53,7 @@ __device__ __forceinline__ void trace_ready(float& v) {
 #endif
 
 #ifndef GQA_DECODE_STAGES_FP8
-#define GQA_DECODE_STAGES_FP8 3  // FP8 stages are half as large as bf16 ones
+#define GQA_DECODE_STAGES_FP8 4  // 16.5 KB each: three CTAs of four stages fit an SM
 #endif
 #ifndef GQA_DECODE_STAGES_FP8_ONE_WAVE
 #define GQA_DECODE_STAGES_FP8_ONE_WAVE 8  // FP8, every CTA has an SM to itself

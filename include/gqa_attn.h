@@ -40,7 +40,7 @@
  * - The same over a paged cache: gqa_attn_decode_paged (+ combine).
  * - An E4M3 cache with per-token scales: gqa_attn_decode_fp8 /
  *   gqa_attn_decode_paged_fp8 (+ combine) with 3x the default split count
- *   (16.1-16.3 us per step at 32K).
+ *   (15.9-16.3 us per step at 32K).
  * - A few new tokens per sequence (speculative verification, T_q <= 64):
  *   gqa_attn_decode_multi / gqa_attn_decode_paged_multi (+ combine with B * T_q
  *   rows); above 16 query rows per KV head at d = 128 they run on the tensor
