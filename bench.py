@@ -348,6 +348,7 @@ class DecodeLeg:
         self.torch, self.g, self.cfg, self.dev = torch, g, cfg, dev
         q, k, v, lens = inputs.decode_inputs_for(cfg, seed=seed)
         self.host = (q, k, v, lens)
+        self.lens_host = lens
         self.kv_bytes = 4 * cfg.d * cfg.H_kv * int(lens.sum())
         self.copies = n_copies(self.kv_bytes)
         self.qd, self.ld = q.to(dev), lens.to(dev)
@@ -394,6 +395,46 @@ class DecodeLeg:
 
     def results(self):
         return self.out.float().cpu(), self.lse.float().cpu()
+
+
+class Fp8DecodeLeg(DecodeLeg):
+    """The decode workload over an E4M3 cache with per-token scales: FP8 split
+    kernel (three times the default split count) + combine, rotating cache copies."""
+
+    def __init__(self, torch, g, cfg, dev, seed=0):
+        from gqa_attention_gb300 import inputs
+
+        self.torch, self.g, self.cfg, self.dev = torch, g, cfg, dev
+        q, k8, v8, ks, vs, lens = inputs.decode_inputs_fp8(cfg.B, cfg.H_q, cfg.H_kv, cfg.d,
+                                                           cfg.S_max, seed=seed, ragged=cfg.ragged)
+        self.host = (q, k8, v8, ks, vs, lens)
+        self.lens_host = lens
+        # bytes the sweep must read: E4M3 codes + one fp32 scale per token, for K and V
+        self.kv_bytes = 2 * int(lens.sum()) * (cfg.H_kv * cfg.d + 4)
+        self.copies = n_copies(self.kv_bytes)
+        self.qd, self.ld = q.to(dev), lens.to(dev)
+        self.caches = []
+        for t in (k8, v8, ks, vs):  # all copies in one allocation per tensor
+            a = torch.empty((self.copies,) + tuple(t.shape), dtype=t.dtype, device=dev)
+            a.copy_(t.to(dev).unsqueeze(0).expand_as(a))
+            self.caches.append(a)
+        self.n_split = 3 * g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, dev.index)
+        self.ws = g.decode_workspace(cfg.B, cfg.H_q, cfg.d, self.n_split, dev)
+        self.out = torch.empty(cfg.B, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(cfg.B, cfg.H_q, dtype=torch.float32, device=dev)
+        self.launches_per_step = 2 if self.n_split > 1 else 1
+        self.ws_bytes = (g.gqa_attn_decode_workspace_bytes(cfg.B, cfg.H_q, cfg.d, self.n_split)
+                         if self.n_split > 1 else 0)
+
+    def split(self, i, stream):
+        c, g = self.cfg, self.g
+        j = i % self.copies
+        kc, vc, ksc, vsc = (a[j] for a in self.caches)
+        st = g.gqa_attn_decode_fp8(self.qd, kc, vc, ksc, vsc, self.ld, c.B, c.S_max, c.H_q,
+                                   c.H_kv, c.d, c.scale, self.n_split, self.ws, self.out,
+                                   self.lse, stream)
+        if st:
+            raise RuntimeError(f"FP8 decode failed: {g.status_str(st)}")
 
 
 class PrefillLeg:
@@ -466,8 +507,11 @@ def run_ours(args, rank, world, dist):
     pre = PrefillLeg(torch, g, inputs.LLAMA70B_PREFILL_8K, dev) if want_prefill else None
     extra = {}
     if want_configs:
+        # (the power-heavy 64K prefill last: the compute-bound FP8 decode is
+        # sensitive to the clocks a long prefill leaves behind)
         extra["decode_tiny"] = DecodeLeg(torch, g, inputs.TINY_DECODE, dev)
         extra["decode_ragged"] = DecodeLeg(torch, g, inputs.LLAMA70B_DECODE_RAGGED, dev)
+        extra["decode_fp8"] = Fp8DecodeLeg(torch, g, inputs.LLAMA70B_DECODE, dev)
         extra["prefill_64k"] = PrefillLeg(torch, g, inputs.PREFILL_64K, dev)
     legs = [x for x in (dec, pre, *extra.values()) if x is not None]
 
@@ -573,7 +617,7 @@ def run_ours(args, rank, world, dist):
                         "frac_of_" + peak_kind + "_hbm": round(gbs / world / hbm_gbs, 4),
                         "frac_of_nominal_8TBs": round(gbs / world / NOMINAL_HBM_GBS, 4),
                         "B": c.B, "H_q": c.H_q, "H_kv": c.H_kv, "d": c.d, "S_max": c.S_max,
-                        "seq_lens": [int(x) for x in leg.host[3]] if c.B > 1 else c.S_max,
+                        "seq_lens": [int(x) for x in leg.lens_host] if c.B > 1 else c.S_max,
                         "n_split": leg.n_split, "kv_bytes": leg.kv_bytes,
                         "all_bytes": leg.all_bytes(),
                         "all_bytes_GBs": round(leg.all_bytes() / (first * 1e-3) / 1e9, 2),
@@ -587,10 +631,16 @@ def run_ours(args, rank, world, dist):
                 kern_ms = s_first
             else:
                 kern_ms = first
-            traffic = (_recorded_traffic("decode_split_llama70b_ctx32768.md", DECODE_SOURCES)
+            fp8 = isinstance(leg, Fp8DecodeLeg)
+            profile = ("decode_fp8_llama70b_ctx32768.md" if fp8 else
+                       "decode_split_llama70b_ctx32768.md")
+            traffic = (_recorded_traffic(profile, DECODE_SOURCES)
                        if c is inputs.LLAMA70B_DECODE else None)
-            rep["roofline"] = _hbm_roofline("gqa_decode_split_kernel", leg.kv_bytes, kern_ms,
-                                            hbm_gbs, peak_kind, traffic)
+            rep["roofline"] = _hbm_roofline(
+                "gqa_decode_split_kernel" + (" (E4M3 cache)" if fp8 else ""), leg.kv_bytes,
+                kern_ms, hbm_gbs, peak_kind, traffic)
+            if fp8:
+                rep["dtype"] = "e4m3 cache with fp32 per-token scales, bf16 q/out"
         else:
             tf = whole_job_rate(world, leg.flops, first * 1e-3) / 1e12
             rep.update({"value": round(tf, 2), "unit": "TFLOP/s",
@@ -683,6 +733,8 @@ def run_ours(args, rank, world, dist):
             "decode_ragged": reports["decode_ragged"] | {"workload": inputs.LLAMA70B_DECODE_RAGGED.name},
             "prefill_8k": {"see": "prefill", "workload": inputs.LLAMA70B_PREFILL_8K.name},
             "prefill_64k": reports["prefill_64k"] | {"workload": inputs.PREFILL_64K.name},
+            "decode_fp8": reports["decode_fp8"] | {"workload": inputs.LLAMA70B_DECODE.name
+                                                   + " with an E4M3 cache (FP8 bytes)"},
         }
     # the oracle on the host cores (and the parity of every timed output
     # against it): a single-GPU figure, taken on rank 0 at N = 1
@@ -695,7 +747,7 @@ def run_ours(args, rank, world, dist):
         if pr and "prefill_8k" in cpu:
             line["prefill"]["cpu_baseline"] = cpu["prefill_8k"]["cpu_baseline"]
             line["prefill"]["parity"] = cpu["prefill_8k"]["parity"]
-        for name in ("decode_tiny", "decode_ragged", "prefill_64k"):
+        for name in ("decode_tiny", "decode_ragged", "prefill_64k", "decode_fp8"):
             if want_configs and name in cpu:
                 line["configs"][name].update(cpu[name])
     else:
@@ -732,21 +784,32 @@ def cpu_baseline(legs, results):
         if leg is None:
             continue
         if isinstance(leg, DecodeLeg):
-            q, k, v, lens = leg.host
+            if isinstance(leg, Fp8DecodeLeg):
+                q, k8, v8, ks, vs, lens = leg.host
+
+                def run(n):
+                    return oracle.decode_fp8(q, k8, v8, ks, vs, lens, leg.cfg.scale, nthreads=n)
+            else:
+                q, k, v, lens = leg.host
+
+                def run(n):
+                    return oracle.decode(q, k, v, lens, leg.cfg.scale, nthreads=n)
             reps = 5 if leg.kv_bytes < (256 << 20) else 1
             times = []
             for _ in range(reps):
                 t0 = time.perf_counter()
-                ref_o, ref_l = oracle.decode(q, k, v, lens, leg.cfg.scale, nthreads=cores)
+                ref_o, ref_l = run(cores)
                 times.append(time.perf_counter() - t0)
             t = statistics.median(times)
             cb = {"value": round(leg.kv_bytes / t / 1e9, 4), "unit": "GB/s", "cores": cores,
                   "cpu": model, "kind": "oracle",
-                  "sample": f"whole {leg.cfg.name} decode (every query head, every visible key), "
+                  "sample": f"whole {leg.cfg.name} decode"
+                            f"{' over the E4M3 cache' if isinstance(leg, Fp8DecodeLeg) else ''}"
+                            " (every query head, every visible key), "
                             f"fp64, median of {reps} run(s), {t:.3f} s each"}
             if leg.kv_bytes < (256 << 20):  # the same sample on one core
                 t0 = time.perf_counter()
-                oracle.decode(q, k, v, lens, leg.cfg.scale, nthreads=1)
+                run(1)
                 cb["value_1core"] = round(leg.kv_bytes / (time.perf_counter() - t0) / 1e9, 4)
             o_gpu, l_gpu = results[id(leg)]
             par = _parity(o_gpu, l_gpu, ref_o, ref_l, "every output row")
