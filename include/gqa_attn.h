@@ -35,17 +35,17 @@
  * Which call for which workload (measured on GB300, Llama3-70B heads, 32K cache)
  * -------------------------------------------------------------------------
  * - One new token per sequence, contiguous cache: gqa_attn_decode with
- *   gqa_attn_decode_default_splits, then gqa_attn_decode_combine (23.4-23.7 us
- *   per step; the split kernel streams K/V at 95-96% of the measured HBM rate).
+ *   gqa_attn_decode_default_splits, then gqa_attn_decode_combine (23.3-23.8 us
+ *   per step; the split kernel streams K/V at 95-97% of the measured HBM rate).
  * - The same over a paged cache: gqa_attn_decode_paged (+ combine).
  * - An E4M3 cache with per-token scales: gqa_attn_decode_fp8 /
  *   gqa_attn_decode_paged_fp8 (+ combine) with 3x the default split count
- *   (15.9-16.3 us per step at 32K).
+ *   (15.8-16.3 us per step at 32K).
  * - A few new tokens per sequence (speculative verification, T_q <= 64):
  *   gqa_attn_decode_multi / gqa_attn_decode_paged_multi (+ combine with B * T_q
  *   rows); above 16 query rows per KV head at d = 128 they run on the tensor
  *   cores (T_q = 8: 25.5 us, against 397 us through the chunked prefill).
- * - A prompt: gqa_attn_prefill_causal (tensor cores, 86% of the measured
+ * - A prompt: gqa_attn_prefill_causal (tensor cores, 86-87% of the measured
  *   dense bf16 rate at d = 128; d = 64 and 32 at about half and a quarter).
  * - A chunk of queries ending a cached sequence, optionally with a sliding
  *   window: gqa_attn_prefill_chunk, or gqa_attn_prefill_chunk_split for long
