@@ -342,7 +342,7 @@ def _repeat_stats(ms_list):
 class DecodeLeg:
     """A decode workload: split kernel (+ combine when split) over rotating cache copies."""
 
-    def __init__(self, torch, g, cfg, dev, seed=0):
+    def __init__(self, torch, g, cfg, dev, seed=0, balanced=False):
         from gqa_attention_gb300 import inputs
 
         self.torch, self.g, self.cfg, self.dev = torch, g, cfg, dev
@@ -361,6 +361,9 @@ class DecodeLeg:
         del kd, vd
         self.n_split = g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, dev.index)
         self.ws = g.decode_workspace(cfg.B, cfg.H_q, cfg.d, self.n_split, dev)
+        # balanced splits: the claim counters, zeroed once (every call leaves them at zero)
+        self.counters = (g.decode_counters(cfg.B, cfg.H_kv, dev)
+                         if balanced and self.n_split > 1 else None)
         self.out = torch.empty(cfg.B, cfg.H_q, cfg.d, dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty(cfg.B, cfg.H_q, dtype=torch.float32, device=dev)
         self.launches_per_step = 2 if self.n_split > 1 else 1
@@ -370,9 +373,14 @@ class DecodeLeg:
     def split(self, i, stream):
         c, g = self.cfg, self.g
         j = i % self.copies
-        st = g.gqa_attn_decode(self.qd, self.kall[j], self.vall[j], self.ld, c.B, c.S_max, c.H_q,
-                               c.H_kv, c.d, c.scale, self.n_split, self.ws, self.out, self.lse,
-                               stream)
+        if self.counters is not None:
+            st = g.gqa_attn_decode_balanced(self.qd, self.kall[j], self.vall[j], self.ld, c.B,
+                                            c.S_max, c.H_q, c.H_kv, c.d, c.scale, self.n_split,
+                                            self.ws, self.counters, self.out, self.lse, stream)
+        else:
+            st = g.gqa_attn_decode(self.qd, self.kall[j], self.vall[j], self.ld, c.B, c.S_max,
+                                   c.H_q, c.H_kv, c.d, c.scale, self.n_split, self.ws, self.out,
+                                   self.lse, stream)
         if st:
             raise RuntimeError(f"decode failed: {g.status_str(st)}")
 
@@ -510,7 +518,9 @@ def run_ours(args, rank, world, dist):
         # (the power-heavy 64K prefill last: the compute-bound FP8 decode is
         # sensitive to the clocks a long prefill leaves behind)
         extra["decode_tiny"] = DecodeLeg(torch, g, inputs.TINY_DECODE, dev)
-        extra["decode_ragged"] = DecodeLeg(torch, g, inputs.LLAMA70B_DECODE_RAGGED, dev)
+        # (the ragged batch through the balanced splits: 1.5% faster than fixed ones)
+        extra["decode_ragged"] = DecodeLeg(torch, g, inputs.LLAMA70B_DECODE_RAGGED, dev,
+                                           balanced=True)
         extra["decode_fp8"] = Fp8DecodeLeg(torch, g, inputs.LLAMA70B_DECODE, dev)
         extra["prefill_64k"] = PrefillLeg(torch, g, inputs.PREFILL_64K, dev)
     legs = [x for x in (dec, pre, *extra.values()) if x is not None]
@@ -641,6 +651,10 @@ def run_ours(args, rank, world, dist):
                 kern_ms, hbm_gbs, peak_kind, traffic)
             if fp8:
                 rep["dtype"] = "e4m3 cache with fp32 per-token scales, bf16 q/out"
+            rep["entry"] = ("gqa_attn_decode_fp8" if fp8 else "gqa_attn_decode_balanced"
+                            if getattr(leg, "counters", None) is not None else "gqa_attn_decode")
+            if leg.n_split > 1:
+                rep["entry"] += " + gqa_attn_decode_combine"
         else:
             tf = whole_job_rate(world, leg.flops, first * 1e-3) / 1e12
             rep.update({"value": round(tf, 2), "unit": "TFLOP/s",
@@ -1075,7 +1089,7 @@ def run_workload(name, args):
 
     if name in ("decode_tiny", "decode_ragged"):
         cfg = inputs.TINY_DECODE if name == "decode_tiny" else inputs.LLAMA70B_DECODE_RAGGED
-        leg = DecodeLeg(torch, g, cfg, dev)
+        leg = DecodeLeg(torch, g, cfg, dev, balanced=name == "decode_ragged")
         for c in range(leg.copies):
             leg.step(c, stream)
         ms, rep = timed(leg.step, leg.copies)

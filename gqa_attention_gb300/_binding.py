@@ -28,6 +28,9 @@ SIGNATURES = {
     "gqa_attn_decode_default_splits": (_I, [_I, _I, _I, _I]),
     "gqa_attn_decode": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
     "gqa_attn_decode_combine": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
+    "gqa_attn_decode_counter_bytes": (_SZ, [_I, _I]),
+    "gqa_attn_decode_balanced": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P,
+                                      _P]),
     "gqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
     "gqa_attn_decode_paged": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P,
                                    _P, _P]),
@@ -135,6 +138,18 @@ def gqa_attn_decode(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale
 def gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream=None) -> int:
     return load().gqa_attn_decode_combine(_ptr(workspace), B, H_q, d, n_split, _ptr(out),
                                           _ptr(lse), _stream(stream))
+
+
+def gqa_attn_decode_counter_bytes(B: int, H_kv: int) -> int:
+    return load().gqa_attn_decode_counter_bytes(B, H_kv)
+
+
+def gqa_attn_decode_balanced(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale,
+                             n_split, workspace, counters, out, lse, stream=None) -> int:
+    return load().gqa_attn_decode_balanced(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+                                           B, S_max, H_q, H_kv, d, scale, n_split,
+                                           _ptr(workspace), _ptr(counters), _ptr(out), _ptr(lse),
+                                           _stream(stream))
 
 
 def gqa_attn_decode_multi(q, k_cache, v_cache, seq_lens, B, T_q, S_max, H_q, H_kv, d, scale,
@@ -282,9 +297,19 @@ def decode_workspace(B, H_q, d, n_split, device="cuda"):
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 
+def decode_counters(B, H_kv, device="cuda"):
+    """Zeroed claim counters for gqa_attn_decode_balanced (int32 [B, H_kv, 2])."""
+    import torch
+
+    return torch.zeros((B, H_kv, 2), dtype=torch.int32, device=device)
+
+
 def decode(q, k_cache, v_cache, seq_lens, scale=None, n_split=None, workspace=None, out=None,
-           lse=None, stream=None):
-    """Split-KV decode + combine on CUDA tensors; returns (out bf16 [B,H_q,d], lse fp32 [B,H_q])."""
+           lse=None, stream=None, counters=None):
+    """Split-KV decode + combine on CUDA tensors; returns (out bf16 [B,H_q,d], lse fp32 [B,H_q]).
+
+    With ``counters`` (from decode_counters, reusable across calls) the splits
+    are balanced (gqa_attn_decode_balanced)."""
     import torch
 
     B, H_q, d = q.shape
@@ -299,8 +324,13 @@ def decode(q, k_cache, v_cache, seq_lens, scale=None, n_split=None, workspace=No
         lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
     if n_split > 1 and workspace is None:
         workspace = decode_workspace(B, H_q, d, n_split, q.device)
-    _check(gqa_attn_decode(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale, n_split,
-                           workspace, out, lse, stream), "gqa_attn_decode")
+    if counters is None:
+        _check(gqa_attn_decode(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d, scale,
+                               n_split, workspace, out, lse, stream), "gqa_attn_decode")
+    else:
+        _check(gqa_attn_decode_balanced(q, k_cache, v_cache, seq_lens, B, S_max, H_q, H_kv, d,
+                                        scale, n_split, workspace, counters, out, lse, stream),
+               "gqa_attn_decode_balanced")
     if n_split > 1:
         _check(gqa_attn_decode_combine(workspace, B, H_q, d, n_split, out, lse, stream),
                "gqa_attn_decode_combine")

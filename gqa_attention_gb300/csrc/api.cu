@@ -243,6 +243,27 @@ gqa_status gqa_attn_decode(const void* q, const void* k_cache, const void* v_cac
   return cuda_status(gqa::launch_decode_split(p, tm_k, tm_v, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t gqa_attn_decode_counter_bytes(int B, int H_kv) {
+  if (B < 1 || H_kv < 1) return 0;
+  return (size_t)B * H_kv * 2 * sizeof(int32_t);
+}
+
+gqa_status gqa_attn_decode_balanced(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* seq_lens, int B, int S_max, int H_q, int H_kv,
+                                    int d, float scale, int n_split, void* workspace,
+                                    int32_t* counters, void* out, float* lse,
+                                    gqa_stream_t stream) {
+  if (n_split > 1 && (!counters || !aligned(counters, 4))) return GQA_ERR_INVALID_ARG;
+  CUtensorMap tm_k, tm_v;
+  gqa::DecodeParams p;
+  gqa_status st = prepare_decode(q, k_cache, v_cache, seq_lens, B, S_max, (long long)B * S_max,
+                                 gqa::kDecodeTile, H_q, H_kv, d, scale, n_split, workspace, out,
+                                 lse, &tm_k, &tm_v, &p);
+  if (st != GQA_OK) return st;
+  if (n_split > 1) p.tile_ctr = counters;
+  return cuda_status(gqa::launch_decode_split(p, tm_k, tm_v, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int gqa_attn_decode_multi_default_splits(int B, int T_q, int H_q, int H_kv, int S_max, int d) {
   if (B < 1 || T_q < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0) return 1;
   const int n = gqa_attn_decode_default_splits(B, H_kv, S_max, -1);

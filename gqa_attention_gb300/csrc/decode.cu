@@ -76,8 +76,23 @@ __device__ __forceinline__ void trace_ready(float& v) {
 constexpr int kTile = kDecodeTile;  // tokens per stage
 constexpr int kMaxClusterSplits = 16;
 constexpr int kConsumerWarps = 4;   // 16 tokens each
-constexpr int kPrefetchTiles = 6;   // tiles a split CTA may warm in L2 before its dependency wait
+#ifndef GQA_PREFETCH_TILES
+#define GQA_PREFETCH_TILES 6  // tiles a split CTA may warm in L2 before its dependency wait
+#endif
+constexpr int kPrefetchTiles = GQA_PREFETCH_TILES;
+static_assert(kPrefetchTiles >= 0 && kPrefetchTiles <= 32, "one tile per producer lane");
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
+
+// Balanced splits: each split CTA first streams a fixed share of about three
+// quarters of its (sequence, KV head)'s tiles; the CTAs then claim the
+// remaining tiles one at a time from a counter they share, so that a CTA that
+// streams faster than its neighbours takes more of the tail.
+constexpr int kStaticNum = 3, kStaticDen = 4;
+// Tiles of a balanced split's own share for a sequence of L tokens.
+__host__ __device__ __forceinline__ int balanced_static_tiles(int L, int n_split) {
+  const long long n_t = (static_cast<long long>(L) + kTile - 1) / kTile;
+  return static_cast<int>(n_t * kStaticNum / (static_cast<long long>(kStaticDen) * n_split));
+}
 
 template <int D>
 struct DecodeLayout {
@@ -218,7 +233,19 @@ __device__ __forceinline__ float online_update(float (&x)[4], float& m, float& l
 // alternate tiles, so that each SM has two warps per scheduler to hide the
 // latency of the per-tile E4M3 work; the eight warp partials are merged at
 // the end as the four are otherwise.
-template <int D, bool ROWS16, int NSTAGE, bool PAGED, bool FP8, bool CLUSTER, int NGRP = 1>
+// DYN = true (balanced splits, contiguous bf16 cache): split s first streams tiles
+// s*n_s .. s*n_s + n_s - 1 of its (sequence, KV head), n_s =
+// balanced_static_tiles(L, n_split); the tiles from n_split * n_s on form a
+// pool that the producer warps of all n_split CTAs claim one tile at a time
+// through p.tile_ctr[2 (b H_kv + kv)].  A split's partial then covers its
+// share plus the tiles it claimed: the keys of a partial need not be
+// contiguous, since the merge of "Attention Kernel 계보" p.4 is order-free.
+// The producer writes each stage's first token next to the stage and ends
+// the ring with a stage whose token is -1.  Every CTA that reaches the claims
+// then counts itself out on p.tile_ctr[... + 1]; the last one returns both
+// words to zero for the next call.
+template <int D, bool ROWS16, int NSTAGE, bool PAGED, bool FP8, bool CLUSTER, int NGRP = 1,
+          bool DYN = false>
 __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
                                   NGRP > 1 ? 1 : ((FP8 && !ROWS16) ? 3 : 2))
     gqa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -227,6 +254,8 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
                             const __grid_constant__ CUtensorMap tm_vs, const DecodeParams p) {
   static_assert(!(CLUSTER && (PAGED || FP8)), "the cluster merge serves the contiguous bf16 cache");
   static_assert(NGRP == 1 || (NGRP <= 3 && !CLUSTER), "several consumer groups: split CTAs only");
+  static_assert(!DYN || (!PAGED && !FP8 && !CLUSTER && NGRP == 1),
+                "balanced splits: a contiguous bf16 cache, one consumer group");
   constexpr int kCW = kConsumerWarps * NGRP;  // consumer warps
   constexpr int kThr = (kCW + 1) * 32;
   using Lay = DecodeLayout<D>;
@@ -239,6 +268,7 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
   __shared__ int abort_flag;
   __shared__ int bad_page;
   __shared__ int pages_sm[PAGED ? kMaxPagesPerCta : 1];
+  __shared__ int stage_tok[DYN ? NSTAGE : 1];  // balanced splits: first token of each stage
 
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -301,8 +331,11 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
     const int h = PAGED ? min(p.page_size, kTile) : kTile;  // rows per box
     const int subs = kTile / h;
     const int i = lane / subs, sub = lane % subs;
-    const int tk = split * p.chunk + i * kTile + sub * h;
-    const int tp_end = min(min(p.S_max, L_hint), split * p.chunk + p.chunk);
+    // (a balanced split prefetches from its own share of the tiles)
+    const int pchunk =
+        DYN ? balanced_static_tiles(max(0, min(p.S_max, L_hint)), p.n_split) * kTile : p.chunk;
+    const int tk = split * pchunk + i * kTile + sub * h;
+    const int tp_end = min(min(p.S_max, L_hint), split * pchunk + pchunk);
     if (i < p.prefetch_tiles && tk < tp_end) {
       int row = b * p.S_max + tk, sc_x = tk, sc_y = b;
       bool ok = true;
@@ -357,20 +390,109 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
     }
     return;
   }
-  const int t0 = split * p.chunk;
-  if (!CLUSTER && t0 >= L) {  // empty split: the merge identity (-inf, 0); O is not written
+  // Balanced splits: the CTA's own share; the claimed tiles may lie anywhere
+  // in [0, L), so the masks use the sequence end.
+  const int n_static = DYN ? balanced_static_tiles(L, p.n_split) : 0;
+  const int t0 = DYN ? split * n_static * kTile : split * p.chunk;
+  if (!CLUSTER && !DYN && t0 >= L) {  // empty split: the merge identity (-inf, 0); O is not written
     for (int r = threadIdx.x; r < R; r += kThr)
       if (in_bounds(out_row(r) * p.n_split + split, 1, n_rows * p.n_split, p.err))
         p.ws_ml[out_row(r) * p.n_split + split] = make_float2(-INFINITY, 0.f);
     return;
   }
   // (in a cluster an empty split still takes part: no tiles, partial (-inf, 0, 0))
-  const int t_end = min(t0 + p.chunk, L);
-  const int n_tiles = t_end > t0 ? (t_end - t0 + kTile - 1) / kTile : 0;
+  const int t_end = DYN ? L : min(t0 + p.chunk, L);
+  const int n_tiles = DYN ? n_static : (t_end > t0 ? (t_end - t0 + kTile - 1) / kTile : 0);
 
   const unsigned long long tp2 = trace_clock();
 
   // ------------------------------------------------------------ producer ----
+  if (DYN && warp == kCW) {
+    // Lane 0 runs the balanced producer: the CTA's own share, then claimed
+    // tiles until the pool is empty, then the closing stage.
+    if (lane == 0) {
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      // one row group per split: every K/V byte is read once
+      const uint64_t kv_pol = l2_policy_evict_first();
+      int* const ctr = p.tile_ctr + 2 * ((size_t)b * p.H_kv + kv);
+      const int pool0 = p.n_split * n_static;
+      const int n_pool = (L + kTile - 1) / kTile - pool0;  // >= 1: the share is below 3/4
+      // Ring position i may be filled once the consumers have released
+      // position i - NSTAGE (the abort flag is read only on the slow path).
+      auto slot_free = [&](int i) -> bool {
+        if (i < NSTAGE) return true;
+        const uint32_t eb = smem_u32(&empty_bar[i % NSTAGE]), par = ((i / NSTAGE) - 1) & 1;
+        if (mbar_try_wait(eb, par)) return true;
+        if (*reinterpret_cast<volatile int*>(&abort_flag) || !mbar_wait(eb, par, p.wait_ns, p.err)) {
+          *reinterpret_cast<volatile int*>(&abort_flag) = 1;
+          return false;
+        }
+        return true;
+      };
+      // Ring position i takes the tile that starts at token tok.  The stage's
+      // token is written before the barrier is armed (the arrive releases it
+      // to the consumers' wait).
+      auto load = [&](int i, int tok) {
+        const int st = i % NSTAGE;
+        stage_tok[st] = tok;
+        const uint32_t fb = smem_u32(&full_bar[st]);
+        mbar_arrive_expect_tx(fb, kTxBytes);
+        const uint32_t dst_k = smem_base + st * kStageBytes;
+        const int row = b * p.S_max + tok;  // rows past the end read as zeros (TMA fill)
+#pragma unroll
+        for (int blk = 0; blk < Lay::kBlocks; ++blk) {
+          tma_load_3d(dst_k + blk * Lay::kBlockBytes, &tm_k, fb, blk * Lay::kBox, kv, row, kv_pol);
+          tma_load_3d(dst_k + Lay::kTileBytes + blk * Lay::kBlockBytes, &tm_v, fb, blk * Lay::kBox,
+                      kv, row, kv_pol);
+        }
+      };
+      int issued = 0;
+      bool live = true;
+      for (; issued < n_static; ++issued) {
+        if (!slot_free(issued)) {
+          live = false;
+          break;
+        }
+        load(issued, t0 + issued * kTile);
+      }
+      if (live) {
+        int c = atomicAdd(ctr, 1);
+        while (c < n_pool) {
+          // the next claim travels while this tile waits for its slot
+          const int c_next = atomicAdd(ctr, 1);
+          if (!slot_free(issued)) {
+            live = false;
+            break;
+          }
+          load(issued, (pool0 + c) * kTile);
+          ++issued;
+          c = c_next;
+        }
+      }
+      // (see the contiguous producer below on the trigger's placement)
+      asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+      // No copy may still target this CTA's shared memory when it exits.
+      for (int i = max(0, issued - NSTAGE); i < issued; ++i)
+        mbar_wait(smem_u32(&full_bar[i % NSTAGE]), (i / NSTAGE) & 1, p.wait_ns, p.err);
+      // The closing stage: no copy, token -1.
+      if (live && slot_free(issued)) {
+        stage_tok[issued % NSTAGE] = -1;
+        mbar_arrive(smem_u32(&full_bar[issued % NSTAGE]));
+      }
+      // Count this CTA out.  Each CTA's claims are performed before its count
+      // (the fence orders them also when a claim's result went unused after
+      // an abort), so the last count ends every claim of this launch and the
+      // words can return to zero.
+      __threadfence();
+      if (atomicAdd(ctr + 1, 1) == p.n_split - 1) {
+        atomicExch(ctr, 0);
+        atomicExch(ctr + 1, 0);
+      }
+    }
+    __syncwarp();
+    return;
+  }
   if (warp == kCW) {
     const int page0 = PAGED ? t0 / p.page_size : 0;
     if (PAGED) {
@@ -582,7 +704,7 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
   const unsigned long long tp3 = trace_clock();
   const unsigned long long tr_loop0 = kTrace ? globaltimer_ns() : 0ull;
   unsigned long long tr_c[6] = {0, 0, 0, 0, trace_clock(), 0};  // wait, qk, softmax, pv, loop, tiles
-  for (int i = grp; i < n_tiles; i += NGRP) {
+  for (int i = grp; DYN || i < n_tiles; i += NGRP) {
     const int st = i % NSTAGE;
     const unsigned long long tc0 = trace_clock();
     // A stage that has landed passes at once; the abort flag is read only on
@@ -599,9 +721,14 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
       aborted = true;
       break;
     }
+    int tile_tok = t0 + i * kTile;
+    if constexpr (DYN) {
+      tile_tok = stage_tok[st];
+      if (tile_tok < 0) break;  // the closing stage (the same value in every lane)
+    }
     uint32_t kbase = smem_base + st * kStageBytes;
     uint32_t vbase = kbase + Lay::kTileBytes;
-    const int tok0 = t0 + i * kTile + ws * 16;  // first token of this warp's slice
+    const int tok0 = tile_tok + ws * 16;  // first token of this warp's slice
     float ksv[4], vsv[4];  // FP8: scales of this thread's 4 score columns
     if constexpr (FP8) {
       // Key order inside a warp's 16-key slice (FP8 only): the lane with
@@ -1191,13 +1318,13 @@ inline cudaError_t resident_ctas(const void* kern, int threads, int smem, int* c
   return cudaSuccess;
 }
 
-template <int D, bool ROWS16, int NSTAGE, bool PAGED, bool FP8, int NGRP = 1>
+template <int D, bool ROWS16, int NSTAGE, bool PAGED, bool FP8, int NGRP = 1, bool DYN = false>
 cudaError_t launch_split(const DecodeParams& p_in, const CUtensorMap& tm_k,
                          const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
                          const CUtensorMap& tm_vs, cudaStream_t stream) {
   constexpr int smem = decode_smem_bytes<D, NSTAGE, FP8>();
   constexpr int threads = (kConsumerWarps * NGRP + 1) * 32;
-  auto kern = gqa_decode_split_kernel<D, ROWS16, NSTAGE, PAGED, FP8, false, NGRP>;
+  auto kern = gqa_decode_split_kernel<D, ROWS16, NSTAGE, PAGED, FP8, false, NGRP, DYN>;
   static unsigned char done[64];
   static int resident[64];
   cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem, done);
@@ -1240,7 +1367,7 @@ inline cudaError_t sm_count(int* out) {
   return e;
 }
 
-template <int D, bool PAGED, bool FP8>
+template <int D, bool PAGED, bool FP8, bool DYN = false>
 cudaError_t launch_split_rows(const DecodeParams& p, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, const CUtensorMap& tm_ks,
                               const CUtensorMap& tm_vs, cudaStream_t stream) {
@@ -1271,23 +1398,23 @@ cudaError_t launch_split_rows(const DecodeParams& p, const CUtensorMap& tm_k,
     if (e != cudaSuccess) return e;
     if ((long long)p.n_split * p.n_rg * p.H_kv * p.B <= sms) {
       if (p.T_q * p.G > 8)
-        return launch_split<D, true, DEEP, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
-      return launch_split<D, false, DEEP, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+        return launch_split<D, true, DEEP, PAGED, FP8, 1, DYN>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+      return launch_split<D, false, DEEP, PAGED, FP8, 1, DYN>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
     }
   }
   if (p.T_q * p.G > 8)  // rows g + 8 are live (in the first row group at least)
-    return launch_split<D, true, NSTAGE, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
-  return launch_split<D, false, NSTAGE, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+    return launch_split<D, true, NSTAGE, PAGED, FP8, 1, DYN>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+  return launch_split<D, false, NSTAGE, PAGED, FP8, 1, DYN>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
 }
 
-template <bool PAGED, bool FP8>
+template <bool PAGED, bool FP8, bool DYN = false>
 cudaError_t launch_split_d(const DecodeParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const CUtensorMap& tm_ks, const CUtensorMap& tm_vs,
                            cudaStream_t stream) {
   switch (p.d) {
-    case 32: return launch_split_rows<32, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
-    case 64: return launch_split_rows<64, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
-    case 128: return launch_split_rows<128, PAGED, FP8>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+    case 32: return launch_split_rows<32, PAGED, FP8, DYN>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+    case 64: return launch_split_rows<64, PAGED, FP8, DYN>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
+    case 128: return launch_split_rows<128, PAGED, FP8, DYN>(p, tm_k, tm_v, tm_ks, tm_vs, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1373,6 +1500,10 @@ cudaError_t launch_comb_cols(const CombineParams& p, cudaStream_t stream) {
 
 cudaError_t launch_decode_split(const DecodeParams& p, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, cudaStream_t stream) {
+  if (p.tile_ctr) {
+    if (p.T_q != 1 || p.n_rg != 1 || p.n_split < 2) return cudaErrorInvalidValue;
+    return launch_split_d<false, false, true>(p, tm_k, tm_v, tm_k, tm_v, stream);
+  }
   return launch_split_d<false, false>(p, tm_k, tm_v, tm_k, tm_v, stream);
 }
 

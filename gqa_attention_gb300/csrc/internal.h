@@ -37,6 +37,9 @@ struct DecodeParams {
   // of the pools, page = block_table[b * max_blocks + t / page_size]
   const int32_t* block_table;
   int max_blocks, page_size, num_pages;
+  // Balanced splits (contiguous cache only): two int32 words per (sequence,
+  // KV head), zero before the launch and zero again after it; null otherwise.
+  int* tile_ctr;
   // Set by the launcher: K/V tiles each split CTA prefetches into L2 before
   // its dependency wait (0 = none; used only when the whole grid is resident
   // at once, so that the prefetch overlaps the previous kernel).

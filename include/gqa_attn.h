@@ -201,6 +201,39 @@ gqa_status gqa_attn_decode_paged_fp8(const void* q, const void* k_pool, const vo
                                      int H_kv, int d, float scale, int n_split, void* workspace,
                                      void* out, float* lse, gqa_stream_t stream);
 
+/* Split-KV decode with balanced splits ("Attention Kernel 계보", p.18 §4: the
+ * stage-1 / stage-2 split of the keys; the merge of p.4 §3-§9 does not depend
+ * on which keys a partial holds).  Fixed splits end at different times: the
+ * CTAs share the GPU's memory bandwidth unevenly, and the step waits for the
+ * slowest.  Here split s first streams its own share, 64-token tiles
+ * s*n_s .. s*n_s + n_s - 1 of its (sequence, KV head) with n_s =
+ * floor(3 * ceil(seq_lens[b] / 64) / (4 * n_split)); the remaining tiles (about a
+ * quarter) are then claimed one at a time by whichever split CTA of that
+ * (sequence, KV head) has room for the next tile.  A partial therefore holds
+ * a share of contiguous keys plus claimed tiles anywhere in the sequence.
+ *   counters  device int32 [B, H_kv, 2], gqa_attn_decode_counter_bytes()
+ *             bytes, 4-byte aligned, caller-owned.  All zero before the first
+ *             call; every call returns them to zero by the time its kernel
+ *             completes (also when a seq_lens entry is out of range or a wait
+ *             timed out), so they can serve the next call as they are.  Calls
+ *             that share one counter array must not overlap on the GPU.
+ * Every other argument, the workspace layout (one partial per split) and the
+ * follow-up gqa_attn_decode_combine() are those of gqa_attn_decode().  The
+ * result is that of gqa_attn_decode() up to rounding; since the claims depend
+ * on timing, two calls on the same inputs may differ in the last bits.
+ * n_split == 1 is exactly gqa_attn_decode() (counters unused, may be NULL).
+ * Measured on GB300 (split + combine, Llama3-70B heads): the ragged batch of 8
+ * sequences of 1K-128K tokens at 16 splits runs in 278.8 us against 283.1 us
+ * with fixed splits; the single 32K sequence at 19 splits gains nothing (23.74
+ * against 23.82 us), so gqa_attn_decode, which is deterministic, stays the
+ * choice there. */
+size_t gqa_attn_decode_counter_bytes(int B, int H_kv);
+gqa_status gqa_attn_decode_balanced(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* seq_lens, int B, int S_max, int H_q, int H_kv,
+                                    int d, float scale, int n_split, void* workspace,
+                                    int32_t* counters, void* out, float* lse,
+                                    gqa_stream_t stream);
+
 /* Split-KV decode that allocates nothing, for callers that cannot call
  * cudaMalloc when they decode: code running inside a custom allocator's
  * critical section (a nested allocation there would deadlock or recurse), or
