@@ -76,11 +76,27 @@ __device__ __forceinline__ void trace_ready(float& v) {
 constexpr int kTile = kDecodeTile;  // tokens per stage
 constexpr int kMaxClusterSplits = 16;
 constexpr int kConsumerWarps = 4;   // 16 tokens each
-#ifndef GQA_PREFETCH_TILES
-#define GQA_PREFETCH_TILES 6  // tiles a split CTA may warm in L2 before its dependency wait
+// K/V bytes a split CTA may warm in L2 before its dependency wait, in whole
+// tiles (at least one, at most kPrefetchMaxTiles).  Measured for the Llama3-70B
+// decode at 32K (step = split + combine, median of three processes per depth):
+// bf16 (32 KB tiles) 0/1/2/3/4/5/6/10/16 tiles 24.56/24.03/23.49/23.33/23.52/
+// 23.64/23.77/24.10/24.51 us; E4M3 (17 KB tiles) best at 4-6 tiles
+// (15.8-15.9 us), 17.9 us without.  A deeper prefetch fetches lines that this
+// grid's own stream and the step's partials evict before use.
+#ifndef GQA_PREFETCH_BYTES
+#define GQA_PREFETCH_BYTES 98304
 #endif
-constexpr int kPrefetchTiles = GQA_PREFETCH_TILES;
-static_assert(kPrefetchTiles >= 0 && kPrefetchTiles <= 32, "one tile per producer lane");
+#ifndef GQA_PREFETCH_MAX_TILES
+#define GQA_PREFETCH_MAX_TILES 6
+#endif
+constexpr int kPrefetchMaxTiles = GQA_PREFETCH_MAX_TILES;
+static_assert(kPrefetchMaxTiles >= 0 && kPrefetchMaxTiles <= 32, "one tile per producer lane");
+constexpr int prefetch_tiles(int stage_bytes) {
+  return GQA_PREFETCH_BYTES / stage_bytes < 1 ? (kPrefetchMaxTiles > 0 ? 1 : 0)
+         : GQA_PREFETCH_BYTES / stage_bytes > kPrefetchMaxTiles
+             ? kPrefetchMaxTiles
+             : GQA_PREFETCH_BYTES / stage_bytes;
+}
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
 // Balanced splits: each split CTA first streams a fixed share of about three
@@ -1336,7 +1352,9 @@ cudaError_t launch_split(const DecodeParams& p_in, const CUtensorMap& tm_k,
   // The L2 prefetch pays only when every CTA is resident while the previous
   // kernel drains; a CTA of a later wave would prefetch what it loads next.
   const long long ctas = (long long)p.n_split * p.n_rg * p.H_kv * p.B;
-  p.prefetch_tiles = ctas <= fit ? kPrefetchTiles : 0;
+  constexpr int kPf =
+      prefetch_tiles(FP8 ? Fp8Layout<D>::kTxBytes : DecodeLayout<D>::kStageBytes);
+  p.prefetch_tiles = ctas <= fit ? kPf : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_split * p.n_rg, p.H_kv, p.B);
   cfg.blockDim = dim3(threads);
