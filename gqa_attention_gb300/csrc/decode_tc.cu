@@ -47,6 +47,10 @@ namespace {
 
 constexpr int kTcThreads = 192;
 constexpr int kTcSlots = 3;                     // slots per ring (K and V)
+#ifndef GQA_TC_PREFETCH_TILES
+#define GQA_TC_PREFETCH_TILES 3  // 128-key tiles a CTA may warm in L2 before its dependency wait
+#endif
+static_assert(GQA_TC_PREFETCH_TILES >= 0 && GQA_TC_PREFETCH_TILES <= 32, "one tile per lane");
 constexpr int kTcKeys = 128;                    // keys per ring stage
 constexpr uint32_t kTileB = 128u * 128u * 2u;   // one 128 x 128 bf16 tile
 constexpr uint32_t kHalfB = kTileB / 2;         // 128 rows x 128 bytes
@@ -564,7 +568,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p_in, const CUtensorMap& tm_q,
   // while the previous kernel drains.
   const long long ctas = (long long)p.n_split * p.H_kv * p.B;
   const int sms = (dev >= 0 && dev < 64) ? sm_count[dev] : 0;
-  p.prefetch_tiles = (!p.block_table && ctas <= sms) ? kTcSlots : 0;
+  p.prefetch_tiles = (!p.block_table && ctas <= sms) ? GQA_TC_PREFETCH_TILES : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_split, p.H_kv, p.B);
   cfg.blockDim = dim3(kTcThreads);

@@ -35,8 +35,10 @@
  * Which call for which workload (measured on GB300, Llama3-70B heads, 32K cache)
  * -------------------------------------------------------------------------
  * - One new token per sequence, contiguous cache: gqa_attn_decode with
- *   gqa_attn_decode_default_splits, then gqa_attn_decode_combine (23.3-23.8 us
- *   per step; the split kernel streams K/V at 95-97% of the measured HBM rate).
+ *   gqa_attn_decode_default_splits, then gqa_attn_decode_combine (23.0-23.3 us
+ *   per step; the split kernel streams K/V at 98-99% of the measured HBM rate).
+ *   Several sequences of very different lengths: gqa_attn_decode_balanced
+ *   (+ combine), whose splits share each sequence's last quarter of tiles.
  * - The same over a paged cache: gqa_attn_decode_paged (+ combine).
  * - An E4M3 cache with per-token scales: gqa_attn_decode_fp8 /
  *   gqa_attn_decode_paged_fp8 (+ combine) with 3x the default split count
