@@ -179,3 +179,22 @@ def test_combine_routes(oracle_mod, B, H_q, H_kv, d, n_split):
     ref_o, ref_l = oracle_mod.decode(q, k, v, sl, 1 / math.sqrt(d))
     out, lse = _run(q, k, v, sl, n_split)
     assert_parity(out, lse, ref_o, ref_l, f"B={B} d={d} n_split={n_split}")
+
+
+@pytest.mark.parametrize("d", [32, 64])
+@pytest.mark.parametrize("G,ctx", [(4, 5000), (8, 1024), (16, 131), (1, 3)])
+def test_small_grid_and_full_grid_paths(oracle_mod, d, G, ctx):
+    """The same sequence alone (2 CTAs, every CTA resident at once: the L2
+    prefetch across the dependency wait is on) and as every member of a batch of
+    160 (more CTAs than fit at once: the prefetch is off), against the oracle."""
+    H_kv = 2
+    q, k, v, lens = inputs.decode_inputs(1, G * H_kv, H_kv, d, ctx, seed=d + G + ctx)
+    ref_o, ref_l = oracle_mod.decode(q, k, v, lens, 1 / math.sqrt(d))
+    small_o, small_l = _run(q, k, v, lens, 1)  # 2 CTAs
+    assert_parity(small_o, small_l, ref_o, ref_l, f"small grid d={d} G={G} ctx={ctx}")
+    B = 160  # 320 CTAs: more than two per SM
+    qb, kb, vb, lb = (x.expand(B, *x.shape[1:]).contiguous() for x in (q, k, v, lens))
+    big_o, big_l = _run(qb, kb, vb, lb, 1)
+    for b in (0, B - 1):
+        assert_parity(big_o[b:b + 1], big_l[b:b + 1], ref_o, ref_l,
+                      f"full grid d={d} G={G} ctx={ctx} b={b}")
