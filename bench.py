@@ -342,7 +342,7 @@ def _repeat_stats(ms_list):
 class DecodeLeg:
     """A decode workload: split kernel (+ combine when split) over rotating cache copies."""
 
-    def __init__(self, torch, g, cfg, dev, seed=0, balanced=False):
+    def __init__(self, torch, g, cfg, dev, seed=0, balanced=False, n_split=None):
         from gqa_attention_gb300 import inputs
 
         self.torch, self.g, self.cfg, self.dev = torch, g, cfg, dev
@@ -359,7 +359,8 @@ class DecodeLeg:
         self.kall.copy_(kd.unsqueeze(0).expand_as(self.kall))
         self.vall.copy_(vd.unsqueeze(0).expand_as(self.vall))
         del kd, vd
-        self.n_split = g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, dev.index)
+        self.n_split = (n_split if n_split is not None else
+                        g.gqa_attn_decode_default_splits(cfg.B, cfg.H_kv, cfg.S_max, dev.index))
         self.ws = g.decode_workspace(cfg.B, cfg.H_q, cfg.d, self.n_split, dev)
         # balanced splits: the claim counters, zeroed once (every call leaves them at zero)
         self.counters = (g.decode_counters(cfg.B, cfg.H_kv, dev)
@@ -511,18 +512,20 @@ def run_ours(args, rank, world, dist):
     want_configs = args.only is None and not args.no_configs
 
     # ---------------- workloads ----------------
-    dec = DecodeLeg(torch, g, inputs.LLAMA70B_DECODE, dev) if want_decode else None
-    pre = PrefillLeg(torch, g, inputs.LLAMA70B_PREFILL_8K, dev) if want_prefill else None
+    seed = args.seed
+    dec = (DecodeLeg(torch, g, inputs.LLAMA70B_DECODE, dev, seed=seed, n_split=args.splits)
+           if want_decode else None)
+    pre = PrefillLeg(torch, g, inputs.LLAMA70B_PREFILL_8K, dev, seed=seed) if want_prefill else None
     extra = {}
     if want_configs:
         # (the power-heavy 64K prefill last: the compute-bound FP8 decode is
         # sensitive to the clocks a long prefill leaves behind)
-        extra["decode_tiny"] = DecodeLeg(torch, g, inputs.TINY_DECODE, dev)
+        extra["decode_tiny"] = DecodeLeg(torch, g, inputs.TINY_DECODE, dev, seed=seed)
         # (the ragged batch through the balanced splits: 1.5% faster than fixed ones)
         extra["decode_ragged"] = DecodeLeg(torch, g, inputs.LLAMA70B_DECODE_RAGGED, dev,
-                                           balanced=True)
-        extra["decode_fp8"] = Fp8DecodeLeg(torch, g, inputs.LLAMA70B_DECODE, dev)
-        extra["prefill_64k"] = PrefillLeg(torch, g, inputs.PREFILL_64K, dev)
+                                           seed=seed, balanced=True)
+        extra["decode_fp8"] = Fp8DecodeLeg(torch, g, inputs.LLAMA70B_DECODE, dev, seed=seed)
+        extra["prefill_64k"] = PrefillLeg(torch, g, inputs.PREFILL_64K, dev, seed=seed)
     legs = [x for x in (dec, pre, *extra.values()) if x is not None]
 
     # one eager call of each workload (library set-up happens outside any capture)
@@ -782,6 +785,7 @@ def run_ours(args, rank, world, dist):
                           "hbm_frac_of_" + peak_kind: dr["frac_of_" + peak_kind + "_hbm"],
                           "hbm_frac_of_nominal_8TBs": dr["frac_of_nominal_8TBs"]}) if dr else None,
             "prefill": {k: pr[k] for k in ("B", "S", "H_q", "H_kv", "d")} if pr else None,
+            "seed": args.seed,
             "l2": "decode: rotating K/V copies, a copy is read again only after >= 1.5 GiB "
                   "(12 x L2) of other cache reads; prefill inputs exceed L2",
             "timing": ("each workload: one CUDA graph holding an untimed lead-in of the same "
@@ -933,7 +937,7 @@ def run_reference(args, rank, world):
 
     oracle.build()
     dc = inputs.LLAMA70B_DECODE
-    q, k, v, lens = inputs.decode_inputs_for(dc, seed=0)
+    q, k, v, lens = inputs.decode_inputs_for(dc, seed=args.seed)
     kv_bytes = 2 * int(lens.sum()) * dc.H_kv * dc.d * 2
     cores = os.cpu_count() or 1
     for _ in range(args.warmup):
@@ -1387,6 +1391,18 @@ def run_workload(name, args):
             "data": "synthetic"}
 
 
+def emit(line, args, name):
+    """Print the JSON line; with --results-dir also write it to
+    <dir>/<name>_<UTC time>.json."""
+    text = json.dumps(line)
+    print(text, flush=True)
+    if args.results_dir:
+        os.makedirs(args.results_dir, exist_ok=True)
+        stamp = time.strftime("%Y%m%dT%H%M%SZ", time.gmtime())
+        with open(os.path.join(args.results_dir, f"{name}_{stamp}.json"), "w") as f:
+            f.write(text + "\n")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1402,7 +1418,17 @@ def main():
     ap.add_argument("--only", choices=["decode", "prefill"], default=None,
                     help="run one leg of the headline step only (for profiler captures); "
                          "the JSON line is partial")
+    ap.add_argument("--seed", type=int, default=0,
+                    help="seed of the synthetic inputs of the headline step, its configs and "
+                         "the reference arm (the oracle parity uses the same inputs)")
+    ap.add_argument("--splits", type=int, default=None,
+                    help="split count of the headline decode (default: "
+                         "gqa_attn_decode_default_splits)")
+    ap.add_argument("--results-dir", default=None,
+                    help="also write the JSON line to a file in this directory")
     args = ap.parse_args()
+    if args.splits is not None and args.splits < 1:
+        ap.error("--splits must be >= 1")
     if args.warmup < 3:
         args.warmup = 3
     args.steps = max(1, args.steps)
@@ -1412,13 +1438,12 @@ def main():
     dist = None
     if args.workload is not None:
         if rank == 0:
-            print(json.dumps(run_workload(args.workload, args)), flush=True)
+            emit(run_workload(args.workload, args), args, args.workload)
         return 0
     if args.impl == "reference":
         if world > 1 and rank != 0:
             return 0
-        line = run_reference(args, rank, world)
-        print(json.dumps(line), flush=True)
+        emit(run_reference(args, rank, world), args, "reference")
         return 0
     if world > 1:
         import torch
@@ -1433,7 +1458,7 @@ def main():
         if dist is not None:
             dist.destroy_process_group()
     if rank == 0 and line is not None:
-        print(json.dumps(line), flush=True)
+        emit(line, args, "step" if args.only is None else args.only)
     return 0
 
 
