@@ -966,7 +966,87 @@ def run_reference(args, rank, world):
 WORKLOADS = ("decode_tiny", "decode_ragged", "decode_paged16", "decode_paged128", "decode_fp8",
              "decode_fp8_ragged", "decode_multi2", "decode_multi4", "decode_multi8", "decode_multi16",
              "decode_paged16_multi8", "decode_paged128_multi8", "prefill_64k", "prefill_window",
-             "prefill_chunk", "prefill_d64", "prefill_d32", "decode_trace", "prefill_trace", "mma_rate")
+             "prefill_chunk", "prefill_d64", "prefill_d32", "decode_trace", "prefill_trace", "mma_rate",
+             "decode_shapes")
+
+# Serving shapes of the Llama3-70B heads (B sequences of S tokens) for the
+# decode_shapes sweep of the default split count, fixed and balanced.
+SERVING_SHAPES = ((4, 32768), (16, 8192), (64, 4096), (16, 32768), (64, 8192), (2, 131072),
+                  (32, 2048), (128, 1024))
+
+
+def run_decode_shapes(args):
+    """Decode step (split + combine) of each serving shape with the library's default
+    split count, through gqa_attn_decode and gqa_attn_decode_balanced: K steps in a
+    CUDA graph over rotating cache copies (>= 1.5 GiB), median of 5 replays.  The
+    inputs are drawn on the device from a seeded generator (a throughput sweep: the
+    kernels' parity is the tests' job)."""
+    import torch
+
+    import gqa_attention_gb300 as g
+    from gqa_attention_gb300 import inputs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    g.load()
+    stream = torch.cuda.current_stream()
+    hbm_gbs, _, _, peak_kind = _peaks()
+    timer = GraphTimer(torch, stream, None)
+    gen = torch.Generator(device=dev).manual_seed(args.seed)
+    cfg = inputs.LLAMA70B_DECODE
+    H_q, H_kv, d, scale = cfg.H_q, cfg.H_kv, cfg.d, cfg.scale
+    steps = max(1, args.steps)
+    shapes = {}
+    for B, S in SERVING_SHAPES:
+        kv_bytes = 4 * d * H_kv * B * S
+        copies = n_copies(kv_bytes)
+        q = torch.randn(B, H_q, d, device=dev, generator=gen).to(torch.bfloat16)
+        ks = [torch.randn(B, S, H_kv, d, device=dev, generator=gen).to(torch.bfloat16)
+              for _ in range(copies)]
+        vs = [torch.randn(B, S, H_kv, d, device=dev, generator=gen).to(torch.bfloat16)
+              for _ in range(copies)]
+        lens = torch.full((B,), S, dtype=torch.int32, device=dev)
+        n = g.gqa_attn_decode_default_splits(B, H_kv, S, dev.index)
+        ws = g.decode_workspace(B, H_q, d, n, dev)
+        ctr = g.decode_counters(B, H_kv, dev)
+        out = torch.empty(B, H_q, d, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(B, H_q, dtype=torch.float32, device=dev)
+        row = {"B": B, "S": S, "n_split": n, "kv_bytes": kv_bytes, "copies": copies}
+        for mode in ("fixed", "balanced"):
+            if mode == "balanced" and n < 2:
+                continue
+
+            def step(i, s, mode=mode):
+                j = i % copies
+                if mode == "fixed":
+                    st = g.gqa_attn_decode(q, ks[j], vs[j], lens, B, S, H_q, H_kv, d, scale, n,
+                                           ws, out, lse, s)
+                else:
+                    st = g.gqa_attn_decode_balanced(q, ks[j], vs[j], lens, B, S, H_q, H_kv, d,
+                                                    scale, n, ws, ctr, out, lse, s)
+                if st == g.GQA_OK and n > 1:
+                    st = g.gqa_attn_decode_combine(ws, B, H_q, d, n, out, lse, s)
+                if st:
+                    raise RuntimeError(f"decode failed: {g.status_str(st)}")
+
+            for i in range(copies):
+                step(i, stream)
+            torch.cuda.synchronize()
+            tg = timer.prepare(step, steps, copies, lead_out=1)
+            timer.warm(tg)
+            ms = statistics.median(timer.time(tg) for _ in range(REPEATS))
+            gbs = kv_bytes / (ms * 1e-3) / 1e9
+            row[mode] = {"us_per_step": round(ms * 1e3, 2), "GBs": round(gbs, 1),
+                         "frac_of_" + peak_kind + "_hbm": round(gbs / hbm_gbs, 4)}
+        if g.gqa_last_device_error(stream) != g.GQA_OK or not bool(torch.isfinite(out.float()).all()):
+            raise RuntimeError(f"decode B={B} S={S}: device error or non-finite output")
+        shapes[f"B{B}_S{S}"] = row
+        del ks, vs
+        torch.cuda.empty_cache()
+    return {"metric": "decode KV GB/s over serving shapes (Llama3-70B heads, default splits)",
+            "unit": "GB/s", "steps": steps, "shapes": shapes, "dtype": "bf16",
+            "data": "synthetic (seeded device generator)",
+            "timing": "K steps in a CUDA graph over rotating copies, median of 5 replays"}
 
 
 def _shuffled_pages(k, v, page_size, seed):
@@ -1146,6 +1226,8 @@ def run_workload(name, args):
         return run_decode_trace(args)
     if name == "mma_rate":
         return run_mma_rate(args)
+    if name == "decode_shapes":
+        return run_decode_shapes(args)
     if name == "prefill_trace":
         return run_prefill_trace(args)
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
