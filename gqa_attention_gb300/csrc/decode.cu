@@ -455,7 +455,9 @@ __global__ void __launch_bounds__((kConsumerWarps * NGRP + 1) * 32,
         const uint32_t fb = smem_u32(&full_bar[st]);
         mbar_arrive_expect_tx(fb, kTxBytes);
         const uint32_t dst_k = smem_base + st * kStageBytes;
-        const int row = b * p.S_max + tok;  // rows past the end read as zeros (TMA fill)
+        // (rows past the sequence end are masked by the consumers; past the
+        // last sequence the copy fills zeros)
+        const int row = b * p.S_max + tok;
 #pragma unroll
         for (int blk = 0; blk < Lay::kBlocks; ++blk) {
           tma_load_3d(dst_k + blk * Lay::kBlockBytes, &tm_k, fb, blk * Lay::kBox, kv, row, kv_pol);
