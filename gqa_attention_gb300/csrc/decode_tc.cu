@@ -129,21 +129,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
   }
   // While the previous kernel finishes, the producer warp prefetches this
-  // split's first K/V tiles into L2, one tile per lane (the launcher enables
-  // it when the whole grid is resident at once).  The extent comes from a
-  // relaxed load of seq_lens[b], which may see the value from before the
-  // previous kernel's writes and only sizes the prefetch; a prefetch hands no
-  // data to the kernel and L2 is where writes become coherent.
-  if (!PAGED && warp == 0 && lane < p.prefetch_tiles) {
+  // split's first K/V tiles into L2, one tile (paged: one page segment of a
+  // tile) per lane; the launcher enables it when the whole grid is resident at
+  // once.  The extent comes from a relaxed load of seq_lens[b] and, for a
+  // paged cache, the rows from relaxed loads of the block table; they may see
+  // values from before the previous kernel's writes and only aim the prefetch
+  // (an index outside the pool is skipped).  A prefetch hands no data to the
+  // kernel and L2 is where writes become coherent.
+  if (warp == 0 && p.prefetch_tiles > 0) {
+    const int h = PAGED ? min(p.page_size, kTcKeys) : kTcKeys;  // rows per box
+    const int nb = kTcKeys / h;
+    const int i = lane / nb, sub = lane % nb;
     int L_hint;
     asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(L_hint) : "l"(p.seq_lens + b));
-    const int tk = split * p.chunk + lane * kTcKeys;
-    if (tk < min(min(p.S_max, L_hint), split * p.chunk + p.chunk)) {
-      const int row = b * p.S_max + tk;
-      for (int dh = 0; dh < 2; ++dh) {
-        tma_prefetch_l2_3d(&tm_k, dh * 64, kv, row);
-        tma_prefetch_l2_3d(&tm_v, dh * 64, kv, row);
+    const int tk = split * p.chunk + i * kTcKeys + sub * h;
+    if (i < p.prefetch_tiles && tk < min(min(p.S_max, L_hint), split * p.chunk + p.chunk)) {
+      int row = b * p.S_max + tk;
+      bool ok = true;
+      if constexpr (PAGED) {
+        int pg;
+        asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];"
+                     : "=r"(pg)
+                     : "l"(p.block_table + (size_t)b * p.max_blocks + tk / p.page_size));
+        ok = pg >= 0 && pg < p.num_pages;
+        row = pg * p.page_size + tk % p.page_size;
       }
+      if (ok)
+        for (int dh = 0; dh < 2; ++dh) {
+          tma_prefetch_l2_3d(&tm_k, dh * 64, kv, row);
+          tma_prefetch_l2_3d(&tm_v, dh * 64, kv, row);
+        }
     }
   }
 
@@ -565,10 +580,14 @@ cudaError_t launch_decode_tc(const DecodeParams& p_in, const CUtensorMap& tm_q,
   }
   DecodeParams p = p_in;
   // One CTA per SM: the L2 prefetch pays only when every CTA is resident
-  // while the previous kernel drains.
+  // while the previous kernel drains, and for a paged cache only with pages
+  // of at least 64 tokens (T_q = 8, Llama3-70B 32K: 28.9 -> 26.5 us at page
+  // 128, but 32.8 -> 34.3 us at page 16, whose 24 small boxes per CTA cost
+  // more than they hide).
   const long long ctas = (long long)p.n_split * p.H_kv * p.B;
   const int sms = (dev >= 0 && dev < 64) ? sm_count[dev] : 0;
-  p.prefetch_tiles = (!p.block_table && ctas <= sms) ? GQA_TC_PREFETCH_TILES : 0;
+  const bool small_pages = p.block_table && p.page_size < 64;
+  p.prefetch_tiles = (ctas <= sms && !small_pages) ? GQA_TC_PREFETCH_TILES : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_split, p.H_kv, p.B);
   cfg.blockDim = dim3(kTcThreads);
