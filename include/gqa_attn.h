@@ -219,6 +219,7 @@ gqa_status gqa_attn_decode_paged_fp8(const void* q, const void* k_pool, const vo
  *             completes (also when a seq_lens entry is out of range or a wait
  *             timed out), so they can serve the next call as they are.  Calls
  *             that share one counter array must not overlap on the GPU.
+ *             NULL or misaligned with n_split > 1: GQA_ERR_INVALID_ARG.
  * Every other argument, the workspace layout (one partial per split) and the
  * follow-up gqa_attn_decode_combine() are those of gqa_attn_decode().  The
  * result is that of gqa_attn_decode() up to rounding; since the claims depend
@@ -226,9 +227,10 @@ gqa_status gqa_attn_decode_paged_fp8(const void* q, const void* k_pool, const vo
  * n_split == 1 is exactly gqa_attn_decode() (counters unused, may be NULL).
  * Measured on GB300 (split + combine, Llama3-70B heads): the ragged batch of 8
  * sequences of 1K-128K tokens at 16 splits runs in 278.8 us against 283.1 us
- * with fixed splits; the single 32K sequence at 19 splits gains nothing (23.74
- * against 23.82 us), so gqa_attn_decode, which is deterministic, stays the
- * choice there. */
+ * with fixed splits, 2 sequences of 128K tokens in 150.9 against 156.2 us; the
+ * single 32K sequence at 19 splits gains nothing (23.74 against 23.82 us), nor
+ * do batches of 8K-32K sequences, so gqa_attn_decode, which is deterministic,
+ * stays the choice there. */
 size_t gqa_attn_decode_counter_bytes(int B, int H_kv);
 gqa_status gqa_attn_decode_balanced(const void* q, const void* k_cache, const void* v_cache,
                                     const int32_t* seq_lens, int B, int S_max, int H_q, int H_kv,
