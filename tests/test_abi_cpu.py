@@ -137,3 +137,19 @@ def test_trace_calls_are_unsupported_in_the_default_build(lib):
     assert g.gqa_trace_read(buf, buf.nbytes) == g.GQA_ERR_UNSUPPORTED
     assert g.gqa_trace_mma_rate(0, 1)[0] == g.GQA_ERR_UNSUPPORTED
     assert g.gqa_trace_prefill_read(buf, buf.nbytes) == g.GQA_ERR_UNSUPPORTED
+
+
+def test_balanced_decode_counters_and_checks(lib):
+    # two int32 words per (sequence, KV head)
+    assert g.gqa_attn_decode_counter_bytes(3, 8) == 3 * 8 * 2 * 4
+    assert g.gqa_attn_decode_counter_bytes(0, 8) == 0
+    assert g.gqa_attn_decode_counter_bytes(2, -1) == 0
+    # with several splits the counters are required and 4-byte aligned; both
+    # checks fail before anything reaches the GPU
+    args = (FAKE, FAKE, FAKE, FAKE, 1, 4096, 64, 8, 128, 0.1, 19, FAKE)
+    assert g.gqa_attn_decode_balanced(*args, None, FAKE, FAKE, stream=0) == g.GQA_ERR_INVALID_ARG
+    assert g.gqa_attn_decode_balanced(*args, FAKE + 2, FAKE, FAKE, stream=0) == \
+        g.GQA_ERR_INVALID_ARG
+    # the shared argument checks of gqa_attn_decode apply as well
+    bad = (FAKE, FAKE, FAKE, FAKE, 1, 4096, 12, 8, 128, 0.1, 19, FAKE)  # H_q % H_kv != 0
+    assert g.gqa_attn_decode_balanced(*bad, FAKE, FAKE, FAKE, stream=0) == g.GQA_ERR_INVALID_ARG
